@@ -1,0 +1,142 @@
+"""Float64 CPU oracle for the batched temperature -> min-p -> top-k -> top-p -> sample chain.
+
+TEST INFRASTRUCTURE. Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU
+baseline may import this package. The product (``nucleus_token_sampler_gb300``) never imports it
+and shares no code with it.
+
+The arithmetic lives in ``tps_oracle.c`` (plain C, float64, no fast-math, no FMA contraction);
+this module only builds it with gcc and marshals numpy arrays through ctypes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "tps_oracle.c")
+_LIB = os.path.join(_HERE, "libtps_oracle.so")
+_lock = threading.Lock()
+_default = None
+
+ROW_OK, ROW_NAN, ROW_ALL_MASKED, ROW_BAD_PARAM = 0, 1, 2, 3
+FLAG_TOPP_BAND, FLAG_MINP_BAND, FLAG_RACE_BAND = 1, 2, 4
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
+    """Compile the oracle (gcc, OpenMP, float64, -ffp-contract=off) into a shared library."""
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           "-fno-fast-math", "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+class Oracle:
+    """ctypes view of one build of the oracle library (the default build, or a test's variant)."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        P = ctypes.c_void_p
+        lib.tpso_sample.restype = ctypes.c_int
+        lib.tpso_sample.argtypes = [P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P, P, P, P, P,
+                                    P, ctypes.c_uint64, P, P, P, P, P, P, P, ctypes.c_int]
+        lib.tpso_uniform.restype = ctypes.c_double
+        lib.tpso_uniform.argtypes = [ctypes.c_uint64] * 4
+        lib.tpso_philox4x32_10.restype = None
+        lib.tpso_philox4x32_10.argtypes = [P, P, P]
+        lib.tpso_max_threads.restype = ctypes.c_int
+        self.lib = lib
+        self.path = lib_path
+
+    def sample(self, z, temperature, top_k, top_p, min_p, seed, step=0, *, row_ids=None,
+               want_probs=False, nthreads=0):
+        """Run the oracle on a [B, V] array of logits (widened exactly to float64).
+
+        ``temperature``, ``top_p`` and ``min_p`` are rounded to float32 first (the values the GPU
+        receives) and then widened, so both sides see the same numbers.  Returns a dict of numpy
+        arrays: token, status, cutoff, kept, flags, z_s, z_k, n_s (+ probs when asked).
+        """
+        z = np.ascontiguousarray(np.asarray(z, dtype=np.float64))
+        if z.ndim != 2:
+            raise ValueError("z must be [B, V]")
+        B, V = z.shape
+
+        def vec(x, dt):
+            return np.ascontiguousarray(np.broadcast_to(np.asarray(x), (B,)).astype(dt))
+
+        T = vec(np.asarray(temperature, dtype=np.float32), np.float64)
+        P = vec(np.asarray(top_p, dtype=np.float32), np.float64)
+        M = vec(np.asarray(min_p, dtype=np.float32), np.float64)
+        K = vec(top_k, np.int32)
+        S = vec(np.asarray(seed).astype(np.uint64), np.uint64)
+        R = None if row_ids is None else vec(row_ids, np.int64)
+        out = {
+            "token": np.empty(B, np.int32),
+            "status": np.empty(B, np.int32),
+            "cutoff": np.empty(B, np.float64),
+            "kept": np.empty(B, np.int32),
+            "flags": np.empty(B, np.int32),
+        }
+        aux = np.empty((B, 3), np.float64)
+        probs = np.empty((B, V), np.float64) if want_probs else None
+        rc = self.lib.tpso_sample(_ptr(z), B, V, V, _ptr(T), _ptr(K), _ptr(P), _ptr(M), _ptr(S),
+                                  _ptr(R), int(step) & ((1 << 64) - 1), _ptr(out["token"]),
+                                  _ptr(probs), _ptr(out["status"]), _ptr(out["cutoff"]),
+                                  _ptr(out["kept"]), _ptr(out["flags"]), _ptr(aux), int(nthreads))
+        if rc != 0:
+            raise MemoryError("oracle scratch allocation failed")
+        out["z_s"], out["z_k"], out["n_s"] = aux[:, 0].copy(), aux[:, 1].copy(), aux[:, 2].copy()
+        if want_probs:
+            out["probs"] = probs
+        return out
+
+    def uniform(self, seed: int, row: int, step: int, token: int) -> float:
+        """The race's uniform u in (0, 1) for (seed, row, step, token)."""
+        m = (1 << 64) - 1
+        return self.lib.tpso_uniform(seed & m, row & m, step & m, token & m)
+
+    def philox4x32_10(self, counter, key):
+        """One Philox4x32-10 block: counter = 4 x uint32, key = 2 x uint32 -> 4 x uint32."""
+        c = np.ascontiguousarray(np.asarray(counter, dtype=np.uint32))
+        k = np.ascontiguousarray(np.asarray(key, dtype=np.uint32))
+        o = np.empty(4, np.uint32)
+        self.lib.tpso_philox4x32_10(_ptr(c), _ptr(k), _ptr(o))
+        return o
+
+    def max_threads(self) -> int:
+        return int(self.lib.tpso_max_threads())
+
+
+def default() -> Oracle:
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+    return _default
+
+
+def sample(*args, **kwargs):
+    return default().sample(*args, **kwargs)
+
+
+def uniform(seed: int, row: int, step: int, token: int) -> float:
+    return default().uniform(seed, row, step, token)
+
+
+def philox4x32_10(counter, key):
+    return default().philox4x32_10(counter, key)
+
+
+def max_threads() -> int:
+    return default().max_threads()
