@@ -1,0 +1,387 @@
+"""Benchmark: batched token sampling throughput on one GB300 (and N GPUs as independent row shards).
+
+Workload (default): a decode batch of B=1024 rows x V=128,256 float32 logits ~ N(0, 2.5^2) with a
+20-token head raised by +6; every row T=0.7, top_k=50, top_p=0.9, min_p=0.05, distinct seeds; the
+step counter advances each iteration.  One step = one call of the sampler over the whole batch.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU oracle instead, on the
+host cores, over a bounded sample of the same rows.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "rows/s & HBM GB/s (% of peak) at B=1024 V=128256 fp32; p50 us at B=1"
+UNIT = "rows/s"
+ROW_PARAM_BYTES = 4 + 4 + 4 + 4 + 8 + 4  # T, top_k, top_p, min_p, seed, token out
+KERNEL_SOURCES = ["nucleus_token_sampler_gb300/csrc/tps_kernel.cuh",
+                  "nucleus_token_sampler_gb300/csrc/tps_device.cuh",
+                  "nucleus_token_sampler_gb300/csrc/tps_api.cu"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--B", type=int, default=1024)
+    ap.add_argument("--V", type=int, default=128256)
+    ap.add_argument("--dtype", default="f32", choices=["f32", "bf16"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "sweep", "mixed", "ties_masked", "small"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-latency", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def committed_traffic(workload_tag: str):
+    """ncu DRAM bytes per launch for this kernel source and workload, if a capture was committed."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    e = d.get(workload_tag)
+    if not e or e.get("kernel_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def make_workload(args, device, seed=0):
+    from nucleus_token_sampler_gb300 import workloads
+    dt = torch.float32 if args.dtype == "f32" else torch.bfloat16
+    if args.workload == "decode":
+        return workloads.make("decode", device=device, seed=seed, B=args.B, V=args.V, dtype=dt)
+    if args.workload == "sweep":
+        return workloads.make("sweep", device=device, seed=seed, B=args.B, V=args.V, dtype=dt)
+    return workloads.make(args.workload, device=device, seed=seed)
+
+
+def cpu_baseline(w_cpu, rows_target_s=10.0, max_rows=512):
+    """Time the float64 oracle on the host cores over a bounded sample of rows; rows/s."""
+    import oracle
+    o = oracle.default()
+    cores = o.max_threads()
+    B = w_cpu.B
+    n = 1
+    spent = 0.0
+    done = 0
+    # grow the sample until ~rows_target_s of CPU work or max_rows
+    while done < max_rows and spent < rows_target_s:
+        rows = np.arange(done, min(done + n, B))
+        if len(rows) == 0:
+            break
+        t0 = time.perf_counter()
+        o.sample(w_cpu.logits[rows].double().numpy(), w_cpu.temperature[rows].numpy(), w_cpu.top_k[rows].numpy(),
+                 w_cpu.top_p[rows].numpy(), w_cpu.min_p[rows].numpy(),
+                 w_cpu.seed[rows].numpy().astype(np.uint64), w_cpu.step, row_ids=rows)
+        spent += time.perf_counter() - t0
+        done += len(rows)
+        n = min(2 * n, max_rows)
+    return {"value": done / spent, "unit": "rows/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} of {B} rows of the same workload, float64 oracle, OpenMP over rows ({spent:.1f} s)"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    o = oracle.default()
+    w = make_workload(args, "cpu")
+    # each step: a bounded sample of rows (sized so the whole run stays within a few minutes)
+    per_step = max(1, min(args.B, 16))
+    times = []
+    total_steps = args.warmup + args.steps
+    for it in range(total_steps):
+        rows = (np.arange(per_step) + it * per_step) % args.B
+        t0 = time.perf_counter()
+        o.sample(w.logits[rows].double().numpy(), w.temperature[rows].numpy(), w.top_k[rows].numpy(),
+                 w.top_p[rows].numpy(), w.min_p[rows].numpy(), w.seed[rows].numpy().astype(np.uint64), it,
+                 row_ids=rows)
+        if it >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    secs = sum(times)
+    value = per_step * len(times) / secs
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(args),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": o.max_threads(), "kind": "oracle",
+                         "sample": f"{per_step} rows per step of the {args.B}-row workload, float64 oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(args):
+    return {"workload": f"{args.workload}_b{args.B}_v{args.V}_{args.dtype}", "B": args.B, "V": args.V,
+            "logits_dtype": args.dtype, "params": "T=0.7 top_k=50 top_p=0.9 min_p=0.05" if args.workload == "decode"
+            else args.workload, "parallelism": "rows sharded over ranks (replicas, no collective)",
+            "l2": "inputs larger than L2 (no flush): %.0f MB of logits per step per GPU" % (
+                args.B * args.V * (4 if args.dtype == "f32" else 2) / 1e6)}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    import nucleus_token_sampler_gb300 as tps
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    tps.load()
+
+    w = make_workload(args, dev, seed=rank)
+    B, V = w.B, w.V
+    es = 4 if args.dtype == "f32" else 2
+    stream = torch.cuda.current_stream(dev)
+    tok = torch.empty(B, dtype=torch.int32, device=dev)
+    out = {"token": tok}
+
+    def step(i):
+        tps.sample(w.logits, w.temperature, w.top_k, w.top_p, w.min_p, w.seed, i, out=out)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local) if not args.no_clocks else None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+        time.sleep(0.5)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    t_wall0 = time.perf_counter()
+    ev[0].record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop() if clocks else None
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    rows_total = B * world
+    value = rows_total * args.steps / (total_ms / 1e3)
+
+    # roofline for the one kernel of the step (each step is exactly one launch)
+    alg_bytes = B * (V * es + ROW_PARAM_BYTES)
+    kern_ms = statistics.mean(per)
+    achieved = alg_bytes / (kern_ms / 1e3) / 1e9
+    peak, peak_kind = measured_peaks()
+    tag = f"{args.workload}_b{B}_v{V}_{args.dtype}"
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+            "frac_of_8000": round(achieved / 8000.0, 4), "traffic": committed_traffic(tag),
+            "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms_mean": round(kern_ms, 5),
+            "kernel_ms_p50": round(statistics.median(per), 5)}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32" if args.dtype == "f32" else "bf16", "data": "synthetic",
+            "config": workload_config(args), "roofline": roof, "gpu_launches": args.steps,
+            "hbm_gbs": round(achieved, 1), "us_per_step": round(1e3 * ms_per_step, 2),
+            "wall_s_timed": round(t_wall, 3), "cluster_size": tps.cluster_size(w.logits.dtype, B, V)}
+    if clk:
+        line["clocks"] = clk
+
+    if rank == 0 and not args.no_latency:
+        line["latency_b1"] = latency_b1(args, dev)
+    if not args.no_e2e:
+        line["e2e"] = e2e(args, w, dev, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        wc = make_workload(args, "cpu", seed=rank)
+        line["cpu_baseline"] = cpu_baseline(wc)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def latency_b1(args, dev, calls=300):
+    """p50/p90 device time of one call at B=1 (same V and dtype), stream-ordered, events per call."""
+    import nucleus_token_sampler_gb300 as tps
+    from nucleus_token_sampler_gb300 import workloads
+    dt = torch.float32 if args.dtype == "f32" else torch.bfloat16
+    w = workloads.make("decode", device=dev, seed=7, B=1, V=args.V, dtype=dt)
+    tok = {"token": torch.empty(1, dtype=torch.int32, device=dev)}
+    s = torch.cuda.current_stream(dev)
+    for i in range(20):
+        tps.sample(w.logits, w.temperature, w.top_k, w.top_p, w.min_p, w.seed, i, out=tok)
+    ts = []
+    for i in range(calls):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        tps.sample(w.logits, w.temperature, w.top_k, w.top_p, w.min_p, w.seed, i, out=tok)
+        b.record(s)
+        b.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3)
+    ts.sort()
+    return {"p50_us": round(ts[len(ts) // 2], 2), "p90_us": round(ts[int(len(ts) * 0.9)], 2),
+            "calls": calls, "cluster_size": tps.cluster_size(dt, 1, args.V)}
+
+
+def e2e(args, w, dev, world, steps=None):
+    """Same metric through the public call with host buffers: per step, pinned host logits and
+    parameters are copied to the device, the batch is sampled and the tokens are read back."""
+    import nucleus_token_sampler_gb300 as tps
+    steps = steps or max(3, min(args.steps, 20))
+    B, V = w.B, w.V
+    host = {k: getattr(w, k).cpu().pin_memory() for k in ("logits", "temperature", "top_k", "top_p", "min_p",
+                                                          "seed")}
+    dbuf = {k: torch.empty_like(getattr(w, k)) for k in host}
+    tok_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    out = {"token": torch.empty(B, dtype=torch.int32, device=dev)}
+    s = torch.cuda.current_stream(dev)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = tok_h.numel() * 4
+
+    def one(i):
+        for k in host:
+            dbuf[k].copy_(host[k], non_blocking=True)
+        tps.sample(dbuf["logits"], dbuf["temperature"], dbuf["top_k"], dbuf["top_p"], dbuf["min_p"], dbuf["seed"],
+                   i, out=out)
+        tok_h.copy_(out["token"], non_blocking=True)
+
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for i in range(steps):
+        one(i)
+    b.record(s)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": B * world * steps / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

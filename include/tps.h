@@ -1,0 +1,122 @@
+/*
+ * tps.h -- C ABI of the GB300 batched token sampler.
+ *
+ * For each row b of a [B, V] logits matrix the library applies, in this fixed order,
+ *   temperature -> min-p -> top-k -> top-p (nucleus) -> renormalise -> sample one token,
+ * as described on the pages "What do temperature, top-k and top-p each do to the next-token
+ * distribution, and in what order does a serving engine apply them?" ('A strong answer': the
+ * p_i(T) equation, the engine order and the exponential-race draw) and "Implement batched top-p
+ * sampling with temperature" ('How to approach it': keep token i iff the mass of strictly more
+ * probable tokens is below p; 'A strong answer': the greedy branch and per-request p).
+ *
+ * Rules, per row (T = temperature[b], k = top_k[b], p = top_p[b], m = min_p[b]):
+ *   - T <= 0: greedy; the token is the lowest index holding the largest logit.
+ *   - min-p keeps tokens with p_i >= m * p_max (m <= 0: off; m > 1 acts as 1).
+ *   - top-k keeps tokens with fewer than k strictly larger logits, so ties at the k-th value all
+ *     survive (k <= 0 or k >= V: off).
+ *   - top-p keeps token i of the survivors S iff the mass of the survivors with a strictly larger
+ *     logit, renormalised over S, is below p.  The class of the largest logit is always kept;
+ *     p >= 1 keeps S; p <= 0 keeps only that class.
+ *   - -inf logits get probability 0 and are never kept.
+ *   - the token is argmax over the kept set of  -(zmax - z_i)/T - ln(-ln u_i)  (an exponential race,
+ *     argmax P_i / E_i), lowest index on equal keys, with
+ *     u_i = (2 * (x >> 9) + 1) * 2^-24 and x = word (i mod 4) of Philox4x32-10 with key = seed[b]
+ *     (low word first) and counter = (i / 4, b, step low word, step high word).
+ *
+ * Calling convention (all entry points):
+ *   - every pointer argument is a DEVICE pointer owned by the caller, except where marked; the
+ *     library allocates no memory per call, never synchronises the host, keeps no state between
+ *     calls and may be called from several host threads at once;
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream); all work is enqueued on it;
+ *   - the return value is a tps_status; errors in the arguments are reported before anything is
+ *     enqueued; problems in a row's data are reported per row in out_status and never abort the
+ *     batch (a failed row gets token -1, cutoff NaN, kept 0 and an all-zero probability row).
+ */
+#ifndef TPS_H_
+#define TPS_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of the logits matrix. */
+typedef enum { TPS_F32 = 0, TPS_BF16 = 1 } tps_dtype;
+
+/* Synchronous return codes. */
+typedef enum {
+    TPS_OK = 0,
+    TPS_ERR_ARG = 1,           /* a required pointer is NULL, B < 0, V < 1 or ld < V            */
+    TPS_ERR_DTYPE = 2,         /* dtype is not a tps_dtype                                      */
+    TPS_ERR_UNSUPPORTED_V = 3, /* V is above tps_max_vocab(dtype)                               */
+    TPS_ERR_ALIGN = 4,         /* logits, out_probs or a parameter array is not element-aligned */
+    TPS_ERR_CUDA = 5           /* the CUDA runtime refused the launch (see tps_last_cuda_error) */
+} tps_status;
+
+/* Per-row outcome written to out_status. */
+typedef enum {
+    TPS_ROW_OK = 0,
+    TPS_ROW_NAN = 1,        /* the row holds a NaN or +inf logit ("Top-p (Nucleus) Sampling, in
+                               depth", 'Failure modes': fail the request rather than sample)    */
+    TPS_ROW_ALL_MASKED = 2, /* every logit is -inf                                              */
+    TPS_ROW_BAD_PARAM = 3,  /* temperature, top_p or min_p is NaN or infinite                    */
+    TPS_ROW_TIMEOUT = 4     /* a bounded wait inside the kernel gave up; the row was not sampled */
+} tps_row_status;
+
+/*
+ * tps_sample -- sample one token per row of a dense [B, V] logits matrix.
+ *
+ *   logits       [B, V] row-major, TPS_F32 (float) or TPS_BF16 (bfloat16); element-aligned.
+ *   dtype        a tps_dtype.
+ *   B, V         rows and vocabulary size; B = 0 returns TPS_OK and enqueues nothing.
+ *   temperature  [B] float.     top_k [B] int32.     top_p [B] float.     min_p [B] float.
+ *   seed         [B] uint64 Philox key per row.
+ *   step         64-bit counter word shared by the batch (advance it every decode step).
+ *   out_token    [B] int32: the sampled token id, or -1 for a failed row.
+ *   out_probs    [B, V] float, or NULL: the renormalised distribution the token was drawn from
+ *                (0 outside the kept set; one-hot for greedy rows).
+ *   stream       cudaStream_t.
+ */
+int tps_sample(const void* logits, int dtype, int64_t B, int64_t V, const float* temperature,
+               const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seed,
+               uint64_t step, int32_t* out_token, float* out_probs, void* stream);
+
+/*
+ * tps_sample_ex -- tps_sample with a row stride and optional diagnostics.
+ *
+ *   ld           row stride of `logits` in elements (ld >= V); out_probs stays dense [B, V].
+ *   out_status   [B] int32 tps_row_status, or NULL.
+ *   out_cutoff   [B] float, or NULL: v*, the smallest kept logit.  Token i is kept iff its logit is
+ *                finite and >= v* (greedy rows: v* = the largest logit and only the returned token
+ *                counts as kept).
+ *   out_kept     [B] int32, or NULL: the number of kept tokens (1 for greedy rows).
+ */
+int tps_sample_ex(const void* logits, int dtype, int64_t B, int64_t V, int64_t ld,
+                  const float* temperature, const int32_t* top_k, const float* top_p,
+                  const float* min_p, const uint64_t* seed, uint64_t step, int32_t* out_token,
+                  float* out_probs, int32_t* out_status, float* out_cutoff, int32_t* out_kept,
+                  void* stream);
+
+/* Largest V the library accepts for `dtype` on the current device (0 for an unknown dtype or
+ * when no device is usable).  Host-only query; enqueues nothing. */
+int64_t tps_max_vocab(int dtype);
+
+/* Cluster size (CTAs per row) tps_sample would use for this shape on the current device, or 0
+ * when the shape is not supported.  Host-only query. */
+int tps_cluster_size(int dtype, int64_t B, int64_t V);
+
+/* Static, human-readable text for a tps_status or (offset by 100) a tps_row_status. */
+const char* tps_status_string(int status);
+
+/* The last cudaError_t seen by a call that returned TPS_ERR_CUDA on this host thread. */
+int tps_last_cuda_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int tps_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPS_H_ */

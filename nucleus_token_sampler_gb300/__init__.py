@@ -1,0 +1,182 @@
+"""GB300 batched token sampler: temperature -> min-p -> top-k -> top-p -> one token per row.
+
+A thin Python view of the C ABI in ``include/tps.h`` (``libtps.so``, built in-tree for sm_103a).
+This module only marshals torch tensors into pointers and the current CUDA stream; every step of
+the sampler runs in the CUDA kernels. There is no CPU fallback: if the library is missing or was
+built for another machine, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import torch
+
+__all__ = ["build", "load", "sample", "TPS_F32", "TPS_BF16", "ROW_STATUS", "library_path", "max_vocab",
+           "cluster_size", "version"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_CSRC = os.path.join(_HERE, "csrc")
+_LIB = os.path.join(_HERE, "libtps.so")
+_INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
+_SOURCES = ["tps_api.cu"]
+_HEADERS = ["tps_device.cuh", "tps_kernel.cuh"]
+
+TPS_F32, TPS_BF16 = 0, 1
+ROW_STATUS = {0: "ok", 1: "nan", 2: "all_masked", 3: "bad_param", 4: "timeout"}
+_ERRORS = {1: "invalid argument", 2: "unknown dtype", 3: "vocabulary too large", 4: "misaligned pointer",
+           5: "CUDA runtime error"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB
+
+
+def _stale() -> bool:
+    if not os.path.exists(_LIB):
+        return True
+    t = os.path.getmtime(_LIB)
+    deps = [os.path.join(_CSRC, f) for f in _SOURCES + _HEADERS] + [os.path.join(_INCLUDE, "tps.h")]
+    return any(os.path.getmtime(p) > t for p in deps)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile ``libtps.so`` for sm_103a with nvcc (one translation unit, a few seconds)."""
+    if not force and not _stale():
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
+           "-Xcompiler", "-fPIC", "-shared", "-o", tmp] + [os.path.join(_CSRC, f) for f in _SOURCES]
+    if verbose:
+        cmd.insert(1, "-Xptxas=-v")
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def load():
+    """Load the CUDA library (building it first if it is missing or older than its sources)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P, I64, I32, U64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64
+            lib.tps_sample.restype = I32
+            lib.tps_sample.argtypes = [P, I32, I64, I64, P, P, P, P, P, U64, P, P, P]
+            lib.tps_sample_ex.restype = I32
+            lib.tps_sample_ex.argtypes = [P, I32, I64, I64, I64, P, P, P, P, P, U64, P, P, P, P, P, P]
+            lib.tps_max_vocab.restype = I64
+            lib.tps_max_vocab.argtypes = [I32]
+            lib.tps_cluster_size.restype = I32
+            lib.tps_cluster_size.argtypes = [I32, I64, I64]
+            lib.tps_status_string.restype = ctypes.c_char_p
+            lib.tps_status_string.argtypes = [I32]
+            lib.tps_last_cuda_error.restype = I32
+            lib.tps_last_cuda_error.argtypes = []
+            lib.tps_version.restype = I32
+            lib.tps_version.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def version() -> int:
+    return int(load().tps_version())
+
+
+def max_vocab(dtype: torch.dtype = torch.float32) -> int:
+    return int(load().tps_max_vocab(_dtype_code(dtype)))
+
+
+def cluster_size(dtype: torch.dtype, B: int, V: int) -> int:
+    return int(load().tps_cluster_size(_dtype_code(dtype), B, V))
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return TPS_F32
+    if dt == torch.bfloat16:
+        return TPS_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {dt}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(rc: int):
+    if rc != 0:
+        lib = load()
+        extra = f" (cudaError {lib.tps_last_cuda_error()})" if rc == 5 else ""
+        raise RuntimeError(f"tps_sample failed: {_ERRORS.get(rc, rc)}{extra}")
+
+
+def _param(x, B, dtype, device):
+    if not isinstance(x, torch.Tensor):
+        x = torch.tensor(x, dtype=dtype)
+    x = x.to(device=device, dtype=dtype)
+    if x.dim() == 0:
+        x = x.expand(B)
+    if x.shape != (B,):
+        raise ValueError(f"per-row parameter must have shape ({B},), got {tuple(x.shape)}")
+    return x.contiguous()
+
+
+def sample(logits: torch.Tensor, temperature, top_k, top_p, min_p, seed, step: int = 0, *,
+           want_probs: bool = False, diagnostics: bool = False, out=None, stream=None):
+    """Sample one token per row of ``logits`` ([B, V] float32/bfloat16 CUDA tensor; the row stride
+    may exceed V).
+
+    Per-row parameters may be tensors of shape [B] or Python scalars: ``temperature``, ``top_p``,
+    ``min_p`` (float32), ``top_k`` (int32), ``seed`` (int64, read as uint64).  ``step`` is the
+    64-bit counter shared by the batch.  Returns the [B] int32 token tensor, or a dict with
+    ``token``, ``status``, ``cutoff``, ``kept`` (and ``probs``) when ``diagnostics`` or
+    ``want_probs`` is set.  Work is enqueued on ``stream`` (default: the current stream).
+    """
+    if not logits.is_cuda:
+        raise ValueError("logits must be a CUDA tensor (the sampler has no CPU path)")
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be [B, V] with unit stride along V")
+    B, V = logits.shape
+    ld = logits.stride(0) if B > 1 else V
+    dev = logits.device
+    code = _dtype_code(logits.dtype)
+    T = _param(temperature, B, torch.float32, dev)
+    K = _param(top_k, B, torch.int32, dev)
+    P = _param(top_p, B, torch.float32, dev)
+    M = _param(min_p, B, torch.float32, dev)
+    S = _param(seed, B, torch.int64, dev)
+    res = out if out is not None else {}
+    tok = res.get("token")
+    if tok is None:
+        tok = torch.empty(B, dtype=torch.int32, device=dev)
+    probs = res.get("probs") if want_probs else None
+    if want_probs and probs is None:
+        probs = torch.empty((B, V), dtype=torch.float32, device=dev)
+    st = cut = kept = None
+    if diagnostics:
+        st = res.get("status", None)
+        st = st if st is not None else torch.empty(B, dtype=torch.int32, device=dev)
+        cut = res.get("cutoff", None)
+        cut = cut if cut is not None else torch.empty(B, dtype=torch.float32, device=dev)
+        kept = res.get("kept", None)
+        kept = kept if kept is not None else torch.empty(B, dtype=torch.int32, device=dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        rc = load().tps_sample_ex(_ptr(logits), code, B, V, ld, _ptr(T), _ptr(K), _ptr(P), _ptr(M), _ptr(S),
+                                  int(step) & ((1 << 64) - 1), _ptr(tok), _ptr(probs), _ptr(st), _ptr(cut),
+                                  _ptr(kept), ctypes.c_void_p(s.cuda_stream))
+    _check(rc)
+    if not (diagnostics or want_probs):
+        return tok
+    r = {"token": tok}
+    if diagnostics:
+        r.update(status=st, cutoff=cut, kept=kept)
+    if want_probs:
+        r["probs"] = probs
+    return r

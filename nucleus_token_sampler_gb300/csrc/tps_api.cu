@@ -1,0 +1,286 @@
+// tps_api.cu -- the C ABI declared in include/tps.h: argument checks, launch-shape choice and the
+// cluster launch.  No allocation, no host synchronisation, no state kept between calls beyond a
+// per-device cache of queried limits.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/tps.h"
+#include "tps_kernel.cuh"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxVocabMass = (int64_t(1) << 20) - 1;  // fixed-point mass sums fit 64 bits
+constexpr uint32_t kSliceTarget = 64u * 1024u;              // preferred slice per CTA
+constexpr int kMaxCluster = 16;
+
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    int smem_optin = 0;
+    bool attrs_f32 = false, attrs_bf16 = false;
+    // Largest dynamic shared memory per CTA seen to co-schedule a cluster of 9..16 CTAs, per dtype
+    // (0 = not known yet).
+    std::atomic<long> wide_ok[2][kMaxCluster + 1];
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+int elem_bytes(int dtype) { return dtype == TPS_F32 ? 4 : (dtype == TPS_BF16 ? 2 : 0); }
+
+bool device_info(DeviceInfo** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!d.ready) {
+            if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+            if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+                return false;
+            d.ready = true;
+        }
+    }
+    *out = &d;
+    return true;
+}
+
+// Slice bytes a CTA must hold for a row of V elements split over C CTAs (upper bound over every
+// alignment of the row start), rounded to 128 bytes.
+uint32_t slice_cap_bytes(int64_t V, int es, int C)
+{
+    const int64_t n16 = (V * es) / 16;          // aligned interior vectors, at most
+    const int64_t per = (n16 + C - 1) / C;      // per CTA
+    return (uint32_t)(((per * 16) + 127) / 128 * 128);
+}
+
+size_t smem_bytes(uint32_t slice_cap) { return (size_t)slice_cap + sizeof(tps::Shared); }
+
+// Choose the cluster size: the smallest C whose slice fits the preferred size, widened for small
+// batches so one row spreads over more SMs.  Returns 0 if even 16 CTAs cannot hold the row.
+int choose_cluster(const DeviceInfo& d, int es, int64_t B, int64_t V)
+{
+    const int64_t row_bytes = V * es;
+    int c = (int)((row_bytes + kSliceTarget - 1) / kSliceTarget);
+    if (c < 1) c = 1;
+    if (B > 0 && B * 2 <= d.sms) {
+        int want = (int)(d.sms / B);
+        if (want > kMaxCluster) want = kMaxCluster;
+        if (want > c) c = want;
+    }
+    if (V < 64 * (int64_t)c) {  // tiny rows: do not spread a handful of vectors over many CTAs
+        c = (int)((V + 63) / 64);
+        if (c < 1) c = 1;
+    }
+    while (c <= kMaxCluster && smem_bytes(slice_cap_bytes(V, es, c)) > (size_t)d.smem_optin) ++c;
+    if (c > kMaxCluster) return 0;
+    return c;
+}
+
+template <typename TIn>
+cudaError_t prepare_kernel(const DeviceInfo& d)
+{
+    auto k = tps::sample_rows_kernel<TIn>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, d.smem_optin);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+}
+
+// Clusters of more than 8 CTAs are not guaranteed to fit a GPC; ask the occupancy calculator
+// once per (dtype, cluster size, shared-memory size) and fall back to 8 when they do not.
+template <typename TIn>
+bool wide_cluster_ok(DeviceInfo& d, int dt, int C, size_t smem)
+{
+    std::atomic<long>& slot = d.wide_ok[dt][C];
+    const long known = slot.load();
+    if (known > 0 && (size_t)known >= smem) return true;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)C, 1, 1);
+    cfg.blockDim = dim3(tps::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, tps::sample_rows_kernel<TIn>, &cfg);
+    if (e != cudaSuccess || n < 1) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    if ((long)smem > known) slot.store((long)smem);
+    return true;
+}
+
+template <typename TIn>
+cudaError_t launch(const tps::Args& a, int C, size_t smem, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.B * C), 1, 1);
+    cfg.blockDim = dim3(tps::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tps::sample_rows_kernel<TIn>, a);
+}
+
+int fail_cuda(cudaError_t e)
+{
+    g_last_cuda_error = (int)e;
+    return TPS_ERR_CUDA;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int tps_version(void) { return 100; }
+
+int tps_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* tps_status_string(int status)
+{
+    switch (status) {
+    case TPS_OK: return "ok";
+    case TPS_ERR_ARG: return "invalid argument (null pointer, B < 0, V < 1 or ld < V)";
+    case TPS_ERR_DTYPE: return "unknown dtype";
+    case TPS_ERR_UNSUPPORTED_V: return "vocabulary too large for this device";
+    case TPS_ERR_ALIGN: return "pointer not aligned to its element type";
+    case TPS_ERR_CUDA: return "CUDA runtime error";
+    case 100 + TPS_ROW_OK: return "row ok";
+    case 100 + TPS_ROW_NAN: return "row holds a NaN or +inf logit";
+    case 100 + TPS_ROW_ALL_MASKED: return "every logit of the row is -inf";
+    case 100 + TPS_ROW_BAD_PARAM: return "temperature, top_p or min_p is not finite";
+    case 100 + TPS_ROW_TIMEOUT: return "a bounded wait in the kernel gave up";
+    default: return "unknown status";
+    }
+}
+
+int64_t tps_max_vocab(int dtype)
+{
+    const int es = elem_bytes(dtype);
+    if (!es) return 0;
+    DeviceInfo* d = nullptr;
+    if (!device_info(&d)) return 0;
+    int64_t lo = 0, hi = kMaxVocabMass;
+    while (lo < hi) {  // largest V whose 16-CTA slice still fits
+        const int64_t mid = (lo + hi + 1) / 2;
+        if (smem_bytes(slice_cap_bytes(mid, es, kMaxCluster)) <= (size_t)d->smem_optin) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+int tps_cluster_size(int dtype, int64_t B, int64_t V)
+{
+    const int es = elem_bytes(dtype);
+    if (!es || V < 1 || B < 0) return 0;
+    DeviceInfo* d = nullptr;
+    if (!device_info(&d)) return 0;
+    if (V > kMaxVocabMass) return 0;
+    return choose_cluster(*d, es, B, V);
+}
+
+int tps_sample_ex(const void* logits, int dtype, int64_t B, int64_t V, int64_t ld, const float* temperature,
+                  const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seed,
+                  uint64_t step, int32_t* out_token, float* out_probs, int32_t* out_status, float* out_cutoff,
+                  int32_t* out_kept, void* stream)
+{
+    if (B < 0 || V < 1 || ld < V) return TPS_ERR_ARG;
+    const int es = elem_bytes(dtype);
+    if (!es) return TPS_ERR_DTYPE;
+    if (B == 0) return TPS_OK;
+    if (!logits || !temperature || !top_k || !top_p || !min_p || !seed || !out_token) return TPS_ERR_ARG;
+    if (!aligned(logits, es) || !aligned(temperature, 4) || !aligned(top_k, 4) || !aligned(top_p, 4) ||
+        !aligned(min_p, 4) || !aligned(seed, 8) || !aligned(out_token, 4) || (out_probs && !aligned(out_probs, 4)) ||
+        (out_status && !aligned(out_status, 4)) || (out_cutoff && !aligned(out_cutoff, 4)) ||
+        (out_kept && !aligned(out_kept, 4)))
+        return TPS_ERR_ALIGN;
+    if (V > kMaxVocabMass || V > INT32_MAX) return TPS_ERR_UNSUPPORTED_V;
+    if (B > (int64_t)INT32_MAX / kMaxCluster) return TPS_ERR_ARG;
+
+    DeviceInfo* d = nullptr;
+    if (!device_info(&d)) return fail_cuda(cudaGetLastError());
+    const int C = choose_cluster(*d, es, B, V);
+    if (C == 0) return TPS_ERR_UNSUPPORTED_V;
+    const uint32_t cap = slice_cap_bytes(V, es, C);
+    const size_t smem = smem_bytes(cap);
+
+    tps::Args a;
+    a.logits = logits;
+    a.B = B;
+    a.V = V;
+    a.ld = ld;
+    a.temperature = temperature;
+    a.top_k = top_k;
+    a.top_p = top_p;
+    a.min_p = min_p;
+    a.seed = seed;
+    a.step = step;
+    a.out_token = out_token;
+    a.out_probs = out_probs;
+    a.out_status = out_status;
+    a.out_cutoff = out_cutoff;
+    a.out_kept = out_kept;
+    a.slice_cap = cap;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    int Cl = C;
+    size_t sm = smem;
+    // A cluster wider than 8 that the GPU cannot co-schedule falls back to 8 CTAs, if they hold the row.
+    auto use_portable = [&]() -> bool {
+        if (smem_bytes(slice_cap_bytes(V, es, 8)) > (size_t)d->smem_optin) return false;
+        Cl = 8;
+        a.slice_cap = slice_cap_bytes(V, es, 8);
+        sm = smem_bytes(a.slice_cap);
+        return true;
+    };
+    if (dtype == TPS_F32) {
+        if (!d->attrs_f32) {
+            e = prepare_kernel<float>(*d);
+            if (e != cudaSuccess) return fail_cuda(e);
+            d->attrs_f32 = true;
+        }
+        if (Cl > 8 && !wide_cluster_ok<float>(*d, 0, Cl, sm) && !use_portable()) return TPS_ERR_UNSUPPORTED_V;
+        e = launch<float>(a, Cl, sm, st);
+    } else {
+        if (!d->attrs_bf16) {
+            e = prepare_kernel<__nv_bfloat16>(*d);
+            if (e != cudaSuccess) return fail_cuda(e);
+            d->attrs_bf16 = true;
+        }
+        if (Cl > 8 && !wide_cluster_ok<__nv_bfloat16>(*d, 1, Cl, sm) && !use_portable())
+            return TPS_ERR_UNSUPPORTED_V;
+        e = launch<__nv_bfloat16>(a, Cl, sm, st);
+    }
+    if (e != cudaSuccess) return fail_cuda(e);
+    return TPS_OK;
+}
+
+int tps_sample(const void* logits, int dtype, int64_t B, int64_t V, const float* temperature, const int32_t* top_k,
+               const float* top_p, const float* min_p, const uint64_t* seed, uint64_t step, int32_t* out_token,
+               float* out_probs, void* stream)
+{
+    return tps_sample_ex(logits, dtype, B, V, V, temperature, top_k, top_p, min_p, seed, step, out_token,
+                         out_probs, nullptr, nullptr, nullptr, stream);
+}
+
+}  // extern "C"

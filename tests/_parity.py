@@ -1,0 +1,77 @@
+"""GPU-versus-oracle comparison used by the GPU parity tests."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import nucleus_token_sampler_gb300 as tps
+import oracle
+
+TOPP_BAND, MINP_BAND, RACE_BAND = oracle.FLAG_TOPP_BAND, oracle.FLAG_MINP_BAND, oracle.FLAG_RACE_BAND
+PROB_TOL = 1e-5  # absolute, on renormalised probabilities
+
+
+def run_gpu(w, want_probs=True, logits=None):
+    d = w.to("cuda")
+    lg = d.logits if logits is None else logits
+    r = tps.sample(lg, d.temperature, d.top_k, d.top_p, d.min_p, d.seed, d.step, want_probs=want_probs,
+                   diagnostics=True)
+    torch.cuda.synchronize()
+    return {k: v.cpu() for k, v in r.items()}
+
+
+def run_oracle(w, rows=None, want_probs=True):
+    z = w.logits if rows is None else w.logits[rows]
+    sel = (lambda t: t) if rows is None else (lambda t: t[rows])
+    return oracle.sample(z.double().numpy(), sel(w.temperature).numpy(), sel(w.top_k).numpy(),
+                         sel(w.top_p).numpy(), sel(w.min_p).numpy(),
+                         sel(w.seed).numpy().astype(np.uint64), w.step,
+                         row_ids=None if rows is None else np.asarray(rows), want_probs=want_probs)
+
+
+def compare(w, g, o, rows=None, check_probs=True):
+    """Return (report dict, list of failure strings)."""
+    B = w.B
+    rows = np.arange(B) if rows is None else np.asarray(rows)
+    st_g = g["status"].numpy()[rows]
+    tok_g = g["token"].numpy()[rows]
+    kept_g = g["kept"].numpy()[rows]
+    cut_g = g["cutoff"].numpy()[rows].astype(np.float64)
+    flags = o["flags"]
+    fails = []
+    if not np.array_equal(st_g, o["status"]):
+        bad = np.nonzero(st_g != o["status"])[0][:5]
+        fails.append(f"status differs at rows {rows[bad].tolist()}: gpu {st_g[bad]} oracle {o['status'][bad]}")
+    okrow = o["status"] == 0
+    setband = (flags & (TOPP_BAND | MINP_BAND)) != 0
+    tokband = setband | ((flags & RACE_BAND) != 0)
+    chk = okrow & ~setband
+    for name, a, b in (("kept", kept_g, o["kept"]),):
+        bad = np.nonzero(chk & (a != b))[0]
+        if len(bad):
+            fails.append(f"{name} differs on {len(bad)} rows, e.g. row {rows[bad[0]]}: gpu {a[bad[0]]} oracle {b[bad[0]]}")
+    cut_o = o["cutoff"]
+    bad = np.nonzero(chk & (cut_g != cut_o))[0]
+    if len(bad):
+        fails.append(f"cutoff differs on {len(bad)} rows, e.g. row {rows[bad[0]]}: gpu {cut_g[bad[0]]} oracle {cut_o[bad[0]]}")
+    tchk = (o["status"] != 0) | ~tokband
+    bad = np.nonzero(tchk & (tok_g != o["token"]))[0]
+    if len(bad):
+        fails.append(f"token differs on {len(bad)} rows, e.g. row {rows[bad[0]]}: gpu {tok_g[bad[0]]} oracle {o['token'][bad[0]]}")
+    maxdp = 0.0
+    if check_probs and "probs" in g and "probs" in o:
+        pg = g["probs"].numpy()[rows].astype(np.float64)
+        po = o["probs"]
+        m = chk
+        if m.any():
+            maxdp = float(np.abs(pg[m] - po[m]).max())
+            if maxdp > PROB_TOL:
+                fails.append(f"probabilities differ by {maxdp:.3e}")
+        sums = pg[okrow].sum(axis=1)
+        if okrow.any() and np.abs(sums - 1).max() > 1e-5:
+            fails.append(f"probability rows sum to {sums.min()}..{sums.max()}")
+        if (~okrow).any() and np.abs(pg[~okrow]).max() != 0:
+            fails.append("failed rows have non-zero probabilities")
+    rep = {"rows": int(len(rows)), "band_rows": int(setband.sum()), "race_band_rows": int(((flags & RACE_BAND) != 0).sum()),
+           "max_abs_dprob": maxdp}
+    return rep, fails

@@ -1,0 +1,67 @@
+"""The C ABI library loads, exports every entry point the header declares, and rejects bad
+arguments synchronously (none of these calls reaches the GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import nucleus_token_sampler_gb300 as tps
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "tps.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tps_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    syms = declared_symbols()
+    for s in ("tps_sample", "tps_sample_ex", "tps_max_vocab", "tps_cluster_size", "tps_status_string",
+              "tps_last_cuda_error", "tps_version"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol():
+    lib = tps.load()
+    for s in declared_symbols():
+        assert hasattr(lib, s), f"{s} declared in tps.h but not exported"
+
+
+def test_version_and_status_strings():
+    lib = tps.load()
+    assert tps.version() >= 100
+    for code in range(6):
+        assert lib.tps_status_string(code)
+    assert b"NaN" in lib.tps_status_string(101)
+    assert lib.tps_status_string(999) == b"unknown status"
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+def call(B=4, V=100, ld=None, dtype=0, logits=FAKE, T=FAKE, K=FAKE, P=FAKE, M=FAKE, S=FAKE, out=FAKE):
+    lib = tps.load()
+    ld = V if ld is None else ld
+    v = lambda p: None if p is None else ctypes.c_void_p(p)
+    return lib.tps_sample_ex(v(logits), dtype, B, V, ld, v(T), v(K), v(P), v(M), v(S), 0, v(out), None, None,
+                             None, None, None)
+
+
+@pytest.mark.parametrize("kw,rc", [
+    (dict(B=-1), 1), (dict(V=0), 1), (dict(V=10, ld=9), 1), (dict(dtype=7), 2), (dict(dtype=-1), 2),
+    (dict(logits=None), 1), (dict(T=None), 1), (dict(K=None), 1), (dict(P=None), 1), (dict(M=None), 1),
+    (dict(S=None), 1), (dict(out=None), 1),
+    (dict(logits=FAKE + 2), 4),
+    (dict(T=FAKE + 1), 4), (dict(S=FAKE + 4), 4),
+    (dict(V=1 << 20), 3),
+])
+def test_argument_validation(kw, rc):
+    assert call(**kw) == rc
+
+
+def test_empty_batch_is_a_noop():
+    # B = 0 returns OK before touching any pointer or the GPU.
+    assert call(B=0, logits=None, T=None, K=None, P=None, M=None, S=None, out=None) == 0
