@@ -30,9 +30,14 @@ def check(w, rows=None, want_probs=True, logits=None, max_band_frac=0.05):
     return g, o, rep
 
 
+# Flat rows (logits 1..0 over 128k tokens) have class masses ~1e-5 apart, so a class within 1e-6 of
+# p is common there: up to a third of those rows are boundary rows.
+BAND_FRAC = {"small": 0.05, "mixed": 0.3, "ties_masked": 0.05}
+
+
 @pytest.mark.parametrize("name", ["small", "mixed", "ties_masked"])
 def test_configs_full(name):
-    check(workloads.make(name, device="cpu"))
+    check(workloads.make(name, device="cpu"), max_band_frac=BAND_FRAC[name])
 
 
 @pytest.mark.parametrize("B,V,dtype", [(3, 1000, torch.float32), (5, 4099, torch.bfloat16),
