@@ -3,20 +3,20 @@
 //
 // Each of the C CTAs of a cluster bulk-copies one contiguous 16-byte-aligned slice of the row from
 // HBM into its own shared memory (one read of the row, no multicast); the ragged head and tail of
-// an unaligned row are fetched with plain loads.  Everything after that reads shared memory only,
-// and the CTAs exchange small reductions through distributed shared memory:
+// an unaligned row are fetched with plain loads.  Everything after that reads shared memory, and
+// the CTAs exchange small values through distributed shared memory (one lane per CTA):
 //
-//   A  zmax (NaN-propagating max) -> row status, greedy branch;
-//   B  one pass: d = (zmax - z)/T, min-p survival, 512-bin histogram over d of {count, exact
-//      fixed-point mass}, and the survivors appended to a candidate list;
-//   C  few survivors (<= 1024): every CTA gathers all candidates, sorts them by (logit desc,
-//      index asc) and walks the classes of equal logits: top-k cut by count, top-p cut by mass,
-//      then the exponential race over the kept prefix;
-//      many survivors: the histogram locates the bin holding each cut; the cut's class is then
-//      resolved exactly by gathering that bin's tokens (or by further sub-histograms over the
-//      logit's order-preserving key until few enough remain or a single value is left);
-//   D  the race over the kept tokens (those with logit >= the cut), and the optional output row
-//      of renormalised probabilities.
+//   A  zmax (NaN-propagating max) -> row status; T <= 0 -> greedy.
+//   B  one compare per token against a threshold below which min-p surely drops the token; the
+//      few tokens above it are checked exactly, counted and appended to a candidate list.
+//   C  few survivors (<= 256): every CTA gathers the candidates, sorts them by (logit desc, index
+//      asc) and walks the classes of equal logits -- top-k cut by count, top-p cut by mass -- then
+//      runs the exponential race over the kept prefix (one warp when there are <= 32).
+//      many survivors: a 256-bin histogram over d = (zmax - z)/T of {count, exact fixed-point
+//      mass} locates the bin holding each cut; the cut's class is then resolved exactly by
+//      gathering that bin's tokens, or by sub-histograms over the logit's order-preserving key
+//      until few enough remain or a single value is left.  The race runs over the slice.
+//   D  optional output row of renormalised probabilities.
 //
 // The chain is the one on "What do temperature, top-k and top-p each do to the next-token
 // distribution, and in what order does a serving engine apply them?" ('A strong answer'), with
@@ -34,10 +34,10 @@ namespace cg = cooperative_groups;
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kBins = 512;            // level-1 bins over d, width 1/16 (last bin: d >= 31.9375)
-constexpr float kBinScale = 16.f;
-constexpr int kSubBins = 512;         // sub-bins over a key interval
-constexpr int kCand = 1024;           // candidates resolved by sorting, per CTA and per cluster
+constexpr int kBins = 256;            // level-1 bins over d, width 1/8 (last bin: d >= 31.875)
+constexpr float kBinScale = 8.f;
+constexpr int kSubBins = 256;         // sub-bins over a key interval
+constexpr int kCand = 256;            // candidates resolved by sorting, per CTA and per cluster
 constexpr int kMaxExtra = 16;         // ragged head/tail elements fetched with plain loads
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s bound on every wait
 
@@ -62,7 +62,7 @@ struct Args {
 
 struct Shared {
     uint64_t mbar;
-    // --- values other CTAs of the cluster read through distributed shared memory
+    // --- values the other CTAs of the cluster read through distributed shared memory
     float pub_max;
     uint32_t pub_timeout;
     uint32_t pub_minidx;
@@ -79,38 +79,50 @@ struct Shared {
     int32_t xi[kMaxExtra];
     // --- block reduction scratch and broadcast slots
     float rf[kWarps];
-    uint32_t ru[kWarps];
-    uint32_t ru2[kWarps];
+    uint32_t ra[kWarps];
+    uint32_t rb[kWarps];
     uint64_t r64[kWarps];
     ArgBest rab[kWarps];
-    uint32_t bu[4];
-    uint64_t b64[2];
-    // --- histograms: local, then (after the cluster reduction) the full reduced histogram
+    uint32_t bu[8];
+    uint64_t b64[4];
+    float bf[2];
+    ArgBest bab;
+    // --- gather bookkeeping: offset and count of each CTA's list
+    uint32_t goff[16];
+    uint32_t gcnt[16];
+    uint32_t gtotal;
+    // --- histogram: local, then (after the cluster reduction) the full reduced histogram
     uint32_t hcnt[kBins];
     uint64_t hmass[kBins];
-    // --- this CTA's share of the reduced histogram (read by the other CTAs)
-    uint32_t rcnt[kBins];
-    uint64_t rmass[kBins];
-    // --- candidates
+    union {
+        struct {  // this CTA's share of the reduced histogram (read by the other CTAs)
+            uint32_t rcnt[kBins];
+            uint64_t rmass[kBins];
+        } sh;
+        struct {  // gathered candidates (key << 32 | ~index), sorted descending, and mass prefixes
+            uint64_t sbuf[kCand];
+            uint64_t pre[kCand + 1];
+        } cd;
+    } u;
+    // --- this CTA's candidate list (read by the other CTAs)
     uint32_t ncand;
     uint32_t ckey[kCand];
     uint32_t cidx[kCand];
-    uint64_t sbuf[kCand];     // gathered (key << 32 | ~index), sorted descending
-    uint64_t pre[kCand + 1];  // exclusive prefix of the fixed-point masses along sbuf
 };
 
 // ---------------------------------------------------------------------------------------------
-// Block-level helpers (every thread of the CTA must call them).
+// Block-level helpers (every thread of the CTA must call them).  Each starts with a barrier so
+// its scratch can be reused right after the previous call.
 // ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ float block_max_nan(float v, Shared& s)
+__device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, Shared& s)
 {
-    v = warp_max_nan(v);
+    v = warp_sum_u32(v);
     __syncthreads();
-    if ((threadIdx.x & 31) == 0) s.rf[threadIdx.x >> 5] = v;
+    if ((threadIdx.x & 31) == 0) s.ra[threadIdx.x >> 5] = v;
     __syncthreads();
-    float r = s.rf[0];
+    uint32_t r = 0;
 #pragma unroll
-    for (int w = 1; w < kWarps; ++w) r = fmax_nan(r, s.rf[w]);
+    for (int w = 0; w < kWarps; ++w) r += s.ra[w];
     return r;
 }
 
@@ -118,11 +130,11 @@ __device__ __forceinline__ uint32_t block_min_u32(uint32_t v, Shared& s)
 {
     v = warp_min_u32(v);
     __syncthreads();
-    if ((threadIdx.x & 31) == 0) s.ru[threadIdx.x >> 5] = v;
+    if ((threadIdx.x & 31) == 0) s.rb[threadIdx.x >> 5] = v;
     __syncthreads();
-    uint32_t r = s.ru[0];
+    uint32_t r = s.rb[0];
 #pragma unroll
-    for (int w = 1; w < kWarps; ++w) r = min(r, s.ru[w]);
+    for (int w = 1; w < kWarps; ++w) r = min(r, s.rb[w]);
     return r;
 }
 
@@ -130,23 +142,11 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, Shared& s)
 {
     v = warp_max_u32(v);
     __syncthreads();
-    if ((threadIdx.x & 31) == 0) s.ru2[threadIdx.x >> 5] = v;
+    if ((threadIdx.x & 31) == 0) s.rb[threadIdx.x >> 5] = v;
     __syncthreads();
-    uint32_t r = s.ru2[0];
+    uint32_t r = s.rb[0];
 #pragma unroll
-    for (int w = 1; w < kWarps; ++w) r = max(r, s.ru2[w]);
-    return r;
-}
-
-__device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, Shared& s)
-{
-    v = warp_sum_u32(v);
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) s.ru[threadIdx.x >> 5] = v;
-    __syncthreads();
-    uint32_t r = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) r += s.ru[w];
+    for (int w = 1; w < kWarps; ++w) r = max(r, s.rb[w]);
     return r;
 }
 
@@ -218,29 +218,35 @@ __device__ __forceinline__ int bin_of(float d)
 }
 
 // Cluster-wide sum of the local histogram hcnt/hmass[0, nb) into hcnt/hmass of every CTA.
-// Step 1: CTA c sums its share of bins over all CTAs into rcnt/rmass; step 2: every CTA copies
-// all shares back into its own hcnt/hmass.
+// Step 1: CTA c sums its share of the bins over all CTAs (one remote read per thread) into
+// u.sh; step 2: every CTA copies all shares back into its own hcnt/hmass.
 __device__ __forceinline__ void cluster_reduce_hist(cg::cluster_group& cluster, Shared& s, int nb,
                                                     uint32_t C, uint32_t rank)
 {
-    cluster.sync();  // all local histograms complete
     const int per = (nb + (int)C - 1) / (int)C;
-    const int b0 = (int)rank * per, b1 = min(nb, b0 + per);
+    const int b0 = min(nb, (int)rank * per), b1 = min(nb, b0 + per);
+    cluster.sync();  // every local histogram complete; nobody reads my previous share any more
     for (int b = b0 + (int)threadIdx.x; b < b1; b += kThreads) {
-        uint32_t c = 0;
-        uint64_t m = 0;
-        for (uint32_t r = 0; r < C; ++r) {
-            c += *cluster.map_shared_rank(&s.hcnt[b], r);
-            m += *cluster.map_shared_rank(&s.hmass[b], r);
-        }
-        s.rcnt[b] = c;
-        s.rmass[b] = m;
+        s.u.sh.rcnt[b] = 0;
+        s.u.sh.rmass[b] = 0;
     }
-    cluster.sync();  // all shares complete; nobody reads hcnt/hmass of another CTA any more
+    __syncthreads();
+    const int npairs = (b1 - b0) * (int)C;
+    for (int p = threadIdx.x; p < npairs; p += kThreads) {
+        const int b = b0 + p / (int)C;
+        const uint32_t r = (uint32_t)(p % (int)C);
+        const uint32_t c = *cluster.map_shared_rank(&s.hcnt[b], r);
+        if (c) {
+            atomicAdd(&s.u.sh.rcnt[b], c);
+            atomicAdd((unsigned long long*)&s.u.sh.rmass[b],
+                      (unsigned long long)*cluster.map_shared_rank(&s.hmass[b], r));
+        }
+    }
+    cluster.sync();  // all shares complete; nobody reads another CTA's hcnt/hmass any more
     for (int b = threadIdx.x; b < nb; b += kThreads) {
         const uint32_t owner = (uint32_t)(b / per);
-        s.hcnt[b] = *cluster.map_shared_rank(&s.rcnt[b], owner);
-        s.hmass[b] = *cluster.map_shared_rank(&s.rmass[b], owner);
+        s.hcnt[b] = *cluster.map_shared_rank(&s.u.sh.rcnt[b], owner);
+        s.hmass[b] = *cluster.map_shared_rank(&s.u.sh.rmass[b], owner);
     }
     __syncthreads();
 }
@@ -262,40 +268,21 @@ struct Crit {
 };
 
 // Scan the (full) histogram hcnt/hmass[0, nb) from bin 0 (largest logits) down and return the
-// last non-empty bin whose (count, mass) above satisfies the criterion.  Bins after `cap` are
-// ignored and bin `cap` counts as (cap_cnt, cap_mass).
-__device__ __forceinline__ void scan_bins(Shared& s, int nb, const Crit& cr, int cap, uint32_t cap_cnt,
-                                          uint64_t cap_mass, uint64_t C0, uint64_t A0, int* out_bin,
-                                          uint64_t* out_c, uint64_t* out_a)
+// last non-empty bin whose (count, mass) above satisfies the criterion.  nb <= kThreads.
+__device__ __forceinline__ void scan_bins(Shared& s, int nb, const Crit& cr, uint64_t C0, uint64_t A0,
+                                          int* out_bin, uint64_t* out_c, uint64_t* out_a)
 {
-    // nb <= 2 * kThreads: each thread owns bins 2t and 2t + 1.
-    const int b0 = 2 * threadIdx.x, b1 = b0 + 1;
-    auto eff_c = [&](int b) -> uint64_t {
-        if (b >= nb || b > cap) return 0;
-        return b == cap ? cap_cnt : s.hcnt[b];
-    };
-    auto eff_m = [&](int b) -> uint64_t {
-        if (b >= nb || b > cap) return 0;
-        return b == cap ? cap_mass : s.hmass[b];
-    };
-    const uint64_t c0 = eff_c(b0), c1 = eff_c(b1), m0 = eff_m(b0), m1 = eff_m(b1);
+    const int b = threadIdx.x;
+    const uint64_t c = (b < nb) ? s.hcnt[b] : 0;
+    const uint64_t m = (b < nb) ? s.hmass[b] : 0;
     uint64_t tot;
-    const uint64_t cpre = block_exscan_u64(c0 + c1, s, &tot);
-    const uint64_t mpre = block_exscan_u64(m0 + m1, s, &tot);
-    uint32_t best = 0;  // bin + 1, 0 = none
-    if (c0 > 0 && cr.keep(C0 + cpre, A0 + mpre)) best = b0 + 1;
-    if (c1 > 0 && cr.keep(C0 + cpre + c0, A0 + mpre + m0)) best = b1 + 1;
+    const uint64_t cpre = block_exscan_u64(c, s, &tot);
+    const uint64_t mpre = block_exscan_u64(m, s, &tot);
+    const uint32_t best = (c > 0 && cr.keep(C0 + cpre, A0 + mpre)) ? (uint32_t)b + 1u : 0u;
     const uint32_t bb = block_max_u32(best, s);
-    // Publish the prefix of the chosen bin.
-    if (bb != 0) {
-        const int b = (int)bb - 1;
-        if (b == b0) {
-            s.b64[0] = C0 + cpre;
-            s.b64[1] = A0 + mpre;
-        } else if (b == b1) {
-            s.b64[0] = C0 + cpre + c0;
-            s.b64[1] = A0 + mpre + m0;
-        }
+    if (bb != 0 && b == (int)bb - 1) {
+        s.b64[0] = C0 + cpre;
+        s.b64[1] = A0 + mpre;
     }
     __syncthreads();
     *out_bin = (int)bb - 1;
@@ -304,22 +291,23 @@ __device__ __forceinline__ void scan_bins(Shared& s, int nb, const Crit& cr, int
     __syncthreads();
 }
 
-// Sort sbuf[0, n) descending (bitonic, padded with zeros to a power of two).
+// Sort u.cd.sbuf[0, n) descending (bitonic, padded with zeros to a power of two).
 __device__ __forceinline__ void block_sort_desc(Shared& s, int n)
 {
+    uint64_t* sb = s.u.cd.sbuf;
     int np = 2;
     while (np < n) np <<= 1;
-    for (int i = n + (int)threadIdx.x; i < np; i += kThreads) s.sbuf[i] = 0;
+    for (int i = n + (int)threadIdx.x; i < np; i += kThreads) sb[i] = 0;
     __syncthreads();
     for (int k2 = 2; k2 <= np; k2 <<= 1) {
         for (int j = k2 >> 1; j > 0; j >>= 1) {
             for (int i = threadIdx.x; i < (np >> 1); i += kThreads) {
                 const int lo = 2 * j * (i / j) + (i % j), hi = lo + j;
                 const bool desc = (lo & k2) == 0;
-                const uint64_t x = s.sbuf[lo], y = s.sbuf[hi];
+                const uint64_t x = sb[lo], y = sb[hi];
                 if (desc ? (x < y) : (x > y)) {
-                    s.sbuf[lo] = y;
-                    s.sbuf[hi] = x;
+                    sb[lo] = y;
+                    sb[hi] = x;
                 }
             }
             __syncthreads();
@@ -329,77 +317,83 @@ __device__ __forceinline__ void block_sort_desc(Shared& s, int n)
 
 __device__ __forceinline__ uint32_t sb_key(uint64_t v) { return (uint32_t)(v >> 32); }
 __device__ __forceinline__ int32_t sb_idx(uint64_t v) { return (int32_t)(~(uint32_t)v); }
+__device__ __forceinline__ uint64_t sb_make(uint32_t key, uint32_t idx)
+{
+    return ((uint64_t)key << 32) | (uint64_t)(~idx);
+}
 
-// Fill pre[0, n] with the exclusive prefix of the fixed-point masses of sbuf[0, n).
+// Fill u.cd.pre[0, n] with the exclusive prefix of the fixed-point masses of sbuf[0, n).
 __device__ __forceinline__ void prefix_masses(Shared& s, const RowCtx& r, int n)
 {
-    // up to kCand = 4 * kThreads entries: each thread takes 4 consecutive ones
-    uint64_t q[4];
-    uint64_t local = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int t = 4 * threadIdx.x + j;
-        q[j] = (t < n) ? qmass_d(dist(r, key_to_float(sb_key(s.sbuf[t])))) : 0;
-        local += q[j];
-    }
+    const int t = threadIdx.x;  // n <= kCand == kThreads
+    const uint64_t q = (t < n) ? qmass_d(dist(r, key_to_float(sb_key(s.u.cd.sbuf[t])))) : 0;
     uint64_t tot;
-    uint64_t run = block_exscan_u64(local, s, &tot);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int t = 4 * threadIdx.x + j;
-        if (t < n) s.pre[t] = run;
-        run += q[j];
-    }
-    if (threadIdx.x == 0) s.pre[n] = tot;
+    const uint64_t run = block_exscan_u64(q, s, &tot);
+    if (t < n) s.u.cd.pre[t] = run;
+    if (t == 0) s.u.cd.pre[n] = tot;
     __syncthreads();
 }
 
-// Walk the classes of the sorted candidates sbuf[0, n) (n <= the list length) and return the
-// last class whose (count, mass) above -- offset by (C0, A0) -- satisfies the criterion.
+// Walk the classes of the sorted candidates sbuf[0, n) and return the last class whose
+// (count, mass) above -- offset by (C0, A0) -- satisfies the criterion.
 __device__ __forceinline__ Sel walk_classes(Shared& s, int n, const Crit& cr, uint64_t C0, uint64_t A0)
 {
-    uint32_t best = 0;  // position + 1 of the chosen class start
-    for (int t = threadIdx.x; t < n; t += kThreads) {
-        const uint32_t kt = sb_key(s.sbuf[t]);
-        const bool start = (t == 0) || sb_key(s.sbuf[t - 1]) != kt;
-        if (start && cr.keep(C0 + (uint64_t)t, A0 + s.pre[t])) best = max(best, (uint32_t)t + 1u);
+    const uint64_t* sb = s.u.cd.sbuf;
+    const int t = threadIdx.x;
+    bool start = false;
+    if (t < n) {
+        start = (t == 0) || sb_key(sb[t - 1]) != sb_key(sb[t]);
     }
-    const uint32_t sb = block_max_u32(best, s);
-    const int st = sb ? (int)sb - 1 : 0;
-    uint32_t end = (uint32_t)n;
-    for (int t = st + 1 + (int)threadIdx.x; t < n; t += kThreads)
-        if (sb_key(s.sbuf[t]) != sb_key(s.sbuf[t - 1])) end = min(end, (uint32_t)t);
+    const uint32_t best = (start && cr.keep(C0 + (uint64_t)t, A0 + s.u.cd.pre[t])) ? (uint32_t)t + 1u : 0u;
+    const uint32_t sbst = block_max_u32(best, s);
+    const int st = sbst ? (int)sbst - 1 : 0;
+    const uint32_t end = (start && t > st) ? (uint32_t)t : (uint32_t)n;
     const uint32_t e = block_min_u32(end, s);
     Sel out;
-    out.key = sb_key(s.sbuf[st]);
+    out.key = sb_key(sb[st]);
     out.cnt = C0 + e;
-    out.mass = A0 + s.pre[e];
+    out.mass = A0 + s.u.cd.pre[e];
     __syncthreads();
     return out;
 }
 
-// Copy every CTA's candidate list (counts published in pub_gcnt) into sbuf, sort it.
+// Copy every CTA's candidate list (counts in pub_gcnt) into u.cd.sbuf and sort it.  Returns n.
 __device__ __forceinline__ int gather_and_sort(cg::cluster_group& cluster, Shared& s, uint32_t C)
 {
-    uint32_t off = 0;
-    for (uint32_t rr = 0; rr < C; ++rr) {
-        const uint32_t n = *cluster.map_shared_rank(&s.pub_gcnt, rr);
-        const uint32_t* rk = cluster.map_shared_rank(&s.ckey[0], rr);
-        const uint32_t* ri = cluster.map_shared_rank(&s.cidx[0], rr);
-        for (uint32_t t = threadIdx.x; t < n; t += kThreads)
-            s.sbuf[off + t] = ((uint64_t)rk[t] << 32) | (uint64_t)(~ri[t]);
-        off += n;
+    if (threadIdx.x < 32) {  // lane r reads rank r's count; exclusive prefix over the ranks
+        const uint32_t lane = threadIdx.x;
+        const uint32_t cnt = (lane < C) ? *cluster.map_shared_rank(&s.pub_gcnt, lane) : 0u;
+        uint32_t inc = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if ((int)lane >= o) inc += y;
+        }
+        if (lane < C) {
+            s.goff[lane] = inc - cnt;
+            s.gcnt[lane] = cnt;
+        }
+        if (lane == 31) s.gtotal = inc;
     }
     __syncthreads();
-    block_sort_desc(s, (int)off);
-    return (int)off;
+    const uint32_t n = s.gtotal;
+    for (uint32_t rr = 0; rr < C; ++rr) {  // each count <= kCand == kThreads
+        const uint32_t off = s.goff[rr], cnt = s.gcnt[rr];
+        if (threadIdx.x < cnt) {
+            const uint32_t k = *cluster.map_shared_rank(&s.ckey[threadIdx.x], rr);
+            const uint32_t i = *cluster.map_shared_rank(&s.cidx[threadIdx.x], rr);
+            s.u.cd.sbuf[off + threadIdx.x] = sb_make(k, i);
+        }
+    }
+    __syncthreads();
+    block_sort_desc(s, (int)n);
+    return (int)n;
 }
 
 // Race key in float (for pruning) and in double (for the decision) of kept token i.
 struct RaceCtx {
     uint32_t k0, k1;    // Philox key = seed
     uint32_t row, s_lo, s_hi;
-    float dmax_tol;     // pruning margin
 };
 
 __device__ __forceinline__ float race_u(const RaceCtx& rc, int32_t i)
@@ -417,25 +411,31 @@ __device__ __forceinline__ double race_key64(const RowCtx& r, float z, float u)
     return __dsub_rn(-d, g);
 }
 
+// Margin between the float race key and the double one (both tokens' errors), for a row whose
+// kept tokens have d <= dcut.
+__device__ __forceinline__ float race_tol(float dcut) { return 1e-5f + 1e-6f * dcut; }
+
 // Refine the cut inside level-1 bin `bin` (tokens with key >= key_lo that survive min-p), given
 // the (count, mass) of the survivors above the bin.  Exact: ends with a sorted candidate list or
 // with a single logit value.
 template <typename TIn>
 __device__ Sel refine_bin(cg::cluster_group& cluster, Shared& s, const Slice<TIn>& sl, const RowCtx& r,
-                          uint32_t C, int bin, uint32_t key_lo, const Crit& cr, uint64_t C0, uint64_t A0)
+                          float zc, uint32_t C, int bin, uint32_t key_lo, const Crit& cr, uint64_t C0,
+                          uint64_t A0)
 {
-    // Phase 1: gather the bin (and its key range).
     uint32_t klo = 0, khi = 0xFFFFFFFFu;
     bool by_bin = true;
     for (int iter = 0; iter < 8; ++iter) {
-        cluster.sync();  // nobody still reads my candidate list or published counts
+        // Gather the tokens of the current range (a level-1 bin, or a key interval).
+        cluster.sync();  // nobody still reads my candidate list, published counts or shares
         if (threadIdx.x == 0) s.ncand = 0;
         __syncthreads();
         uint32_t lcnt = 0, lmin = 0xFFFFFFFFu, lmax = 0;
+        const uint32_t lo = klo, hi = khi;
         sl.for_each(s, [&](float z, int32_t i) {
-            if (!(z > -INFINITY)) return;
+            if (!(z > zc)) return;
             const uint32_t key = fkey(z);
-            if (key < key_lo || key < klo || key > khi) return;
+            if (key < key_lo || key < lo || key > hi) return;
             const float d = dist(r, z);
             if (by_bin && bin_of(d) != bin) return;
             if (!minp_ok(r, z, d)) return;
@@ -454,24 +454,38 @@ __device__ Sel refine_bin(cg::cluster_group& cluster, Shared& s, const Slice<TIn
         const uint32_t kmn = block_min_u32(lmin, s);
         const uint32_t kmx = block_max_u32(lmax, s);
         if (threadIdx.x == 0) {
-            s.pub_gcnt = cnt;
+            s.pub_gcnt = min(cnt, (uint32_t)kCand);
+            s.pub_nsurv = cnt;
             s.pub_gkmin = kmn;
             s.pub_gkmax = kmx;
         }
         cluster.sync();
-        uint64_t total = 0;
-        uint32_t gmin = 0xFFFFFFFFu, gmax = 0;
-        for (uint32_t rr = 0; rr < C; ++rr) {
-            total += *cluster.map_shared_rank(&s.pub_gcnt, rr);
-            gmin = min(gmin, *cluster.map_shared_rank(&s.pub_gkmin, rr));
-            gmax = max(gmax, *cluster.map_shared_rank(&s.pub_gkmax, rr));
+        if (threadIdx.x < 32) {
+            const uint32_t lane = threadIdx.x;
+            uint32_t tc = 0, gmn = 0xFFFFFFFFu, gmx = 0;
+            if (lane < C) {
+                tc = *cluster.map_shared_rank(&s.pub_nsurv, lane);
+                gmn = *cluster.map_shared_rank(&s.pub_gkmin, lane);
+                gmx = *cluster.map_shared_rank(&s.pub_gkmax, lane);
+            }
+            tc = warp_sum_u32(tc);
+            gmn = warp_min_u32(gmn);
+            gmx = warp_max_u32(gmx);
+            if (lane == 0) {
+                s.bu[4] = tc;
+                s.bu[5] = gmn;
+                s.bu[6] = gmx;
+            }
         }
-        if (total == 0) {  // cannot happen for a bin chosen as non-empty; keep the bound
-            Sel z0;
-            z0.key = key_lo;
-            z0.cnt = C0;
-            z0.mass = A0;
-            return z0;
+        __syncthreads();
+        const uint64_t total = s.bu[4];
+        const uint32_t gmin = s.bu[5], gmax = s.bu[6];
+        if (total == 0) {  // cannot happen for a bin chosen as non-empty; keep a valid answer
+            Sel o;
+            o.key = key_lo;
+            o.cnt = C0;
+            o.mass = A0;
+            return o;
         }
         if (gmin == gmax) {  // a single logit value: one class
             const uint64_t q = qmass_d(dist(r, key_to_float(gmin)));
@@ -498,36 +512,158 @@ __device__ Sel refine_bin(cg::cluster_group& cluster, Shared& s, const Slice<TIn
             s.hmass[b] = 0;
         }
         __syncthreads();
-        const uint32_t lo = klo, hi = khi;
+        const uint32_t lo2 = klo, hi2 = khi;
         sl.for_each(s, [&](float z, int32_t) {
-            if (!(z > -INFINITY)) return;
+            if (!(z > zc)) return;
             const uint32_t key = fkey(z);
-            if (key < key_lo || key < lo || key > hi) return;
+            if (key < key_lo || key < lo2 || key > hi2) return;
             const float d = dist(r, z);
             if (!minp_ok(r, z, d)) return;
-            const int sb = (int)((hi - key) >> sh);
+            const int sb = (int)((hi2 - key) >> sh);
             atomicAdd(&s.hcnt[sb], 1u);
             atomicAdd((unsigned long long*)&s.hmass[sb], (unsigned long long)qmass_d(d));
         });
         cluster_reduce_hist(cluster, s, kSubBins, C, cluster.block_rank());
         int jb;
         uint64_t c_at, a_at;
-        scan_bins(s, nsub, cr, nsub - 1, s.hcnt[nsub - 1], s.hmass[nsub - 1], C0, A0, &jb, &c_at, &a_at);
+        scan_bins(s, nsub, cr, C0, A0, &jb, &c_at, &a_at);
         if (jb < 0) jb = 0;
         C0 = c_at;
         A0 = a_at;
-        const uint64_t top = (uint64_t)hi - ((uint64_t)jb << sh);
+        const uint64_t top = (uint64_t)hi2 - ((uint64_t)jb << sh);
         const uint64_t width = (uint64_t)1 << sh;
         const uint64_t bot = (top + 1 >= width) ? top + 1 - width : 0;
         khi = (uint32_t)top;
-        klo = (uint32_t)max((uint64_t)lo, bot);
+        klo = (uint32_t)max((uint64_t)lo2, bot);
     }
-    // Unreachable in practice (each split shrinks the 32-bit range by 2^9); keep a valid answer.
+    // Unreachable in practice (each split shrinks the 32-bit range by 2^8); keep a valid answer.
     Sel o;
     o.key = khi;
     o.cnt = C0;
     o.mass = A0;
     return o;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Few candidates (n <= 32): one warp sorts, cuts and races with shuffles.  Every lane returns the
+// same results.  cnt/off of rank r are in lanes r of `rcnt`, `roff`.
+// ---------------------------------------------------------------------------------------------
+struct WarpResult {
+    uint32_t key_cut;
+    uint32_t nk;
+    uint64_t zk;
+    ArgBest win;
+};
+
+__device__ __forceinline__ WarpResult warp_candidates(cg::cluster_group& cluster, Shared& s, const RowCtx& r,
+                                                      const RaceCtx& rc, uint32_t C, uint32_t rcnt, uint32_t roff,
+                                                      uint32_t n, uint32_t key_cut, bool topk_on, int32_t K,
+                                                      float P)
+{
+    const uint32_t lane = threadIdx.x & 31;
+    // locate this lane's entry: rank rr with roff[rr] <= lane < roff[rr] + rcnt[rr]
+    uint64_t v = 0;
+    {
+        uint32_t my_rank = 0xFFFFFFFFu, my_off = 0;
+        for (uint32_t rr = 0; rr < C; ++rr) {
+            const uint32_t o = __shfl_sync(0xFFFFFFFFu, roff, rr);
+            const uint32_t c = __shfl_sync(0xFFFFFFFFu, rcnt, rr);
+            if (lane >= o && lane < o + c) {
+                my_rank = rr;
+                my_off = lane - o;
+            }
+        }
+        if (lane < n && my_rank != 0xFFFFFFFFu) {
+            const uint32_t k = *cluster.map_shared_rank(&s.ckey[my_off], my_rank);
+            const uint32_t i = *cluster.map_shared_rank(&s.cidx[my_off], my_rank);
+            v = sb_make(k, i);
+        }
+    }
+    // bitonic sort across the warp, descending
+#pragma unroll
+    for (int k2 = 2; k2 <= 32; k2 <<= 1) {
+#pragma unroll
+        for (int j = k2 >> 1; j > 0; j >>= 1) {
+            const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, v, j);
+            const bool desc = (lane & k2) == 0;
+            const bool lower = (lane & j) == 0;
+            // in a descending block the lower lane keeps the larger value
+            const bool take_max = (desc == lower);
+            v = take_max ? (v > o ? v : o) : (v < o ? v : o);
+        }
+    }
+    const uint32_t key = sb_key(v);
+    const int32_t idx = sb_idx(v);
+    const bool valid = lane < n;
+    const float z = key_to_float(key);
+    const float d = dist(r, z);
+    const uint64_t q = valid ? qmass_d(d) : 0;
+    uint64_t inc = q;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if ((int)lane >= o) inc += y;
+    }
+    const uint64_t exc = inc - q;
+    const uint64_t total = __shfl_sync(0xFFFFFFFFu, inc, 31);
+    const uint32_t prev_key = __shfl_up_sync(0xFFFFFFFFu, key, 1);
+    const bool start = valid && (lane == 0 || prev_key != key);
+    auto prefix_at = [&](uint32_t e) -> uint64_t {
+        const uint64_t a = __shfl_sync(0xFFFFFFFFu, exc, e & 31u);
+        return e >= 32 ? total : a;
+    };
+    auto cut = [&](uint32_t lim, bool by_mass, uint64_t tcnt, double tmass, uint32_t* s_out, uint32_t* e_out) {
+        const bool ok = start && lane < lim &&
+                        (by_mass ? ((double)exc < tmass) : ((uint64_t)lane < tcnt));
+        const uint32_t m = __ballot_sync(0xFFFFFFFFu, ok);
+        const uint32_t st = m ? 31u - __clz(m) : 0u;
+        const uint32_t ends = __ballot_sync(0xFFFFFFFFu, start && lane < lim && lane > st);
+        *s_out = st;
+        *e_out = ends ? (uint32_t)(__ffs(ends) - 1) : lim;
+    };
+    uint32_t ns = n;
+    uint64_t zs = total;
+    if (topk_on && n > (uint32_t)K) {
+        uint32_t st, e;
+        cut(n, false, (uint64_t)K, 0.0, &st, &e);
+        key_cut = max(key_cut, __shfl_sync(0xFFFFFFFFu, key, st));
+        ns = e;
+        zs = prefix_at(e);
+    }
+    uint32_t nk = ns;
+    uint64_t zk = zs;
+    if (P < 1.f) {
+        uint32_t st, e;
+        cut(ns, P > 0.f, 1, (double)P * (double)zs, &st, &e);
+        key_cut = max(key_cut, __shfl_sync(0xFFFFFFFFu, key, st));
+        nk = e;
+        zk = prefix_at(e);
+    }
+    // race over lanes < nk
+    const bool kept = lane < nk;
+    float u = 0.f, k32 = -INFINITY;
+    if (kept) {
+        u = race_u(rc, idx);
+        k32 = race_key32(d, u);
+    }
+    float m32 = k32;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m32 = fmaxf(m32, __shfl_xor_sync(0xFFFFFFFFu, m32, o));
+    const float tol = race_tol(dist(r, key_to_float(key_cut)));
+    ArgBest a;
+    a.key = -INFINITY;
+    a.idx = 0x7FFFFFFF;
+    if (kept && k32 >= m32 - tol) {
+        a.key = race_key64(r, z, u);
+        a.idx = idx;
+    }
+    a = warp_argbest(a);
+    WarpResult res;
+    res.key_cut = key_cut;
+    res.nk = nk;
+    res.zk = zk;
+    res.win = a;
+    return res;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -547,6 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_rows_kernel(const Args a)
     const int64_t row = (int64_t)(blockIdx.x / C);
     Shared& s = *reinterpret_cast<Shared*>(dsmem + a.slice_cap);
     const int tid = threadIdx.x;
+    const uint32_t lane = tid & 31;
 
     // ---- geometry: the aligned interior of the row in 16-byte vectors, split evenly over the CTAs
     const unsigned char* rowp = static_cast<const unsigned char*>(a.logits) + row * a.ld * ES;
@@ -570,19 +707,18 @@ __global__ void __launch_bounds__(kThreads, 1) sample_rows_kernel(const Args a)
     sl.nvec = nvec;
     sl.elem0 = nhead + v_lo * EPV;
 
-    // ---- stage the slice: one bulk copy (split in 32 KB pieces) completing on an mbarrier
+    // ---- stage the slice: one bulk copy (in 32 KB pieces) completing on an mbarrier
     const int my_head = (rank == 0) ? (int)nhead : 0;
     const int my_tail = (rank == C - 1) ? (int)ntail : 0;
     if (tid == 0) {
         s.nx = my_head + my_tail;
-        if (bytes > 0) mbar_init(&s.mbar, 1);
-    }
-    __syncthreads();
-    if (tid == 0 && bytes > 0) {
-        mbar_arrive_expect_tx(&s.mbar, bytes);
-        const unsigned char* src = reinterpret_cast<const unsigned char*>(a0) + v_lo * 16;
-        for (uint32_t off = 0; off < bytes; off += 32768u)
-            bulk_g2s(dsmem + off, src + off, min(32768u, bytes - off), &s.mbar);
+        if (bytes > 0) {
+            mbar_init(&s.mbar, 1);
+            mbar_arrive_expect_tx(&s.mbar, bytes);
+            const unsigned char* src = reinterpret_cast<const unsigned char*>(a0) + v_lo * 16;
+            for (uint32_t off = 0; off < bytes; off += 32768u)
+                bulk_g2s(dsmem + off, src + off, min(32768u, bytes - off), &s.mbar);
+        }
     }
     if (tid < my_head) {
         s.xz[tid] = E::load1(rowp, tid);
@@ -592,32 +728,48 @@ __global__ void __launch_bounds__(kThreads, 1) sample_rows_kernel(const Args a)
         s.xz[tid] = E::load1(rowp, i);
         s.xi[tid] = (int32_t)i;
     }
-    uint32_t timed_out = 0;
-    if (bytes > 0 && !mbar_wait_bounded(&s.mbar, 0, kWaitLimitNs)) timed_out = 1;
-    __syncthreads();
-
-    // ---- A: zmax with NaN propagation (a NaN anywhere makes the maximum NaN)
-    float vmax = -INFINITY;
-    if (!timed_out) sl.for_each(s, [&](float z, int32_t) { vmax = fmax_nan(vmax, z); });
-    vmax = block_max_nan(vmax, s);
-    const uint32_t any_to = block_max_u32(timed_out, s);
-    if (tid == 0) {
-        s.pub_max = vmax;
-        s.pub_timeout = any_to;
-    }
-    cluster.sync();
-    float zmax = -INFINITY;
-    uint32_t cl_timeout = 0;
-    for (uint32_t rr = 0; rr < C; ++rr) {
-        zmax = fmax_nan(zmax, *cluster.map_shared_rank(&s.pub_max, rr));
-        cl_timeout |= *cluster.map_shared_rank(&s.pub_timeout, rr);
-    }
-
+    // per-row parameters (read while the copy is in flight)
     const float T = a.temperature[row];
     const float P = a.top_p[row];
     const float MP = a.min_p[row];
     const int32_t K = a.top_k[row];
     const uint64_t seed = a.seed[row];
+    __syncthreads();  // mbarrier initialised, extras stored
+    uint32_t timed_out = 0;
+    if (bytes > 0 && !mbar_wait_bounded(&s.mbar, 0, kWaitLimitNs)) timed_out = 1;
+    timed_out = __syncthreads_or(timed_out) ? 1u : 0u;
+
+    // ---- A: zmax with NaN propagation (a NaN anywhere makes the maximum NaN)
+    float vmax = -INFINITY;
+    if (!timed_out) sl.for_each(s, [&](float z, int32_t) { vmax = fmax_nan(vmax, z); });
+    vmax = warp_max_nan(vmax);
+    if (lane == 0) s.rf[tid >> 5] = vmax;
+    __syncthreads();
+    if (tid == 0) {
+        float m = s.rf[0];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) m = fmax_nan(m, s.rf[w]);
+        s.pub_max = m;
+        s.pub_timeout = timed_out;
+    }
+    cluster.sync();
+    if (tid < 32) {
+        float m = -INFINITY;
+        uint32_t to = 0;
+        if (lane < C) {
+            m = *cluster.map_shared_rank(&s.pub_max, lane);
+            to = *cluster.map_shared_rank(&s.pub_timeout, lane);
+        }
+        m = warp_max_nan(m);
+        to = warp_max_u32(to);
+        if (lane == 0) {
+            s.bf[0] = m;
+            s.bu[0] = to;
+        }
+    }
+    __syncthreads();
+    const float zmax = s.bf[0];
+    const uint32_t cl_timeout = s.bu[0];
 
     int32_t status = kRowOk;
     if (cl_timeout) status = kRowTimeout;
@@ -629,8 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_rows_kernel(const Args a)
     const bool writer = (rank == 0) && (tid == 0);
 
     if (status != kRowOk) {
-        if (prow && !timed_out) sl.for_each(s, [&](float, int32_t i) { prow[i] = 0.f; });
-        if (prow && timed_out) {
+        if (prow) {
             for (int64_t i = sl.elem0 + tid; i < sl.elem0 + (int64_t)nvec * EPV; i += kThreads) prow[i] = 0.f;
             for (int x = tid; x < s.nx; x += kThreads) prow[s.xi[x]] = 0.f;
         }
@@ -656,8 +807,13 @@ __global__ void __launch_bounds__(kThreads, 1) sample_rows_kernel(const Args a)
         mi = block_min_u32(mi, s);
         if (tid == 0) s.pub_minidx = mi;
         cluster.sync();
-        uint32_t arg = 0xFFFFFFFFu;
-        for (uint32_t rr = 0; rr < C; ++rr) arg = min(arg, *cluster.map_shared_rank(&s.pub_minidx, rr));
+        if (tid < 32) {
+            uint32_t m = (lane < C) ? *cluster.map_shared_rank(&s.pub_minidx, lane) : 0xFFFFFFFFu;
+            m = warp_min_u32(m);
+            if (lane == 0) s.bu[1] = m;
+        }
+        __syncthreads();
+        const uint32_t arg = s.bu[1];
         if (prow) sl.for_each(s, [&](float, int32_t i) { prow[i] = ((uint32_t)i == arg) ? 1.f : 0.f; });
         if (writer) {
             a.out_token[row] = (int32_t)arg;
@@ -677,30 +833,40 @@ __global__ void __launch_bounds__(kThreads, 1) sample_rows_kernel(const Args a)
     if (!(r.invT <= FLT_MAX)) r.invT = FLT_MAX;
     r.minp = (MP > 0.f) ? fminf(MP, 1.f) : 0.f;
     r.L_lo = r.L_hi = 0.f;
+    // zc: every token with z <= zc surely fails min-p (d(zc) > L_hi and d is monotone in z).
+    float zc = -INFINITY;
     if (r.minp > 0.f) {
         const float L = -logf(r.minp);
         const float eps = 4e-6f * (1.f + L) + 1e-6f;
         r.L_lo = L - eps;
         r.L_hi = L + eps;
+        float c = zmax - r.L_hi * T;
+        float step = fmaxf(fabsf(c) * 1e-6f, 1e-30f);
+        int it = 0;
+        while (!(dist(r, c) > r.L_hi) && it < 64) {
+            c -= step;
+            step *= 2.f;
+            ++it;
+        }
+        zc = (dist(r, c) > r.L_hi) ? c : -INFINITY;
     }
 
-    // ---- B: min-p survivors -> histogram over d + candidate list
-    for (int b = tid; b < kBins; b += kThreads) {
-        s.hcnt[b] = 0;
-        s.hmass[b] = 0;
-    }
+    RaceCtx rc;
+    rc.k0 = (uint32_t)seed;
+    rc.k1 = (uint32_t)(seed >> 32);
+    rc.row = (uint32_t)row;
+    rc.s_lo = (uint32_t)a.step;
+    rc.s_hi = (uint32_t)(a.step >> 32);
+
+    // ---- B: min-p survivors -> count, smallest key, candidate list
     if (tid == 0) s.ncand = 0;
     __syncthreads();
     uint32_t my_minkey = 0xFFFFFFFFu;
     uint32_t my_surv = 0;
     sl.for_each(s, [&](float z, int32_t i) {
-        if (!(z > -INFINITY)) return;
-        const float d = dist(r, z);
-        if (!minp_ok(r, z, d)) return;
+        if (!(z > zc)) return;
+        if (!minp_ok(r, z, dist(r, z))) return;
         const uint32_t key = fkey(z);
-        const int b = bin_of(d);
-        atomicAdd(&s.hcnt[b], 1u);
-        atomicAdd((unsigned long long*)&s.hmass[b], (unsigned long long)qmass_d(d));
         my_minkey = min(my_minkey, key);
         ++my_surv;
         if (*(volatile uint32_t*)&s.ncand < (uint32_t)kCand) {
@@ -711,42 +877,81 @@ __global__ void __launch_bounds__(kThreads, 1) sample_rows_kernel(const Args a)
             }
         }
     });
-    const uint32_t nsurv = block_sum_u32(my_surv, s);
-    const uint32_t mink = block_min_u32(my_minkey, s);
+    my_surv = warp_sum_u32(my_surv);
+    my_minkey = warp_min_u32(my_minkey);
+    if (lane == 0) {
+        s.ra[tid >> 5] = my_surv;
+        s.rb[tid >> 5] = my_minkey;
+    }
+    __syncthreads();
     if (tid == 0) {
-        s.pub_nsurv = nsurv;
-        s.pub_gcnt = min(nsurv, (uint32_t)kCand);
-        s.pub_minkey = mink;
+        uint32_t ns = 0, mk = 0xFFFFFFFFu;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            ns += s.ra[w];
+            mk = min(mk, s.rb[w]);
+        }
+        s.pub_nsurv = ns;
+        s.pub_gcnt = min(ns, (uint32_t)kCand);
+        s.pub_minkey = mk;
     }
     cluster.sync();
-    uint64_t NS0 = 0;
-    uint32_t key_minp = 0xFFFFFFFFu;
-    for (uint32_t rr = 0; rr < C; ++rr) {
-        NS0 += *cluster.map_shared_rank(&s.pub_nsurv, rr);
-        key_minp = min(key_minp, *cluster.map_shared_rank(&s.pub_minkey, rr));
+    uint32_t rcnt = 0, roff = 0;  // warp 0: lane r holds rank r's list count and offset
+    if (tid < 32) {
+        uint32_t ns = 0, mk = 0xFFFFFFFFu;
+        if (lane < C) {
+            ns = *cluster.map_shared_rank(&s.pub_nsurv, lane);
+            mk = *cluster.map_shared_rank(&s.pub_minkey, lane);
+        }
+        rcnt = min(ns, (uint32_t)kCand);
+        uint32_t inc = rcnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if ((int)lane >= o) inc += y;
+        }
+        roff = inc - rcnt;
+        ns = warp_sum_u32(ns);
+        mk = warp_min_u32(mk);
+        if (lane == 0) {
+            s.bu[2] = ns;
+            s.bu[3] = mk;
+        }
     }
+    __syncthreads();
+    const uint64_t NS0 = s.bu[2];
+    const uint32_t key_minp = s.bu[3];
 
     const bool topk_on = (K > 0) && ((int64_t)K < a.V);
     uint32_t key_cut = key_minp;
     uint64_t NK = NS0, ZK = 0;
-
-    RaceCtx rc;
-    rc.k0 = (uint32_t)seed;
-    rc.k1 = (uint32_t)(seed >> 32);
-    rc.row = (uint32_t)row;
-    rc.s_lo = (uint32_t)a.step;
-    rc.s_hi = (uint32_t)(a.step >> 32);
-
     ArgBest win;
     win.key = -INFINITY;
     win.idx = 0x7FFFFFFF;
 
-    if (NS0 <= (uint64_t)kCand) {
-        // ---- C (few survivors): sort all candidates and walk their classes, in every CTA
+    if (NS0 <= 32) {
+        // ---- C, one warp: every CTA resolves the row redundantly (no further cluster traffic)
+        if (tid < 32) {
+            const WarpResult wr = warp_candidates(cluster, s, r, rc, C, rcnt, roff, (uint32_t)NS0, key_cut, topk_on,
+                                                  K, P);
+            if (lane == 0) {
+                s.bu[4] = wr.key_cut;
+                s.bu[5] = wr.nk;
+                s.b64[0] = wr.zk;
+                s.bab = wr.win;
+            }
+        }
+        __syncthreads();
+        key_cut = s.bu[4];
+        NK = s.bu[5];
+        ZK = s.b64[0];
+        win = s.bab;
+    } else if (NS0 <= (uint64_t)kCand) {
+        // ---- C, whole CTA: sort all candidates and walk their classes, in every CTA
         const int n = gather_and_sort(cluster, s, C);
         prefix_masses(s, r, n);
         int nS = n;
-        uint64_t ZS = s.pre[n];
+        uint64_t ZS = s.u.cd.pre[n];
         if (topk_on && (uint64_t)n > (uint64_t)K) {
             Crit ck;
             ck.by_mass = false;
@@ -770,77 +975,59 @@ __global__ void __launch_bounds__(kThreads, 1) sample_rows_kernel(const Args a)
             ZK = sp.mass;
         }
         // Race over the kept prefix: float keys locate the finalists, double keys decide.
-        const int nk = (int)NK;
-        const float dcut = dist(r, key_to_float(key_cut));
-        const float tol = 1e-5f + 1e-6f * dcut;
-        float k32 = -INFINITY;
-        // kept <= kCand = 4 * kThreads: a thread holds up to 4 entries; keep the best locally.
-        float kk[4];
-        float uu[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int t = tid + j * kThreads;
-            kk[j] = -INFINITY;
-            uu[j] = 0.f;
-            if (t < nk) {
-                const uint64_t v = s.sbuf[t];
-                const float z = key_to_float(sb_key(v));
-                uu[j] = race_u(rc, sb_idx(v));
-                kk[j] = race_key32(dist(r, z), uu[j]);
-                k32 = fmaxf(k32, kk[j]);
-            }
+        const int t = tid;  // NK <= kCand == kThreads
+        float k32 = -INFINITY, u = 0.f, z = 0.f;
+        if (t < (int)NK) {
+            const uint64_t v = s.u.cd.sbuf[t];
+            z = key_to_float(sb_key(v));
+            u = race_u(rc, sb_idx(v));
+            k32 = race_key32(dist(r, z), u);
         }
-        // block max of the float keys
         float m32 = k32;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m32 = fmaxf(m32, __shfl_xor_sync(0xFFFFFFFFu, m32, o));
         __syncthreads();
-        if ((tid & 31) == 0) s.rf[tid >> 5] = m32;
+        if (lane == 0) s.rf[tid >> 5] = m32;
         __syncthreads();
         m32 = s.rf[0];
 #pragma unroll
         for (int w = 1; w < kWarps; ++w) m32 = fmaxf(m32, s.rf[w]);
+        const float tol = race_tol(dist(r, key_to_float(key_cut)));
         ArgBest mine;
         mine.key = -INFINITY;
         mine.idx = 0x7FFFFFFF;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int t = tid + j * kThreads;
-            if (t < nk && kk[j] >= m32 - tol) {
-                const uint64_t v = s.sbuf[t];
-                const double k64 = race_key64(r, key_to_float(sb_key(v)), uu[j]);
-                if (better(k64, sb_idx(v), mine.key, mine.idx)) {
-                    mine.key = k64;
-                    mine.idx = sb_idx(v);
-                }
-            }
+        if (t < (int)NK && k32 >= m32 - tol) {
+            mine.key = race_key64(r, z, u);
+            mine.idx = sb_idx(s.u.cd.sbuf[t]);
         }
         win = block_argbest(mine, s);
-        // optional probabilities over the slice
-        if (prow) {
-            const double zk = (double)ZK;
-            const uint32_t kc = key_cut;
-            sl.for_each(s, [&](float z, int32_t i) {
-                float pv = 0.f;
-                if (z > -INFINITY && fkey(z) >= kc) pv = (float)((double)qmass_d(dist(r, z)) / zk);
-                prow[i] = pv;
-            });
-        }
     } else {
         // ---- C (many survivors): histogram-located cuts, refined exactly
-        cluster_reduce_hist(cluster, s, kBins, C, rank);
-        uint64_t Z0 = 0;
-        {
-            uint64_t m = 0;
-            for (int b = tid; b < kBins; b += kThreads) m += s.hmass[b];
-            uint64_t tot;
-            (void)block_exscan_u64(m, s, &tot);
-            Z0 = tot;
+        for (int b = tid; b < kBins; b += kThreads) {
+            s.hcnt[b] = 0;
+            s.hmass[b] = 0;
         }
-        uint64_t NS = NS0, ZS = Z0;
-        int cap = kBins - 1;
-        uint32_t cap_cnt = s.hcnt[kBins - 1];
-        uint64_t cap_mass = s.hmass[kBins - 1];
+        __syncthreads();
+        auto build_hist = [&](uint32_t key_floor) {
+            sl.for_each(s, [&](float z, int32_t) {
+                if (!(z > zc)) return;
+                if (fkey(z) < key_floor) return;
+                const float d = dist(r, z);
+                if (!minp_ok(r, z, d)) return;
+                const int b = bin_of(d);
+                atomicAdd(&s.hcnt[b], 1u);
+                atomicAdd((unsigned long long*)&s.hmass[b], (unsigned long long)qmass_d(d));
+            });
+        };
+        build_hist(0u);
+        cluster_reduce_hist(cluster, s, kBins, C, rank);
+        uint64_t ZS;
+        {
+            uint64_t tot;
+            (void)block_exscan_u64(s.hmass[tid], s, &tot);  // kBins == kThreads
+            ZS = tot;
+        }
+        uint64_t NS = NS0;
         if (topk_on && NS0 > (uint64_t)K) {
             Crit ck;
             ck.by_mass = false;
@@ -848,35 +1035,22 @@ __global__ void __launch_bounds__(kThreads, 1) sample_rows_kernel(const Args a)
             ck.tmass = 0.0;
             int bk;
             uint64_t c_at, a_at;
-            scan_bins(s, kBins, ck, cap, cap_cnt, cap_mass, 0, 0, &bk, &c_at, &a_at);
+            scan_bins(s, kBins, ck, 0, 0, &bk, &c_at, &a_at);
             if (bk < 0) bk = 0;
-            const Sel sk = refine_bin<TIn>(cluster, s, sl, r, C, bk, 0u, ck, c_at, a_at);
+            const Sel sk = refine_bin<TIn>(cluster, s, sl, r, zc, C, bk, 0u, ck, c_at, a_at);
             key_cut = max(key_cut, sk.key);
             NS = sk.cnt;
             ZS = sk.mass;
-            // The refinement may have reused the histogram; rebuild it over S for the top-p scan.
-            if (P < 1.f) {
+            if (P < 1.f) {  // rebuild the histogram over S = {key >= key_cut} for the top-p scan
                 cluster.sync();
                 for (int b = tid; b < kBins; b += kThreads) {
                     s.hcnt[b] = 0;
                     s.hmass[b] = 0;
                 }
                 __syncthreads();
-                const uint32_t kc = key_cut;
-                sl.for_each(s, [&](float z, int32_t) {
-                    if (!(z > -INFINITY)) return;
-                    if (fkey(z) < kc) return;
-                    const float d = dist(r, z);
-                    if (!minp_ok(r, z, d)) return;
-                    const int b = bin_of(d);
-                    atomicAdd(&s.hcnt[b], 1u);
-                    atomicAdd((unsigned long long*)&s.hmass[b], (unsigned long long)qmass_d(d));
-                });
+                build_hist(key_cut);
                 cluster_reduce_hist(cluster, s, kBins, C, rank);
             }
-            cap = kBins - 1;
-            cap_cnt = s.hcnt[kBins - 1];
-            cap_mass = s.hmass[kBins - 1];
         }
         NK = NS;
         ZK = ZS;
@@ -887,16 +1061,15 @@ __global__ void __launch_bounds__(kThreads, 1) sample_rows_kernel(const Args a)
             cp.tmass = (double)P * (double)ZS;
             int bp;
             uint64_t c_at, a_at;
-            scan_bins(s, kBins, cp, cap, cap_cnt, cap_mass, 0, 0, &bp, &c_at, &a_at);
+            scan_bins(s, kBins, cp, 0, 0, &bp, &c_at, &a_at);
             if (bp < 0) bp = 0;
-            const Sel sp = refine_bin<TIn>(cluster, s, sl, r, C, bp, key_cut, cp, c_at, a_at);
+            const Sel sp = refine_bin<TIn>(cluster, s, sl, r, zc, C, bp, key_cut, cp, c_at, a_at);
             key_cut = max(key_cut, sp.key);
             NK = sp.cnt;
             ZK = sp.mass;
         }
-        // ---- D: race over the kept tokens of the slice (+ probabilities)
-        const float dcut = dist(r, key_to_float(key_cut));
-        const float tol = 1e-5f + 1e-6f * dcut;
+        // ---- race over the kept tokens of the slice (+ probabilities)
+        const float tol = race_tol(dist(r, key_to_float(key_cut)));
         const uint32_t kc = key_cut;
         const double zk = (double)ZK;
         float best32 = -INFINITY;
@@ -924,16 +1097,32 @@ __global__ void __launch_bounds__(kThreads, 1) sample_rows_kernel(const Args a)
             s.pub_idx = mine.idx;
         }
         cluster.sync();
-        for (uint32_t rr = 0; rr < C; ++rr) {
-            const double kq = *cluster.map_shared_rank(&s.pub_k64, rr);
-            const int32_t iq = *cluster.map_shared_rank(&s.pub_idx, rr);
-            if (better(kq, iq, win.key, win.idx)) {
-                win.key = kq;
-                win.idx = iq;
+        if (tid < 32) {
+            ArgBest x;
+            x.key = -INFINITY;
+            x.idx = 0x7FFFFFFF;
+            if (lane < C) {
+                x.key = *cluster.map_shared_rank(&s.pub_k64, lane);
+                x.idx = *cluster.map_shared_rank(&s.pub_idx, lane);
             }
+            x = warp_argbest(x);
+            if (lane == 0) s.bab = x;
         }
+        __syncthreads();
+        win = s.bab;
+        prow = nullptr;  // already written
     }
 
+    // ---- D: optional probabilities over the slice
+    if (prow) {
+        const double zk = (double)ZK;
+        const uint32_t kc = key_cut;
+        sl.for_each(s, [&](float z, int32_t i) {
+            float pv = 0.f;
+            if (z > -INFINITY && fkey(z) >= kc) pv = (float)((double)qmass_d(dist(r, z)) / zk);
+            prow[i] = pv;
+        });
+    }
     if (writer) {
         a.out_token[row] = win.idx;
         if (a.out_status) a.out_status[row] = kRowOk;

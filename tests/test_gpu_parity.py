@@ -60,7 +60,9 @@ def test_decode_full_size_sampled_rows():
 @pytest.mark.parametrize("V", [128256, 256000])
 def test_sweep_large_rows_sampled(V):
     w = workloads.make("sweep", device="cpu", B=64, V=V, dtype=torch.bfloat16 if V == 256000 else torch.float32)
-    check(w, rows=np.arange(0, 64, 4))
+    # wide nuclei over 128k-256k tokens: neighbouring classes differ by ~1e-5 of the mass, so many
+    # rows have a class within 1e-6 of p (boundary rows, excluded from the exact checks)
+    check(w, rows=np.arange(0, 64, 4), max_band_frac=0.6)
 
 
 def test_tiny_vocabularies_grid():
@@ -158,13 +160,13 @@ def test_sampled_distribution_million_draws():
     probs = np.array([0.30, 0.25, 0.25, 0.12, 0.08])
     n = 1_000_000
     z = np.tile(np.log(probs), (n, 1))
-    w = _w(z, 1.0, 0, 0.95, 0.0, seed=np.arange(n, dtype=np.int64) * 7919 + 5, step=3)
+    w = _w(z, 1.0, 0, 0.9, 0.0, seed=np.arange(n, dtype=np.int64) * 7919 + 5, step=3)
     g = _parity.run_gpu(w, want_probs=False)
     o = _parity.run_oracle(w, want_probs=False)
     tok = g["token"].numpy()
     eq = tok == o["token"]
     assert eq.mean() == 1.0 or eq[(o["flags"] & 4) == 0].all()
-    exact = probs[:4] / probs[:4].sum()  # p = 0.95 keeps the first four
+    exact = probs[:4] / probs[:4].sum()  # p = 0.9 keeps the first four (mass above 0.08 is 0.92)
     freq = np.bincount(tok, minlength=5) / n
     assert freq[4] == 0
     tv = 0.5 * np.abs(freq[:4] - exact).sum()
