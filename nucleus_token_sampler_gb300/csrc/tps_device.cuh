@@ -188,6 +188,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
 }
 
+// Split cluster barrier: arrive (release this CTA's prior shared-memory writes and reads), wait
+// (acquire).  Every thread of every CTA of the cluster executes both, in order.
+__device__ __forceinline__ void cluster_arrive()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // max with NaN propagation (a NaN anywhere in the row survives the reduction).
 __device__ __forceinline__ float fmax_nan(float a, float b)
 {

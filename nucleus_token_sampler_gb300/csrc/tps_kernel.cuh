@@ -196,15 +196,32 @@ struct Slice {
     int nvec;
     int64_t elem0;     // row index of the first element of vec[0]
 
-    // Apply f(z, i) to every element of the slice (vectors, then the ragged extras).
+    // Apply f(z, i) to every element of the slice (vectors, then the ragged extras).  Four vectors
+    // are loaded before any of them is processed, so the shared-memory latency overlaps even when f
+    // holds atomics.
     template <typename F>
     __device__ __forceinline__ void for_each(const Shared& s, F&& f) const
     {
         using E = Elem<TIn>;
-        for (int v = threadIdx.x; v < nvec; v += kThreads) {
+        constexpr int U = 4;
+        int v = threadIdx.x;
+        for (; v + (U - 1) * kThreads < nvec; v += U * kThreads) {
+            uint4 w[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) w[u] = vec[v + u * kThreads];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                float z[E::kPerVec];
+                E::unpack(w[u], z);
+                const int32_t i0 = (int32_t)elem0 + (v + u * kThreads) * E::kPerVec;
+#pragma unroll
+                for (int j = 0; j < E::kPerVec; ++j) f(z[j], i0 + j);
+            }
+        }
+        for (; v < nvec; v += kThreads) {
             float z[E::kPerVec];
             E::unpack(vec[v], z);
-            const int32_t i0 = (int32_t)(elem0 + (int64_t)v * E::kPerVec);
+            const int32_t i0 = (int32_t)elem0 + v * E::kPerVec;
 #pragma unroll
             for (int j = 0; j < E::kPerVec; ++j) f(z[j], i0 + j);
         }
@@ -545,50 +562,32 @@ __device__ Sel refine_bin(cg::cluster_group& cluster, Shared& s, const Slice<TIn
 }
 
 // ---------------------------------------------------------------------------------------------
-// Few candidates (n <= 32): one warp sorts, cuts and races with shuffles.  Every lane returns the
-// same results.  cnt/off of rank r are in lanes r of `rcnt`, `roff`.
+// Exponential race, decided exactly.  Float keys rank the kept tokens; when the best float key
+// leads every other by more than the float/double error margin, it is the double-precision argmax
+// too.  Only near-ties (two keys within the margin) are re-evaluated in double precision, exactly
+// as the float64 definition computes them, with the lowest index winning equal keys.
 // ---------------------------------------------------------------------------------------------
 struct WarpResult {
     uint32_t key_cut;
     uint32_t nk;
     uint64_t zk;
-    ArgBest win;
+    int32_t token;
 };
 
-__device__ __forceinline__ WarpResult warp_candidates(cg::cluster_group& cluster, Shared& s, const RowCtx& r,
-                                                      const RaceCtx& rc, uint32_t C, uint32_t rcnt, uint32_t roff,
-                                                      uint32_t n, uint32_t key_cut, bool topk_on, int32_t K,
-                                                      float P)
+// Resolve a row whose survivors are u.cd.sbuf[0, n) (n <= 32, unsorted) with one warp.  Every
+// lane returns the same result.
+__device__ __forceinline__ WarpResult warp_resolve(const Shared& s, const RowCtx& r, const RaceCtx& rc, uint32_t n,
+                                                   bool topk_on, int32_t K, float P)
 {
     const uint32_t lane = threadIdx.x & 31;
-    // locate this lane's entry: rank rr with roff[rr] <= lane < roff[rr] + rcnt[rr]
-    uint64_t v = 0;
-    {
-        uint32_t my_rank = 0xFFFFFFFFu, my_off = 0;
-        for (uint32_t rr = 0; rr < C; ++rr) {
-            const uint32_t o = __shfl_sync(0xFFFFFFFFu, roff, rr);
-            const uint32_t c = __shfl_sync(0xFFFFFFFFu, rcnt, rr);
-            if (lane >= o && lane < o + c) {
-                my_rank = rr;
-                my_off = lane - o;
-            }
-        }
-        if (lane < n && my_rank != 0xFFFFFFFFu) {
-            const uint32_t k = *cluster.map_shared_rank(&s.ckey[my_off], my_rank);
-            const uint32_t i = *cluster.map_shared_rank(&s.cidx[my_off], my_rank);
-            v = sb_make(k, i);
-        }
-    }
+    uint64_t v = (lane < n) ? s.u.cd.sbuf[lane] : 0;
     // bitonic sort across the warp, descending
 #pragma unroll
     for (int k2 = 2; k2 <= 32; k2 <<= 1) {
 #pragma unroll
         for (int j = k2 >> 1; j > 0; j >>= 1) {
             const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, v, j);
-            const bool desc = (lane & k2) == 0;
-            const bool lower = (lane & j) == 0;
-            // in a descending block the lower lane keeps the larger value
-            const bool take_max = (desc == lower);
+            const bool take_max = ((lane & k2) == 0) == ((lane & j) == 0);
             v = take_max ? (v > o ? v : o) : (v < o ? v : o);
         }
     }
@@ -609,16 +608,16 @@ __device__ __forceinline__ WarpResult warp_candidates(cg::cluster_group& cluster
     const uint32_t prev_key = __shfl_up_sync(0xFFFFFFFFu, key, 1);
     const bool start = valid && (lane == 0 || prev_key != key);
     auto prefix_at = [&](uint32_t e) -> uint64_t {
-        const uint64_t a = __shfl_sync(0xFFFFFFFFu, exc, e & 31u);
-        return e >= 32 ? total : a;
+        const uint64_t x = __shfl_sync(0xFFFFFFFFu, exc, e & 31u);
+        return e >= 32 ? total : x;
     };
-    auto cut = [&](uint32_t lim, bool by_mass, uint64_t tcnt, double tmass, uint32_t* s_out, uint32_t* e_out) {
-        const bool ok = start && lane < lim &&
-                        (by_mass ? ((double)exc < tmass) : ((uint64_t)lane < tcnt));
+    // last class start in [0, lim) satisfying the criterion, and the end of that class
+    auto cut = [&](uint32_t lim, bool by_mass, uint64_t tcnt, double tmass, uint32_t* st_out, uint32_t* e_out) {
+        const bool ok = start && lane < lim && (by_mass ? ((double)exc < tmass) : ((uint64_t)lane < tcnt));
         const uint32_t m = __ballot_sync(0xFFFFFFFFu, ok);
         const uint32_t st = m ? 31u - __clz(m) : 0u;
         const uint32_t ends = __ballot_sync(0xFFFFFFFFu, start && lane < lim && lane > st);
-        *s_out = st;
+        *st_out = st;
         *e_out = ends ? (uint32_t)(__ffs(ends) - 1) : lim;
     };
     uint32_t ns = n;
@@ -626,7 +625,6 @@ __device__ __forceinline__ WarpResult warp_candidates(cg::cluster_group& cluster
     if (topk_on && n > (uint32_t)K) {
         uint32_t st, e;
         cut(n, false, (uint64_t)K, 0.0, &st, &e);
-        key_cut = max(key_cut, __shfl_sync(0xFFFFFFFFu, key, st));
         ns = e;
         zs = prefix_at(e);
     }
@@ -635,10 +633,10 @@ __device__ __forceinline__ WarpResult warp_candidates(cg::cluster_group& cluster
     if (P < 1.f) {
         uint32_t st, e;
         cut(ns, P > 0.f, 1, (double)P * (double)zs, &st, &e);
-        key_cut = max(key_cut, __shfl_sync(0xFFFFFFFFu, key, st));
         nk = e;
         zk = prefix_at(e);
     }
+    const uint32_t key_cut = __shfl_sync(0xFFFFFFFFu, key, (nk - 1) & 31u);
     // race over lanes < nk
     const bool kept = lane < nk;
     float u = 0.f, k32 = -INFINITY;
@@ -650,27 +648,78 @@ __device__ __forceinline__ WarpResult warp_candidates(cg::cluster_group& cluster
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m32 = fmaxf(m32, __shfl_xor_sync(0xFFFFFFFFu, m32, o));
     const float tol = race_tol(dist(r, key_to_float(key_cut)));
-    ArgBest a;
-    a.key = -INFINITY;
-    a.idx = 0x7FFFFFFF;
-    if (kept && k32 >= m32 - tol) {
-        a.key = race_key64(r, z, u);
-        a.idx = idx;
+    const bool fin = kept && k32 >= m32 - tol;
+    const uint32_t fm = __ballot_sync(0xFFFFFFFFu, fin);
+    int32_t token;
+    if (__popc(fm) == 1) {
+        token = __shfl_sync(0xFFFFFFFFu, idx, __ffs(fm) - 1);
+    } else {
+        ArgBest a;
+        a.key = -INFINITY;
+        a.idx = 0x7FFFFFFF;
+        if (fin) {
+            a.key = race_key64(r, z, u);
+            a.idx = idx;
+        }
+        token = warp_argbest(a).idx;
     }
-    a = warp_argbest(a);
     WarpResult res;
     res.key_cut = key_cut;
     res.nk = nk;
     res.zk = zk;
-    res.win = a;
+    res.token = token;
     return res;
+}
+
+// Best and second-best float race keys (and the best's index) over a set of tokens.
+struct Top2 {
+    float k1, k2;
+    int32_t i1;
+    __device__ __forceinline__ void init()
+    {
+        k1 = k2 = -INFINITY;
+        i1 = 0x7FFFFFFF;
+    }
+    __device__ __forceinline__ void add(float k, int32_t i)
+    {
+        if (k > k1 || (k == k1 && (uint32_t)i < (uint32_t)i1)) {
+            k2 = k1;
+            k1 = k;
+            i1 = i;
+        } else if (k > k2) {
+            k2 = k;
+        }
+    }
+    __device__ __forceinline__ void merge(const Top2& o)
+    {
+        if (o.k1 > k1 || (o.k1 == k1 && (uint32_t)o.i1 < (uint32_t)i1)) {
+            k2 = fmaxf(k1, o.k2);
+            k1 = o.k1;
+            i1 = o.i1;
+        } else {
+            k2 = fmaxf(k2, o.k1);
+        }
+    }
+};
+
+__device__ __forceinline__ Top2 warp_top2(Top2 t)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        Top2 x;
+        x.k1 = __shfl_xor_sync(0xFFFFFFFFu, t.k1, o);
+        x.k2 = __shfl_xor_sync(0xFFFFFFFFu, t.k2, o);
+        x.i1 = __shfl_xor_sync(0xFFFFFFFFu, t.i1, o);
+        t.merge(x);
+    }
+    return t;
 }
 
 // ---------------------------------------------------------------------------------------------
 // The kernel.  Grid: B * C CTAs in clusters of C along x; cluster q samples row q.
 // ---------------------------------------------------------------------------------------------
 template <typename TIn>
-__global__ void __launch_bounds__(kThreads, 1) sample_rows_kernel(const Args a)
+__global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
 {
     using E = Elem<TIn>;
     constexpr int EPV = E::kPerVec;
@@ -734,47 +783,123 @@ __global__ void __launch_bounds__(kThreads, 1) sample_rows_kernel(const Args a)
     const float MP = a.min_p[row];
     const int32_t K = a.top_k[row];
     const uint64_t seed = a.seed[row];
+    const bool params_ok = isfinite(T) && isfinite(P) && isfinite(MP);
+    const bool sampling = params_ok && T > 0.f;
+    const float minp = (MP > 0.f) ? fminf(MP, 1.f) : 0.f;
     __syncthreads();  // mbarrier initialised, extras stored
     uint32_t timed_out = 0;
     if (bytes > 0 && !mbar_wait_bounded(&s.mbar, 0, kWaitLimitNs)) timed_out = 1;
     timed_out = __syncthreads_or(timed_out) ? 1u : 0u;
 
-    // ---- A: zmax with NaN propagation (a NaN anywhere makes the maximum NaN)
+    // ---- A: local maximum with NaN propagation (a NaN anywhere makes the maximum NaN)
     float vmax = -INFINITY;
     if (!timed_out) sl.for_each(s, [&](float z, int32_t) { vmax = fmax_nan(vmax, z); });
     vmax = warp_max_nan(vmax);
     if (lane == 0) s.rf[tid >> 5] = vmax;
     __syncthreads();
-    if (tid == 0) {
-        float m = s.rf[0];
+    float mloc = s.rf[0];
 #pragma unroll
-        for (int w = 1; w < kWarps; ++w) m = fmax_nan(m, s.rf[w]);
-        s.pub_max = m;
+    for (int w = 1; w < kWarps; ++w) mloc = fmax_nan(mloc, s.rf[w]);
+
+    // ---- B (local): list every token above a threshold that min-p relative to the LOCAL maximum
+    //      already rejects; the global maximum is >= the local one, so the lists cover every
+    //      survivor of the row.  Without min-p nothing can be excluded and no list is built.
+    auto make_ctx = [&](float zm) {
+        RowCtx r;
+        r.zmax = zm;
+        r.T = T;
+        r.invT = 1.f / T;
+        if (!(r.invT <= FLT_MAX)) r.invT = FLT_MAX;
+        r.minp = minp;
+        r.L_lo = r.L_hi = 0.f;
+        if (minp > 0.f) {
+            const float L = -logf(minp);
+            const float eps = 4e-6f * (1.f + L) + 1e-6f;
+            r.L_lo = L - eps;
+            r.L_hi = L + eps;
+        }
+        return r;
+    };
+    // zc: every token with z <= zc surely fails min-p (d(zc) > L_hi and d is monotone in z).
+    auto threshold = [&](const RowCtx& r) -> float {
+        if (!(r.minp > 0.f)) return -INFINITY;
+        float c = r.zmax - r.L_hi * r.T;
+        float step = fmaxf(fabsf(c) * 1e-6f, 1e-30f);
+        int it = 0;
+        while (!(dist(r, c) > r.L_hi) && it < 64) {
+            c -= step;
+            step *= 2.f;
+            ++it;
+        }
+        return (dist(r, c) > r.L_hi) ? c : -INFINITY;
+    };
+    const bool local_ok = sampling && !timed_out && minp > 0.f && mloc > -INFINITY && mloc < INFINITY;
+    uint32_t nlisted = 0xFFFFFFFFu;  // "no complete list"
+    if (sampling && !timed_out && minp > 0.f && mloc == -INFINITY) nlisted = 0;  // nothing finite here
+    if (local_ok) {
+        const RowCtx rl = make_ctx(mloc);
+        const float zc_loc = threshold(rl);
+        if (tid == 0) s.ncand = 0;
+        __syncthreads();
+        if (zc_loc > -INFINITY) {
+            sl.for_each(s, [&](float z, int32_t i) {
+                if (!(z > zc_loc)) return;
+                const uint32_t slot = atomicAdd(&s.ncand, 1u);
+                if (slot < (uint32_t)kCand) {
+                    s.ckey[slot] = fkey(z);
+                    s.cidx[slot] = (uint32_t)i;
+                }
+            });
+            __syncthreads();
+            nlisted = s.ncand;
+        }
+    }
+    if (tid == 0) {
+        s.pub_max = mloc;
         s.pub_timeout = timed_out;
+        s.pub_nsurv = nlisted;  // 0xFFFFFFFF or > kCand: this CTA's list is not complete
+        s.pub_gcnt = min(nlisted, (uint32_t)kCand);
     }
     cluster.sync();
     if (tid < 32) {
         float m = -INFINITY;
-        uint32_t to = 0;
+        uint32_t to = 0, nl = 0, cnt = 0, bad = 0;
         if (lane < C) {
             m = *cluster.map_shared_rank(&s.pub_max, lane);
             to = *cluster.map_shared_rank(&s.pub_timeout, lane);
+            nl = *cluster.map_shared_rank(&s.pub_nsurv, lane);
+            bad = nl > (uint32_t)kCand;
+            cnt = bad ? 0u : nl;
+        }
+        uint32_t inc = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if ((int)lane >= o) inc += y;
+        }
+        if (lane < C) {
+            s.goff[lane] = inc - cnt;
+            s.gcnt[lane] = cnt;
         }
         m = warp_max_nan(m);
         to = warp_max_u32(to);
+        bad = warp_max_u32(bad);
+        if (lane == 31) s.gtotal = inc;
         if (lane == 0) {
             s.bf[0] = m;
             s.bu[0] = to;
+            s.bu[1] = bad;
         }
     }
     __syncthreads();
     const float zmax = s.bf[0];
     const uint32_t cl_timeout = s.bu[0];
+    const bool lists_complete = (s.bu[1] == 0) && (s.gtotal <= (uint32_t)kCand);
 
     int32_t status = kRowOk;
     if (cl_timeout) status = kRowTimeout;
     else if (isnan(zmax) || zmax == INFINITY) status = kRowNan;
-    else if (!isfinite(T) || !isfinite(P) || !isfinite(MP)) status = kRowBadParam;
+    else if (!params_ok) status = kRowBadParam;
     else if (zmax == -INFINITY) status = kRowAllMasked;
 
     float* prow = a.out_probs ? a.out_probs + row * a.V : nullptr;
@@ -810,10 +935,10 @@ __global__ void __launch_bounds__(kThreads, 1) sample_rows_kernel(const Args a)
         if (tid < 32) {
             uint32_t m = (lane < C) ? *cluster.map_shared_rank(&s.pub_minidx, lane) : 0xFFFFFFFFu;
             m = warp_min_u32(m);
-            if (lane == 0) s.bu[1] = m;
+            if (lane == 0) s.bu[2] = m;
         }
         __syncthreads();
-        const uint32_t arg = s.bu[1];
+        const uint32_t arg = s.bu[2];
         if (prow) sl.for_each(s, [&](float, int32_t i) { prow[i] = ((uint32_t)i == arg) ? 1.f : 0.f; });
         if (writer) {
             a.out_token[row] = (int32_t)arg;
@@ -825,31 +950,9 @@ __global__ void __launch_bounds__(kThreads, 1) sample_rows_kernel(const Args a)
         return;
     }
 
-    // ---- row constants
-    RowCtx r;
-    r.zmax = zmax;
-    r.T = T;
-    r.invT = 1.f / T;
-    if (!(r.invT <= FLT_MAX)) r.invT = FLT_MAX;
-    r.minp = (MP > 0.f) ? fminf(MP, 1.f) : 0.f;
-    r.L_lo = r.L_hi = 0.f;
-    // zc: every token with z <= zc surely fails min-p (d(zc) > L_hi and d is monotone in z).
-    float zc = -INFINITY;
-    if (r.minp > 0.f) {
-        const float L = -logf(r.minp);
-        const float eps = 4e-6f * (1.f + L) + 1e-6f;
-        r.L_lo = L - eps;
-        r.L_hi = L + eps;
-        float c = zmax - r.L_hi * T;
-        float step = fmaxf(fabsf(c) * 1e-6f, 1e-30f);
-        int it = 0;
-        while (!(dist(r, c) > r.L_hi) && it < 64) {
-            c -= step;
-            step *= 2.f;
-            ++it;
-        }
-        zc = (dist(r, c) > r.L_hi) ? c : -INFINITY;
-    }
+    const RowCtx r = make_ctx(zmax);
+    const float zc = threshold(r);
+    const bool topk_on = (K > 0) && ((int64_t)K < a.V);
 
     RaceCtx rc;
     rc.k0 = (uint32_t)seed;
@@ -858,7 +961,130 @@ __global__ void __launch_bounds__(kThreads, 1) sample_rows_kernel(const Args a)
     rc.s_lo = (uint32_t)a.step;
     rc.s_hi = (uint32_t)(a.step >> 32);
 
-    // ---- B: min-p survivors -> count, smallest key, candidate list
+    uint32_t key_cut;
+    uint64_t NK, ZK;
+    int32_t token;
+
+    if (lists_complete) {
+        // ================= fast path: every survivor is on some CTA's list =================
+        // Gather the lists (one entry per thread), keep the survivors of min-p against the global
+        // maximum.  This is the last read of another CTA's shared memory.
+        if (tid == 0) s.ncand = 0;
+        __syncthreads();
+        const uint32_t total = s.gtotal;
+        if ((uint32_t)tid < total) {
+            uint32_t rr = 0;
+            while (rr + 1 < C && s.goff[rr + 1] <= (uint32_t)tid) ++rr;
+            const uint32_t off = (uint32_t)tid - s.goff[rr];
+            const uint32_t key = *cluster.map_shared_rank(&s.ckey[off], rr);
+            const uint32_t idx = *cluster.map_shared_rank(&s.cidx[off], rr);
+            const float z = key_to_float(key);
+            if (z > zc && minp_ok(r, z, dist(r, z))) {
+                const uint32_t slot = atomicAdd(&s.ncand, 1u);
+                s.u.cd.sbuf[slot] = sb_make(key, idx);
+            }
+        }
+        cluster_arrive();  // no more remote reads by this CTA; waited for just before exit
+        __syncthreads();
+        const uint32_t n = s.ncand;
+        if (n <= 32) {
+            if (tid < 32) {
+                const WarpResult wr = warp_resolve(s, r, rc, n, topk_on, K, P);
+                if (lane == 0) {
+                    s.bu[4] = wr.key_cut;
+                    s.bu[5] = wr.nk;
+                    s.b64[0] = wr.zk;
+                    s.bu[6] = (uint32_t)wr.token;
+                }
+            }
+            __syncthreads();
+            key_cut = s.bu[4];
+            NK = s.bu[5];
+            ZK = s.b64[0];
+            token = (int32_t)s.bu[6];
+        } else {
+            block_sort_desc(s, (int)n);
+            prefix_masses(s, r, (int)n);
+            int nS = (int)n;
+            uint64_t ZS = s.u.cd.pre[n];
+            if (topk_on && n > (uint32_t)K) {
+                Crit ck;
+                ck.by_mass = false;
+                ck.tcnt = (uint64_t)K;
+                ck.tmass = 0.0;
+                const Sel sk = walk_classes(s, (int)n, ck, 0, 0);
+                nS = (int)sk.cnt;
+                ZS = sk.mass;
+            }
+            NK = (uint64_t)nS;
+            ZK = ZS;
+            if (P < 1.f) {
+                Crit cp;
+                cp.by_mass = P > 0.f;
+                cp.tcnt = 1;
+                cp.tmass = (double)P * (double)ZS;
+                const Sel sp = walk_classes(s, nS, cp, 0, 0);
+                NK = sp.cnt;
+                ZK = sp.mass;
+            }
+            key_cut = sb_key(s.u.cd.sbuf[NK - 1]);
+            // race over the kept prefix (one entry per thread: n <= kCand == kThreads)
+            float k32 = -INFINITY, u = 0.f, z = 0.f;
+            int32_t idx = 0x7FFFFFFF;
+            if (tid < (int)NK) {
+                const uint64_t v = s.u.cd.sbuf[tid];
+                z = key_to_float(sb_key(v));
+                idx = sb_idx(v);
+                u = race_u(rc, idx);
+                k32 = race_key32(dist(r, z), u);
+            }
+            float m32 = k32;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m32 = fmaxf(m32, __shfl_xor_sync(0xFFFFFFFFu, m32, o));
+            if (lane == 0) s.rf[tid >> 5] = m32;
+            __syncthreads();
+            m32 = s.rf[0];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) m32 = fmaxf(m32, s.rf[w]);
+            const float tol = race_tol(dist(r, key_to_float(key_cut)));
+            const bool fin = tid < (int)NK && k32 >= m32 - tol;
+            const int nfin = __syncthreads_count(fin);
+            if (nfin == 1) {
+                if (fin) s.bu[6] = (uint32_t)idx;
+                __syncthreads();
+                token = (int32_t)s.bu[6];
+            } else {
+                ArgBest mine;
+                mine.key = -INFINITY;
+                mine.idx = 0x7FFFFFFF;
+                if (fin) {
+                    mine.key = race_key64(r, z, u);
+                    mine.idx = idx;
+                }
+                token = block_argbest(mine, s).idx;
+            }
+        }
+        if (prow) {
+            const double zk = (double)ZK;
+            const uint32_t kc = key_cut;
+            sl.for_each(s, [&](float z, int32_t i) {
+                float pv = 0.f;
+                if (z > -INFINITY && fkey(z) >= kc) pv = (float)((double)qmass_d(dist(r, z)) / zk);
+                prow[i] = pv;
+            });
+        }
+        if (writer) {
+            a.out_token[row] = token;
+            if (a.out_status) a.out_status[row] = kRowOk;
+            if (a.out_cutoff) a.out_cutoff[row] = key_to_float(key_cut);
+            if (a.out_kept) a.out_kept[row] = (int32_t)NK;
+        }
+        cluster_wait();  // every CTA has finished reading this CTA's lists
+        return;
+    }
+
+    // ================= general path: survivors against the global maximum =================
+    cluster.sync();  // nobody still reads the local lists or the published values
     if (tid == 0) s.ncand = 0;
     __syncthreads();
     uint32_t my_minkey = 0xFFFFFFFFu;
@@ -896,21 +1122,12 @@ __global__ void __launch_bounds__(kThreads, 1) sample_rows_kernel(const Args a)
         s.pub_minkey = mk;
     }
     cluster.sync();
-    uint32_t rcnt = 0, roff = 0;  // warp 0: lane r holds rank r's list count and offset
     if (tid < 32) {
         uint32_t ns = 0, mk = 0xFFFFFFFFu;
         if (lane < C) {
             ns = *cluster.map_shared_rank(&s.pub_nsurv, lane);
             mk = *cluster.map_shared_rank(&s.pub_minkey, lane);
         }
-        rcnt = min(ns, (uint32_t)kCand);
-        uint32_t inc = rcnt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-            if ((int)lane >= o) inc += y;
-        }
-        roff = inc - rcnt;
         ns = warp_sum_u32(ns);
         mk = warp_min_u32(mk);
         if (lane == 0) {
@@ -920,34 +1137,11 @@ __global__ void __launch_bounds__(kThreads, 1) sample_rows_kernel(const Args a)
     }
     __syncthreads();
     const uint64_t NS0 = s.bu[2];
-    const uint32_t key_minp = s.bu[3];
-
-    const bool topk_on = (K > 0) && ((int64_t)K < a.V);
-    uint32_t key_cut = key_minp;
-    uint64_t NK = NS0, ZK = 0;
-    ArgBest win;
-    win.key = -INFINITY;
-    win.idx = 0x7FFFFFFF;
-
-    if (NS0 <= 32) {
-        // ---- C, one warp: every CTA resolves the row redundantly (no further cluster traffic)
-        if (tid < 32) {
-            const WarpResult wr = warp_candidates(cluster, s, r, rc, C, rcnt, roff, (uint32_t)NS0, key_cut, topk_on,
-                                                  K, P);
-            if (lane == 0) {
-                s.bu[4] = wr.key_cut;
-                s.bu[5] = wr.nk;
-                s.b64[0] = wr.zk;
-                s.bab = wr.win;
-            }
-        }
-        __syncthreads();
-        key_cut = s.bu[4];
-        NK = s.bu[5];
-        ZK = s.b64[0];
-        win = s.bab;
-    } else if (NS0 <= (uint64_t)kCand) {
-        // ---- C, whole CTA: sort all candidates and walk their classes, in every CTA
+    key_cut = s.bu[3];
+    NK = NS0;
+    ZK = 0;
+    if (NS0 <= (uint64_t)kCand) {
+        // ---- few survivors after all (the local lists overflowed): sort them in every CTA
         const int n = gather_and_sort(cluster, s, C);
         prefix_masses(s, r, n);
         int nS = n;
@@ -958,7 +1152,6 @@ __global__ void __launch_bounds__(kThreads, 1) sample_rows_kernel(const Args a)
             ck.tcnt = (uint64_t)K;
             ck.tmass = 0.0;
             const Sel sk = walk_classes(s, n, ck, 0, 0);
-            key_cut = max(key_cut, sk.key);
             nS = (int)sk.cnt;
             ZS = sk.mass;
         }
@@ -970,39 +1163,12 @@ __global__ void __launch_bounds__(kThreads, 1) sample_rows_kernel(const Args a)
             cp.tcnt = 1;
             cp.tmass = (double)P * (double)ZS;
             const Sel sp = walk_classes(s, nS, cp, 0, 0);
-            key_cut = max(key_cut, sp.key);
             NK = sp.cnt;
             ZK = sp.mass;
         }
-        // Race over the kept prefix: float keys locate the finalists, double keys decide.
-        const int t = tid;  // NK <= kCand == kThreads
-        float k32 = -INFINITY, u = 0.f, z = 0.f;
-        if (t < (int)NK) {
-            const uint64_t v = s.u.cd.sbuf[t];
-            z = key_to_float(sb_key(v));
-            u = race_u(rc, sb_idx(v));
-            k32 = race_key32(dist(r, z), u);
-        }
-        float m32 = k32;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m32 = fmaxf(m32, __shfl_xor_sync(0xFFFFFFFFu, m32, o));
-        __syncthreads();
-        if (lane == 0) s.rf[tid >> 5] = m32;
-        __syncthreads();
-        m32 = s.rf[0];
-#pragma unroll
-        for (int w = 1; w < kWarps; ++w) m32 = fmaxf(m32, s.rf[w]);
-        const float tol = race_tol(dist(r, key_to_float(key_cut)));
-        ArgBest mine;
-        mine.key = -INFINITY;
-        mine.idx = 0x7FFFFFFF;
-        if (t < (int)NK && k32 >= m32 - tol) {
-            mine.key = race_key64(r, z, u);
-            mine.idx = sb_idx(s.u.cd.sbuf[t]);
-        }
-        win = block_argbest(mine, s);
+        key_cut = sb_key(s.u.cd.sbuf[NK - 1]);
     } else {
-        // ---- C (many survivors): histogram-located cuts, refined exactly
+        // ---- many survivors: histogram-located cuts, refined exactly
         for (int b = tid; b < kBins; b += kThreads) {
             s.hcnt[b] = 0;
             s.hmass[b] = 0;
@@ -1068,30 +1234,80 @@ __global__ void __launch_bounds__(kThreads, 1) sample_rows_kernel(const Args a)
             NK = sp.cnt;
             ZK = sp.mass;
         }
-        // ---- race over the kept tokens of the slice (+ probabilities)
-        const float tol = race_tol(dist(r, key_to_float(key_cut)));
-        const uint32_t kc = key_cut;
-        const double zk = (double)ZK;
-        float best32 = -INFINITY;
+    }
+
+    // ---- race over the kept tokens of the slice (+ probabilities): float keys first; the
+    //      cluster's best two decide whether double precision is needed at all
+    const float tol = race_tol(dist(r, key_to_float(key_cut)));
+    const uint32_t kc = key_cut;
+    const double zk = (double)ZK;
+    Top2 t2;
+    t2.init();
+    sl.for_each(s, [&](float z, int32_t i) {
+        const bool kept = (z > -INFINITY) && fkey(z) >= kc;
+        if (prow) prow[i] = kept ? (float)((double)qmass_d(dist(r, z)) / zk) : 0.f;
+        if (!kept) return;
+        t2.add(race_key32(dist(r, z), race_u(rc, i)), i);
+    });
+    t2 = warp_top2(t2);
+    __syncthreads();
+    if (lane == 0) {
+        s.rab[tid >> 5].key = (double)t2.k1;
+        s.rab[tid >> 5].idx = t2.i1;
+        s.rf[tid >> 5] = t2.k2;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        Top2 b;
+        b.init();
+        for (int w = 0; w < kWarps; ++w) {
+            Top2 x;
+            x.k1 = (float)s.rab[w].key;
+            x.i1 = s.rab[w].idx;
+            x.k2 = s.rf[w];
+            b.merge(x);
+        }
+        s.pub_k64 = (double)b.k1;   // published: best float key, its index, second float key
+        s.pub_idx = b.i1;
+        s.pub_max = b.k2;
+    }
+    cluster.sync();
+    if (tid < 32) {
+        Top2 x;
+        x.init();
+        if (lane < C) {
+            x.k1 = (float)*cluster.map_shared_rank(&s.pub_k64, lane);
+            x.i1 = *cluster.map_shared_rank(&s.pub_idx, lane);
+            x.k2 = *cluster.map_shared_rank(&s.pub_max, lane);
+        }
+        x = warp_top2(x);
+        if (lane == 0) {
+            s.bf[1] = x.k1;
+            s.bf[0] = x.k2;
+            s.bu[6] = (uint32_t)x.i1;
+        }
+    }
+    __syncthreads();
+    const float M1 = s.bf[1], M2 = s.bf[0];
+    token = (int32_t)s.bu[6];
+    if (!(M1 - M2 > tol)) {
+        // near-tie: every kept token within tol of the best is re-evaluated in double precision
         ArgBest mine;
         mine.key = -INFINITY;
         mine.idx = 0x7FFFFFFF;
         sl.for_each(s, [&](float z, int32_t i) {
-            const bool kept = (z > -INFINITY) && fkey(z) >= kc;
-            if (prow) prow[i] = kept ? (float)((double)qmass_d(dist(r, z)) / zk) : 0.f;
-            if (!kept) return;
+            if (!((z > -INFINITY) && fkey(z) >= kc)) return;
             const float u = race_u(rc, i);
-            const float k32 = race_key32(dist(r, z), u);
-            if (k32 >= best32 - tol) {
+            if (race_key32(dist(r, z), u) >= M1 - tol) {
                 const double k64 = race_key64(r, z, u);
                 if (better(k64, i, mine.key, mine.idx)) {
                     mine.key = k64;
                     mine.idx = i;
                 }
             }
-            best32 = fmaxf(best32, k32);
         });
         mine = block_argbest(mine, s);
+        cluster.sync();  // everyone has read the published float keys
         if (tid == 0) {
             s.pub_k64 = mine.key;
             s.pub_idx = mine.idx;
@@ -1106,25 +1322,13 @@ __global__ void __launch_bounds__(kThreads, 1) sample_rows_kernel(const Args a)
                 x.idx = *cluster.map_shared_rank(&s.pub_idx, lane);
             }
             x = warp_argbest(x);
-            if (lane == 0) s.bab = x;
+            if (lane == 0) s.bu[6] = (uint32_t)x.idx;
         }
         __syncthreads();
-        win = s.bab;
-        prow = nullptr;  // already written
-    }
-
-    // ---- D: optional probabilities over the slice
-    if (prow) {
-        const double zk = (double)ZK;
-        const uint32_t kc = key_cut;
-        sl.for_each(s, [&](float z, int32_t i) {
-            float pv = 0.f;
-            if (z > -INFINITY && fkey(z) >= kc) pv = (float)((double)qmass_d(dist(r, z)) / zk);
-            prow[i] = pv;
-        });
+        token = (int32_t)s.bu[6];
     }
     if (writer) {
-        a.out_token[row] = win.idx;
+        a.out_token[row] = token;
         if (a.out_status) a.out_status[row] = kRowOk;
         if (a.out_cutoff) a.out_cutoff[row] = key_to_float(key_cut);
         if (a.out_kept) a.out_kept[row] = (int32_t)NK;
