@@ -29,7 +29,9 @@ import torch  # noqa: E402
 METRIC = "rows/s & HBM GB/s (% of peak) at B=1024 V=128256 fp32; p50 us at B=1"
 UNIT = "rows/s"
 ROW_PARAM_BYTES = 4 + 4 + 4 + 4 + 8 + 4  # T, top_k, top_p, min_p, seed, token out
-KERNEL_SOURCES = ["nucleus_token_sampler_gb300/csrc/tps_kernel.cuh",
+KERNEL_SOURCES = ["nucleus_token_sampler_gb300/csrc/tps_stream.cuh",
+                  "nucleus_token_sampler_gb300/csrc/tps_cluster.cuh",
+                  "nucleus_token_sampler_gb300/csrc/tps_common.cuh",
                   "nucleus_token_sampler_gb300/csrc/tps_device.cuh",
                   "nucleus_token_sampler_gb300/csrc/tps_api.cu"]
 

@@ -98,12 +98,31 @@ int tps_sample_ex(const void* logits, int dtype, int64_t B, int64_t V, int64_t l
                   float* out_probs, int32_t* out_status, float* out_cutoff, int32_t* out_kept,
                   void* stream);
 
+/* Which kernel samples the rows (tps_sample_kernel). */
+typedef enum {
+    TPS_KERNEL_AUTO = 0,    /* the library's choice for the shape (what tps_sample uses)            */
+    TPS_KERNEL_CLUSTER = 1, /* one thread-block cluster per row, the row held in shared memory      */
+    TPS_KERNEL_STREAM = 2   /* one persistent CTA per SM, rows streamed through a ring of chunks     */
+} tps_kernel;
+
+/*
+ * tps_sample_kernel -- tps_sample_ex with an explicit kernel choice (same results for every
+ * choice; the choice only changes speed).  `kernel` is a tps_kernel; any other value is
+ * TPS_ERR_ARG.  TPS_KERNEL_CLUSTER returns TPS_ERR_UNSUPPORTED_V when 16 CTAs cannot hold a row.
+ */
+int tps_sample_kernel(const void* logits, int dtype, int64_t B, int64_t V, int64_t ld,
+                      const float* temperature, const int32_t* top_k, const float* top_p,
+                      const float* min_p, const uint64_t* seed, uint64_t step, int32_t* out_token,
+                      float* out_probs, int32_t* out_status, float* out_cutoff, int32_t* out_kept,
+                      int kernel, void* stream);
+
 /* Largest V the library accepts for `dtype` on the current device (0 for an unknown dtype or
- * when no device is usable).  Host-only query; enqueues nothing. */
+ * when no device is usable); the exact 64-bit mass sums bound it at 2^20 - 1.  Host-only query;
+ * enqueues nothing. */
 int64_t tps_max_vocab(int dtype);
 
-/* Cluster size (CTAs per row) tps_sample would use for this shape on the current device, or 0
- * when the shape is not supported.  Host-only query. */
+/* Cluster size (CTAs per row) the cluster kernel would use for this shape on the current device,
+ * or 0 when 16 CTAs cannot hold the row.  Host-only query. */
 int tps_cluster_size(int dtype, int64_t B, int64_t V);
 
 /* Static, human-readable text for a tps_status or (offset by 100) a tps_row_status. */

@@ -22,7 +22,7 @@ _CSRC = os.path.join(_HERE, "csrc")
 _LIB = os.path.join(_HERE, "libtps.so")
 _INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
 _SOURCES = ["tps_api.cu"]
-_HEADERS = ["tps_device.cuh", "tps_kernel.cuh"]
+_HEADERS = ["tps_device.cuh", "tps_common.cuh", "tps_cluster.cuh", "tps_stream.cuh"]
 
 TPS_F32, TPS_BF16 = 0, 1
 ROW_STATUS = {0: "ok", 1: "nan", 2: "all_masked", 3: "bad_param", 4: "timeout"}
@@ -71,6 +71,8 @@ def load():
             lib.tps_sample.argtypes = [P, I32, I64, I64, P, P, P, P, P, U64, P, P, P]
             lib.tps_sample_ex.restype = I32
             lib.tps_sample_ex.argtypes = [P, I32, I64, I64, I64, P, P, P, P, P, U64, P, P, P, P, P, P]
+            lib.tps_sample_kernel.restype = I32
+            lib.tps_sample_kernel.argtypes = [P, I32, I64, I64, I64, P, P, P, P, P, U64, P, P, P, P, P, I32, P]
             lib.tps_max_vocab.restype = I64
             lib.tps_max_vocab.argtypes = [I32]
             lib.tps_cluster_size.restype = I32
@@ -127,8 +129,11 @@ def _param(x, B, dtype, device):
     return x.contiguous()
 
 
+KERNELS = {"auto": 0, "cluster": 1, "stream": 2}
+
+
 def sample(logits: torch.Tensor, temperature, top_k, top_p, min_p, seed, step: int = 0, *,
-           want_probs: bool = False, diagnostics: bool = False, out=None, stream=None):
+           want_probs: bool = False, diagnostics: bool = False, out=None, stream=None, kernel: str = "auto"):
     """Sample one token per row of ``logits`` ([B, V] float32/bfloat16 CUDA tensor; the row stride
     may exceed V).
 
@@ -137,6 +142,7 @@ def sample(logits: torch.Tensor, temperature, top_k, top_p, min_p, seed, step: i
     64-bit counter shared by the batch.  Returns the [B] int32 token tensor, or a dict with
     ``token``, ``status``, ``cutoff``, ``kept`` (and ``probs``) when ``diagnostics`` or
     ``want_probs`` is set.  Work is enqueued on ``stream`` (default: the current stream).
+    ``kernel`` picks the sampler kernel ("auto", "cluster" or "stream"); results do not depend on it.
     """
     if not logits.is_cuda:
         raise ValueError("logits must be a CUDA tensor (the sampler has no CPU path)")
@@ -168,9 +174,9 @@ def sample(logits: torch.Tensor, temperature, top_k, top_p, min_p, seed, step: i
         kept = kept if kept is not None else torch.empty(B, dtype=torch.int32, device=dev)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     with torch.cuda.device(dev):
-        rc = load().tps_sample_ex(_ptr(logits), code, B, V, ld, _ptr(T), _ptr(K), _ptr(P), _ptr(M), _ptr(S),
-                                  int(step) & ((1 << 64) - 1), _ptr(tok), _ptr(probs), _ptr(st), _ptr(cut),
-                                  _ptr(kept), ctypes.c_void_p(s.cuda_stream))
+        rc = load().tps_sample_kernel(_ptr(logits), code, B, V, ld, _ptr(T), _ptr(K), _ptr(P), _ptr(M), _ptr(S),
+                                      int(step) & ((1 << 64) - 1), _ptr(tok), _ptr(probs), _ptr(st), _ptr(cut),
+                                      _ptr(kept), KERNELS[kernel], ctypes.c_void_p(s.cuda_stream))
     _check(rc)
     if not (diagnostics or want_probs):
         return tok

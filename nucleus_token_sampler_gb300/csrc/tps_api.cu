@@ -1,6 +1,11 @@
-// tps_api.cu -- the C ABI declared in include/tps.h: argument checks, launch-shape choice and the
-// cluster launch.  No allocation, no host synchronisation, no state kept between calls beyond a
-// per-device cache of queried limits.
+// tps_api.cu -- the C ABI declared in include/tps.h: argument checks, kernel and launch-shape
+// choice, and the launch.  No allocation, no host synchronisation, no state kept between calls
+// beyond a per-device cache of queried limits.
+//
+// Two kernels sample the rows.  The streaming kernel (one persistent CTA per SM, rows streamed
+// through a ring of bulk-copied chunks) is used when the batch can occupy the GPU with whole rows;
+// the cluster kernel (one thread-block cluster per row, the row held in the cluster's shared
+// memory) spreads each row over up to 16 SMs for small batches.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -8,7 +13,8 @@
 #include <mutex>
 
 #include "../../include/tps.h"
-#include "tps_kernel.cuh"
+#include "tps_cluster.cuh"
+#include "tps_stream.cuh"
 
 namespace {
 
@@ -19,11 +25,16 @@ constexpr int64_t kMaxVocabMass = (int64_t(1) << 20) - 1;  // fixed-point mass s
 constexpr uint32_t kSliceTarget = 64u * 1024u;              // preferred slice per CTA
 constexpr int kMaxCluster = 16;
 
+constexpr int kStreamStages = 6;
+constexpr uint32_t kStreamChunk = 32u * 1024u;
+constexpr int64_t kStreamMinRows = 32;  // batches at least this large use the streaming kernel
+
 struct DeviceInfo {
     bool ready = false;
     int sms = 0;
     int smem_optin = 0;
     bool attrs_f32 = false, attrs_bf16 = false;
+    bool sattrs_f32 = false, sattrs_bf16 = false;
     // Largest dynamic shared memory per CTA seen to co-schedule a cluster of 9..16 CTAs, per dtype
     // (0 = not known yet).
     std::atomic<long> wide_ok[2][kMaxCluster + 1];
@@ -121,6 +132,23 @@ bool wide_cluster_ok(DeviceInfo& d, int dt, int C, size_t smem)
     return true;
 }
 
+size_t stream_smem_bytes() { return (size_t)kStreamStages * kStreamChunk + sizeof(tps::Shared) + sizeof(tps::StreamState); }
+
+template <typename TIn>
+cudaError_t launch_stream(const DeviceInfo& d, bool* attrs_done, const tps::Args& a, cudaStream_t stream)
+{
+    auto k = tps::stream_rows_kernel<TIn>;
+    const size_t smem = stream_smem_bytes();
+    if (!*attrs_done) {
+        const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        *attrs_done = true;
+    }
+    const int64_t grid = a.B < (int64_t)d.sms ? a.B : (int64_t)d.sms;
+    k<<<(unsigned)grid, tps::kThreads, smem, stream>>>(a, kStreamStages, kStreamChunk);
+    return cudaGetLastError();
+}
+
 template <typename TIn>
 cudaError_t launch(const tps::Args& a, int C, size_t smem, cudaStream_t stream)
 {
@@ -175,17 +203,12 @@ const char* tps_status_string(int status)
 
 int64_t tps_max_vocab(int dtype)
 {
+    // The streaming kernel holds no row in shared memory; the limit is the exact 64-bit mass sum.
     const int es = elem_bytes(dtype);
     if (!es) return 0;
     DeviceInfo* d = nullptr;
     if (!device_info(&d)) return 0;
-    int64_t lo = 0, hi = kMaxVocabMass;
-    while (lo < hi) {  // largest V whose 16-CTA slice still fits
-        const int64_t mid = (lo + hi + 1) / 2;
-        if (smem_bytes(slice_cap_bytes(mid, es, kMaxCluster)) <= (size_t)d->smem_optin) lo = mid;
-        else hi = mid - 1;
-    }
-    return lo;
+    return kMaxVocabMass;
 }
 
 int tps_cluster_size(int dtype, int64_t B, int64_t V)
@@ -198,11 +221,12 @@ int tps_cluster_size(int dtype, int64_t B, int64_t V)
     return choose_cluster(*d, es, B, V);
 }
 
-int tps_sample_ex(const void* logits, int dtype, int64_t B, int64_t V, int64_t ld, const float* temperature,
-                  const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seed,
-                  uint64_t step, int32_t* out_token, float* out_probs, int32_t* out_status, float* out_cutoff,
-                  int32_t* out_kept, void* stream)
+int tps_sample_kernel(const void* logits, int dtype, int64_t B, int64_t V, int64_t ld, const float* temperature,
+                      const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seed,
+                      uint64_t step, int32_t* out_token, float* out_probs, int32_t* out_status, float* out_cutoff,
+                      int32_t* out_kept, int kernel, void* stream)
 {
+    if (kernel < TPS_KERNEL_AUTO || kernel > TPS_KERNEL_STREAM) return TPS_ERR_ARG;
     if (B < 0 || V < 1 || ld < V) return TPS_ERR_ARG;
     const int es = elem_bytes(dtype);
     if (!es) return TPS_ERR_DTYPE;
@@ -218,9 +242,11 @@ int tps_sample_ex(const void* logits, int dtype, int64_t B, int64_t V, int64_t l
 
     DeviceInfo* d = nullptr;
     if (!device_info(&d)) return fail_cuda(cudaGetLastError());
-    const int C = choose_cluster(*d, es, B, V);
+    const bool use_stream = kernel == TPS_KERNEL_STREAM || (kernel == TPS_KERNEL_AUTO && B >= kStreamMinRows) ||
+                            (kernel == TPS_KERNEL_AUTO && choose_cluster(*d, es, B, V) == 0);
+    const int C = use_stream ? 1 : choose_cluster(*d, es, B, V);
     if (C == 0) return TPS_ERR_UNSUPPORTED_V;
-    const uint32_t cap = slice_cap_bytes(V, es, C);
+    const uint32_t cap = use_stream ? 0u : slice_cap_bytes(V, es, C);
     const size_t smem = smem_bytes(cap);
 
     tps::Args a;
@@ -243,6 +269,12 @@ int tps_sample_ex(const void* logits, int dtype, int64_t B, int64_t V, int64_t l
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
+    if (use_stream) {
+        e = (dtype == TPS_F32) ? launch_stream<float>(*d, &d->sattrs_f32, a, st)
+                               : launch_stream<__nv_bfloat16>(*d, &d->sattrs_bf16, a, st);
+        if (e != cudaSuccess) return fail_cuda(e);
+        return TPS_OK;
+    }
     int Cl = C;
     size_t sm = smem;
     // A cluster wider than 8 that the GPU cannot co-schedule falls back to 8 CTAs, if they hold the row.
@@ -273,6 +305,15 @@ int tps_sample_ex(const void* logits, int dtype, int64_t B, int64_t V, int64_t l
     }
     if (e != cudaSuccess) return fail_cuda(e);
     return TPS_OK;
+}
+
+int tps_sample_ex(const void* logits, int dtype, int64_t B, int64_t V, int64_t ld, const float* temperature,
+                  const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seed, uint64_t step,
+                  int32_t* out_token, float* out_probs, int32_t* out_status, float* out_cutoff, int32_t* out_kept,
+                  void* stream)
+{
+    return tps_sample_kernel(logits, dtype, B, V, ld, temperature, top_k, top_p, min_p, seed, step, out_token,
+                             out_probs, out_status, out_cutoff, out_kept, TPS_KERNEL_AUTO, stream);
 }
 
 int tps_sample(const void* logits, int dtype, int64_t B, int64_t V, const float* temperature, const int32_t* top_k,

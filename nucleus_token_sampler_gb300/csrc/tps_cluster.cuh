@@ -1,0 +1,275 @@
+// tps_cluster.cuh -- the cluster sampler: one thread-block cluster per row, the row held in the
+// cluster's shared memory.  Used when the batch is too small to fill the GPU with whole rows.
+//
+// Each of the C CTAs bulk-copies one contiguous 16-byte-aligned slice of the row from HBM into its
+// own shared memory (one read of the row, no multicast); the ragged head and tail of an unaligned
+// row are fetched with plain loads.  Each CTA takes its local maximum and lists the tokens that
+// min-p, measured against that local maximum, does not already reject -- a superset of the row's
+// survivors, because the global maximum is at least the local one.  One exchange through
+// distributed shared memory gives the global maximum and the lists; every CTA then filters the
+// lists exactly and resolves the row (top-k, top-p, race).  Rows whose lists overflow, or rows
+// without min-p, take the general path over the slices.
+#pragma once
+
+#include "tps_common.cuh"
+
+namespace tps {
+
+// ---------------------------------------------------------------------------------------------
+// The kernel.  Grid: B * C CTAs in clusters of C along x; cluster q samples row q.
+// ---------------------------------------------------------------------------------------------
+template <typename TIn>
+__global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
+{
+    using E = Elem<TIn>;
+    constexpr int EPV = E::kPerVec;
+    constexpr int ES = E::kBytes;
+    extern __shared__ __align__(128) unsigned char dsmem[];
+
+    ClusterTopo topo;
+    cg::cluster_group& cluster = topo.g;
+    const uint32_t C = topo.C;
+    const uint32_t rank = topo.rank;
+    const int64_t row = (int64_t)(blockIdx.x / C);
+    Shared& s = *reinterpret_cast<Shared*>(dsmem + a.slice_cap);
+    const int tid = threadIdx.x;
+    const uint32_t lane = tid & 31;
+
+    // ---- geometry: the aligned interior of the row in 16-byte vectors, split evenly over the CTAs
+    const unsigned char* rowp = static_cast<const unsigned char*>(a.logits) + row * a.ld * ES;
+    const uintptr_t g0 = reinterpret_cast<uintptr_t>(rowp), g1 = g0 + (uintptr_t)a.V * ES;
+    uintptr_t a0 = (g0 + 15) & ~(uintptr_t)15, a1 = g1 & ~(uintptr_t)15;
+    int64_t nhead, ntail;
+    if (a1 <= a0) {
+        a0 = a1 = g1;
+        nhead = a.V;
+        ntail = 0;
+    } else {
+        nhead = (int64_t)(a0 - g0) / ES;
+        ntail = (int64_t)(g1 - a1) / ES;
+    }
+    const int64_t n16 = (int64_t)(a1 - a0) / 16;
+    const int64_t v_lo = n16 * rank / C, v_hi = n16 * (rank + 1) / C;
+    const int nvec = (int)(v_hi - v_lo);
+    const uint32_t bytes = (uint32_t)nvec * 16u;
+    Slice<TIn> sl;
+    sl.vec = reinterpret_cast<const uint4*>(dsmem);
+    sl.nvec = nvec;
+    sl.elem0 = nhead + v_lo * EPV;
+
+    // ---- stage the slice: one bulk copy (in 32 KB pieces) completing on an mbarrier
+    const int my_head = (rank == 0) ? (int)nhead : 0;
+    const int my_tail = (rank == C - 1) ? (int)ntail : 0;
+    if (tid == 0) {
+        s.nx = my_head + my_tail;
+        if (bytes > 0) {
+            mbar_init(&s.mbar, 1);
+            mbar_arrive_expect_tx(&s.mbar, bytes);
+            const unsigned char* src = reinterpret_cast<const unsigned char*>(a0) + v_lo * 16;
+            for (uint32_t off = 0; off < bytes; off += 32768u)
+                bulk_g2s(dsmem + off, src + off, min(32768u, bytes - off), &s.mbar);
+        }
+    }
+    if (tid < my_head) {
+        s.xz[tid] = E::load1(rowp, tid);
+        s.xi[tid] = tid;
+    } else if (tid < my_head + my_tail) {
+        const int64_t i = a.V - ntail + (tid - my_head);
+        s.xz[tid] = E::load1(rowp, i);
+        s.xi[tid] = (int32_t)i;
+    }
+    // per-row parameters (read while the copy is in flight)
+    const float T = a.temperature[row];
+    const float P = a.top_p[row];
+    const float MP = a.min_p[row];
+    const int32_t K = a.top_k[row];
+    const uint64_t seed = a.seed[row];
+    const bool params_ok = isfinite(T) && isfinite(P) && isfinite(MP);
+    const bool sampling = params_ok && T > 0.f;
+    const float minp = (MP > 0.f) ? fminf(MP, 1.f) : 0.f;
+    __syncthreads();  // mbarrier initialised, extras stored
+    uint32_t timed_out = 0;
+    if (bytes > 0 && !mbar_wait_bounded(&s.mbar, 0, kWaitLimitNs)) timed_out = 1;
+    timed_out = __syncthreads_or(timed_out) ? 1u : 0u;
+
+    // ---- A: local maximum with NaN propagation (a NaN anywhere makes the maximum NaN)
+    float vmax = -INFINITY;
+    if (!timed_out) sl.for_each(s, [&](float z, int32_t) { vmax = fmax_nan(vmax, z); });
+    vmax = warp_max_nan(vmax);
+    if (lane == 0) s.rf[tid >> 5] = vmax;
+    __syncthreads();
+    float mloc = s.rf[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) mloc = fmax_nan(mloc, s.rf[w]);
+
+    // ---- B (local): list every token above a threshold that min-p relative to the LOCAL maximum
+    //      already rejects; the global maximum is >= the local one, so the lists cover every
+    //      survivor of the row.  Without min-p nothing can be excluded and no list is built.
+    const bool local_ok = sampling && !timed_out && minp > 0.f && mloc > -INFINITY && mloc < INFINITY;
+    uint32_t nlisted = 0xFFFFFFFFu;  // "no complete list"
+    if (sampling && !timed_out && minp > 0.f && mloc == -INFINITY) nlisted = 0;  // nothing finite here
+    if (local_ok) {
+        const RowCtx rl = make_ctx(mloc, T, minp);
+        const float zc_loc = minp_threshold(rl);
+        if (tid == 0) s.ncand = 0;
+        __syncthreads();
+        if (zc_loc > -INFINITY) {
+            sl.for_each(s, [&](float z, int32_t i) {
+                if (!(z > zc_loc)) return;
+                const uint32_t slot = atomicAdd(&s.ncand, 1u);
+                if (slot < (uint32_t)kCand) {
+                    s.ckey[slot] = fkey(z);
+                    s.cidx[slot] = (uint32_t)i;
+                }
+            });
+            __syncthreads();
+            nlisted = s.ncand;
+        }
+    }
+    if (tid == 0) {
+        s.pub_max = mloc;
+        s.pub_timeout = timed_out;
+        s.pub_nsurv = nlisted;  // 0xFFFFFFFF or > kCand: this CTA's list is not complete
+        s.pub_gcnt = min(nlisted, (uint32_t)kCand);
+    }
+    cluster.sync();
+    if (tid < 32) {
+        float m = -INFINITY;
+        uint32_t to = 0, nl = 0, cnt = 0, bad = 0;
+        if (lane < C) {
+            m = *cluster.map_shared_rank(&s.pub_max, lane);
+            to = *cluster.map_shared_rank(&s.pub_timeout, lane);
+            nl = *cluster.map_shared_rank(&s.pub_nsurv, lane);
+            bad = nl > (uint32_t)kCand;
+            cnt = bad ? 0u : nl;
+        }
+        uint32_t inc = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if ((int)lane >= o) inc += y;
+        }
+        if (lane < C) {
+            s.goff[lane] = inc - cnt;
+            s.gcnt[lane] = cnt;
+        }
+        m = warp_max_nan(m);
+        to = warp_max_u32(to);
+        bad = warp_max_u32(bad);
+        if (lane == 31) s.gtotal = inc;
+        if (lane == 0) {
+            s.bf[0] = m;
+            s.bu[0] = to;
+            s.bu[1] = bad;
+        }
+    }
+    __syncthreads();
+    const float zmax = s.bf[0];
+    const uint32_t cl_timeout = s.bu[0];
+    const bool lists_complete = (s.bu[1] == 0) && (s.gtotal <= (uint32_t)kCand);
+
+    int32_t status = kRowOk;
+    if (cl_timeout) status = kRowTimeout;
+    else if (isnan(zmax) || zmax == INFINITY) status = kRowNan;
+    else if (!params_ok) status = kRowBadParam;
+    else if (zmax == -INFINITY) status = kRowAllMasked;
+
+    float* prow = a.out_probs ? a.out_probs + row * a.V : nullptr;
+    const bool writer = (rank == 0) && (tid == 0);
+
+    if (status != kRowOk) {
+        if (prow) {
+            for (int64_t i = sl.elem0 + tid; i < sl.elem0 + (int64_t)nvec * EPV; i += kThreads) prow[i] = 0.f;
+            for (int x = tid; x < s.nx; x += kThreads) prow[s.xi[x]] = 0.f;
+        }
+        if (writer) {
+            a.out_token[row] = -1;
+            if (a.out_status) a.out_status[row] = status;
+            if (a.out_cutoff) a.out_cutoff[row] = __uint_as_float(0x7FC00000u);
+            if (a.out_kept) a.out_kept[row] = 0;
+        }
+        // A copy still in flight after a timeout must land before the shared memory is released.
+        if (timed_out && bytes > 0) (void)mbar_wait_bounded(&s.mbar, 0, kWaitLimitNs);
+        cluster.sync();
+        return;
+    }
+
+    // ---- greedy branch: lowest index of the maximum ("Implement batched top-p sampling with
+    //      temperature", 'A strong answer': temperature 0 means greedy, ties to the lowest index)
+    if (T <= 0.f) {
+        uint32_t mi = 0xFFFFFFFFu;
+        sl.for_each(s, [&](float z, int32_t i) {
+            if (z == zmax) mi = min(mi, (uint32_t)i);
+        });
+        mi = block_min_u32(mi, s);
+        if (tid == 0) s.pub_minidx = mi;
+        cluster.sync();
+        if (tid < 32) {
+            uint32_t m = (lane < C) ? *cluster.map_shared_rank(&s.pub_minidx, lane) : 0xFFFFFFFFu;
+            m = warp_min_u32(m);
+            if (lane == 0) s.bu[2] = m;
+        }
+        __syncthreads();
+        const uint32_t arg = s.bu[2];
+        if (prow) sl.for_each(s, [&](float, int32_t i) { prow[i] = ((uint32_t)i == arg) ? 1.f : 0.f; });
+        if (writer) {
+            a.out_token[row] = (int32_t)arg;
+            if (a.out_status) a.out_status[row] = kRowOk;
+            if (a.out_cutoff) a.out_cutoff[row] = zmax;
+            if (a.out_kept) a.out_kept[row] = 1;
+        }
+        cluster.sync();
+        return;
+    }
+
+    const RowCtx r = make_ctx(zmax, T, minp);
+    const float zc = minp_threshold(r);
+    const bool topk_on = (K > 0) && ((int64_t)K < a.V);
+
+    RaceCtx rc;
+    rc.k0 = (uint32_t)seed;
+    rc.k1 = (uint32_t)(seed >> 32);
+    rc.row = (uint32_t)row;
+    rc.s_lo = (uint32_t)a.step;
+    rc.s_hi = (uint32_t)(a.step >> 32);
+
+
+    if (lists_complete) {
+        // ================= fast path: every survivor is on some CTA's list =================
+        // Gather the lists (one entry per thread), keep the survivors of min-p against the global
+        // maximum.  This is the last read of another CTA's shared memory.
+        if (tid == 0) s.ncand = 0;
+        __syncthreads();
+        const uint32_t total = s.gtotal;
+        if ((uint32_t)tid < total) {
+            uint32_t rr = 0;
+            while (rr + 1 < C && s.goff[rr + 1] <= (uint32_t)tid) ++rr;
+            const uint32_t off = (uint32_t)tid - s.goff[rr];
+            const uint32_t key = *cluster.map_shared_rank(&s.ckey[off], rr);
+            const uint32_t idx = *cluster.map_shared_rank(&s.cidx[off], rr);
+            const float z = key_to_float(key);
+            if (z > zc && minp_ok(r, z, dist(r, z))) {
+                const uint32_t slot = atomicAdd(&s.ncand, 1u);
+                s.u.cd.sbuf[slot] = sb_make(key, idx);
+            }
+        }
+        cluster_arrive();  // no more remote reads by this CTA; waited for just before exit
+        __syncthreads();
+        const uint32_t n = s.ncand;
+        const RowResult res = resolve_candidates(s, r, rc, n, topk_on, K, P);
+        const uint32_t key_cut = res.key_cut;
+        const uint64_t NK = res.nk, ZK = res.zk;
+        const int32_t token = res.token;
+        if (prow) write_probs(sl, s, r, key_cut, ZK, prow);
+        if (writer) write_row(a, row, token, kRowOk, key_to_float(key_cut), (int32_t)NK);
+        cluster_wait();  // every CTA has finished reading this CTA's lists
+        return;
+    }
+
+    // ================= general path: survivors against the global maximum =================
+    const RowResult res = general_path(topo, s, sl, r, zc, topk_on, K, P, rc, prow);
+    if (writer) write_row(a, row, res.token, kRowOk, key_to_float(res.key_cut), (int32_t)res.nk);
+    topo.sync();  // keep this CTA's shared memory alive until every remote read is done
+}
+
+}  // namespace tps

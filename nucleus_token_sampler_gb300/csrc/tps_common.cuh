@@ -1,22 +1,7 @@
-// tps_kernel.cuh -- the row sampler: one thread-block cluster per row, the row held in the
-// cluster's shared memory.
-//
-// Each of the C CTAs of a cluster bulk-copies one contiguous 16-byte-aligned slice of the row from
-// HBM into its own shared memory (one read of the row, no multicast); the ragged head and tail of
-// an unaligned row are fetched with plain loads.  Everything after that reads shared memory, and
-// the CTAs exchange small values through distributed shared memory (one lane per CTA):
-//
-//   A  zmax (NaN-propagating max) -> row status; T <= 0 -> greedy.
-//   B  one compare per token against a threshold below which min-p surely drops the token; the
-//      few tokens above it are checked exactly, counted and appended to a candidate list.
-//   C  few survivors (<= 256): every CTA gathers the candidates, sorts them by (logit desc, index
-//      asc) and walks the classes of equal logits -- top-k cut by count, top-p cut by mass -- then
-//      runs the exponential race over the kept prefix (one warp when there are <= 32).
-//      many survivors: a 256-bin histogram over d = (zmax - z)/T of {count, exact fixed-point
-//      mass} locates the bin holding each cut; the cut's class is then resolved exactly by
-//      gathering that bin's tokens, or by sub-histograms over the logit's order-preserving key
-//      until few enough remain or a single value is left.  The race runs over the slice.
-//   D  optional output row of renormalised probabilities.
+// tps_common.cuh -- pieces shared by the two row samplers (the cluster kernel and the streaming
+// kernel): shared-memory state, block reductions, the sources a pass reads (a slice in shared
+// memory or a whole row in global memory), the cluster/single-CTA "topology" the exchanges use,
+// histogram-located cuts with exact refinement, candidate resolution and the exponential race.
 //
 // The chain is the one on "What do temperature, top-k and top-p each do to the next-token
 // distribution, and in what order does a serving engine apply them?" ('A strong answer'), with
@@ -188,17 +173,52 @@ __device__ __forceinline__ uint64_t block_exscan_u64(uint64_t v, Shared& s, uint
 }
 
 // ---------------------------------------------------------------------------------------------
-// The slice of the row this CTA holds.
+// Topologies: the CTAs that share one row.  ClusterTopo is a thread-block cluster exchanging
+// through distributed shared memory; SoloTopo is a single CTA (map() is the identity).
 // ---------------------------------------------------------------------------------------------
-template <typename TIn>
-struct Slice {
-    const uint4* vec;  // shared-memory vectors of Elem<TIn>::kPerVec elements
+struct ClusterTopo {
+    cg::cluster_group g;
+    uint32_t C, rank;
+    __device__ __forceinline__ ClusterTopo() : g(cg::this_cluster())
+    {
+        C = g.num_blocks();
+        rank = g.block_rank();
+    }
+    __device__ __forceinline__ void sync() { g.sync(); }
+    template <typename T>
+    __device__ __forceinline__ T* map(T* p, uint32_t r)
+    {
+        return g.map_shared_rank(p, r);
+    }
+};
+
+struct SoloTopo {
+    uint32_t C = 1, rank = 0;
+    __device__ __forceinline__ void sync() { __syncthreads(); }
+    template <typename T>
+    __device__ __forceinline__ T* map(T* p, uint32_t)
+    {
+        return p;
+    }
+};
+
+// ---------------------------------------------------------------------------------------------
+// Sources: what one pass reads.  Both apply f(z, i) to every element they cover -- 16-byte vectors
+// (four loaded before any is processed, so the latency overlaps even when f holds atomics), then
+// the ragged head/tail elements kept in s.xz/s.xi.
+// ---------------------------------------------------------------------------------------------
+template <typename TIn, bool kGlobal>
+struct VecSource {
+    const uint4* vec;  // kGlobal: the row's aligned interior in global memory; else a shared slice
     int nvec;
     int64_t elem0;     // row index of the first element of vec[0]
 
-    // Apply f(z, i) to every element of the slice (vectors, then the ragged extras).  Four vectors
-    // are loaded before any of them is processed, so the shared-memory latency overlaps even when f
-    // holds atomics.
+    __device__ __forceinline__ uint4 load(int v) const
+    {
+        if constexpr (kGlobal) return __ldg(vec + v);
+        else return vec[v];
+    }
+
     template <typename F>
     __device__ __forceinline__ void for_each(const Shared& s, F&& f) const
     {
@@ -208,7 +228,7 @@ struct Slice {
         for (; v + (U - 1) * kThreads < nvec; v += U * kThreads) {
             uint4 w[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) w[u] = vec[v + u * kThreads];
+            for (int u = 0; u < U; ++u) w[u] = load(v + u * kThreads);
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 float z[E::kPerVec];
@@ -220,7 +240,7 @@ struct Slice {
         }
         for (; v < nvec; v += kThreads) {
             float z[E::kPerVec];
-            E::unpack(vec[v], z);
+            E::unpack(load(v), z);
             const int32_t i0 = (int32_t)elem0 + v * E::kPerVec;
 #pragma unroll
             for (int j = 0; j < E::kPerVec; ++j) f(z[j], i0 + j);
@@ -228,6 +248,10 @@ struct Slice {
         for (int x = threadIdx.x; x < s.nx; x += kThreads) f(s.xz[x], s.xi[x]);
     }
 };
+template <typename TIn>
+using Slice = VecSource<TIn, false>;
+template <typename TIn>
+using GlobalRow = VecSource<TIn, true>;
 
 __device__ __forceinline__ int bin_of(float d)
 {
@@ -237,12 +261,17 @@ __device__ __forceinline__ int bin_of(float d)
 // Cluster-wide sum of the local histogram hcnt/hmass[0, nb) into hcnt/hmass of every CTA.
 // Step 1: CTA c sums its share of the bins over all CTAs (one remote read per thread) into
 // u.sh; step 2: every CTA copies all shares back into its own hcnt/hmass.
-__device__ __forceinline__ void cluster_reduce_hist(cg::cluster_group& cluster, Shared& s, int nb,
-                                                    uint32_t C, uint32_t rank)
+template <typename Topo>
+__device__ __forceinline__ void cluster_reduce_hist(Topo& topo, Shared& s, int nb)
 {
+    const uint32_t C = topo.C, rank = topo.rank;
+    if (C == 1) {  // a single CTA already holds the full histogram
+        __syncthreads();
+        return;
+    }
     const int per = (nb + (int)C - 1) / (int)C;
     const int b0 = min(nb, (int)rank * per), b1 = min(nb, b0 + per);
-    cluster.sync();  // every local histogram complete; nobody reads my previous share any more
+    topo.sync();  // every local histogram complete; nobody reads my previous share any more
     for (int b = b0 + (int)threadIdx.x; b < b1; b += kThreads) {
         s.u.sh.rcnt[b] = 0;
         s.u.sh.rmass[b] = 0;
@@ -252,18 +281,18 @@ __device__ __forceinline__ void cluster_reduce_hist(cg::cluster_group& cluster, 
     for (int p = threadIdx.x; p < npairs; p += kThreads) {
         const int b = b0 + p / (int)C;
         const uint32_t r = (uint32_t)(p % (int)C);
-        const uint32_t c = *cluster.map_shared_rank(&s.hcnt[b], r);
+        const uint32_t c = *topo.map(&s.hcnt[b], r);
         if (c) {
             atomicAdd(&s.u.sh.rcnt[b], c);
             atomicAdd((unsigned long long*)&s.u.sh.rmass[b],
-                      (unsigned long long)*cluster.map_shared_rank(&s.hmass[b], r));
+                      (unsigned long long)*topo.map(&s.hmass[b], r));
         }
     }
-    cluster.sync();  // all shares complete; nobody reads another CTA's hcnt/hmass any more
+    topo.sync();  // all shares complete; nobody reads another CTA's hcnt/hmass any more
     for (int b = threadIdx.x; b < nb; b += kThreads) {
         const uint32_t owner = (uint32_t)(b / per);
-        s.hcnt[b] = *cluster.map_shared_rank(&s.u.sh.rcnt[b], owner);
-        s.hmass[b] = *cluster.map_shared_rank(&s.u.sh.rmass[b], owner);
+        s.hcnt[b] = *topo.map(&s.u.sh.rcnt[b], owner);
+        s.hmass[b] = *topo.map(&s.u.sh.rmass[b], owner);
     }
     __syncthreads();
 }
@@ -375,11 +404,13 @@ __device__ __forceinline__ Sel walk_classes(Shared& s, int n, const Crit& cr, ui
 }
 
 // Copy every CTA's candidate list (counts in pub_gcnt) into u.cd.sbuf and sort it.  Returns n.
-__device__ __forceinline__ int gather_and_sort(cg::cluster_group& cluster, Shared& s, uint32_t C)
+template <typename Topo>
+__device__ __forceinline__ int gather_and_sort(Topo& topo, Shared& s)
 {
+    const uint32_t C = topo.C;
     if (threadIdx.x < 32) {  // lane r reads rank r's count; exclusive prefix over the ranks
         const uint32_t lane = threadIdx.x;
-        const uint32_t cnt = (lane < C) ? *cluster.map_shared_rank(&s.pub_gcnt, lane) : 0u;
+        const uint32_t cnt = (lane < C) ? *topo.map(&s.pub_gcnt, lane) : 0u;
         uint32_t inc = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -397,8 +428,8 @@ __device__ __forceinline__ int gather_and_sort(cg::cluster_group& cluster, Share
     for (uint32_t rr = 0; rr < C; ++rr) {  // each count <= kCand == kThreads
         const uint32_t off = s.goff[rr], cnt = s.gcnt[rr];
         if (threadIdx.x < cnt) {
-            const uint32_t k = *cluster.map_shared_rank(&s.ckey[threadIdx.x], rr);
-            const uint32_t i = *cluster.map_shared_rank(&s.cidx[threadIdx.x], rr);
+            const uint32_t k = *topo.map(&s.ckey[threadIdx.x], rr);
+            const uint32_t i = *topo.map(&s.cidx[threadIdx.x], rr);
             s.u.cd.sbuf[off + threadIdx.x] = sb_make(k, i);
         }
     }
@@ -435,16 +466,16 @@ __device__ __forceinline__ float race_tol(float dcut) { return 1e-5f + 1e-6f * d
 // Refine the cut inside level-1 bin `bin` (tokens with key >= key_lo that survive min-p), given
 // the (count, mass) of the survivors above the bin.  Exact: ends with a sorted candidate list or
 // with a single logit value.
-template <typename TIn>
-__device__ Sel refine_bin(cg::cluster_group& cluster, Shared& s, const Slice<TIn>& sl, const RowCtx& r,
-                          float zc, uint32_t C, int bin, uint32_t key_lo, const Crit& cr, uint64_t C0,
-                          uint64_t A0)
+template <typename Topo, typename Src>
+__device__ Sel refine_bin(Topo& topo, Shared& s, const Src& sl, const RowCtx& r, float zc, int bin, uint32_t key_lo,
+                          const Crit& cr, uint64_t C0, uint64_t A0)
 {
+    const uint32_t C = topo.C;
     uint32_t klo = 0, khi = 0xFFFFFFFFu;
     bool by_bin = true;
     for (int iter = 0; iter < 8; ++iter) {
         // Gather the tokens of the current range (a level-1 bin, or a key interval).
-        cluster.sync();  // nobody still reads my candidate list, published counts or shares
+        topo.sync();  // nobody still reads my candidate list, published counts or shares
         if (threadIdx.x == 0) s.ncand = 0;
         __syncthreads();
         uint32_t lcnt = 0, lmin = 0xFFFFFFFFu, lmax = 0;
@@ -476,14 +507,14 @@ __device__ Sel refine_bin(cg::cluster_group& cluster, Shared& s, const Slice<TIn
             s.pub_gkmin = kmn;
             s.pub_gkmax = kmx;
         }
-        cluster.sync();
+        topo.sync();
         if (threadIdx.x < 32) {
             const uint32_t lane = threadIdx.x;
             uint32_t tc = 0, gmn = 0xFFFFFFFFu, gmx = 0;
             if (lane < C) {
-                tc = *cluster.map_shared_rank(&s.pub_nsurv, lane);
-                gmn = *cluster.map_shared_rank(&s.pub_gkmin, lane);
-                gmx = *cluster.map_shared_rank(&s.pub_gkmax, lane);
+                tc = *topo.map(&s.pub_nsurv, lane);
+                gmn = *topo.map(&s.pub_gkmin, lane);
+                gmx = *topo.map(&s.pub_gkmax, lane);
             }
             tc = warp_sum_u32(tc);
             gmn = warp_min_u32(gmn);
@@ -513,7 +544,7 @@ __device__ Sel refine_bin(cg::cluster_group& cluster, Shared& s, const Slice<TIn
             return o;
         }
         if (total <= (uint64_t)kCand) {
-            const int n = gather_and_sort(cluster, s, C);
+            const int n = gather_and_sort(topo, s);
             prefix_masses(s, r, n);
             return walk_classes(s, n, cr, C0, A0);
         }
@@ -540,7 +571,7 @@ __device__ Sel refine_bin(cg::cluster_group& cluster, Shared& s, const Slice<TIn
             atomicAdd(&s.hcnt[sb], 1u);
             atomicAdd((unsigned long long*)&s.hmass[sb], (unsigned long long)qmass_d(d));
         });
-        cluster_reduce_hist(cluster, s, kSubBins, C, cluster.block_rank());
+        cluster_reduce_hist(topo, s, kSubBins);
         int jb;
         uint64_t c_at, a_at;
         scan_bins(s, nsub, cr, C0, A0, &jb, &c_at, &a_at);
@@ -716,380 +747,172 @@ __device__ __forceinline__ Top2 warp_top2(Top2 t)
 }
 
 // ---------------------------------------------------------------------------------------------
-// The kernel.  Grid: B * C CTAs in clusters of C along x; cluster q samples row q.
+// Row-level building blocks used by both kernels.  All threads of the CTA call them.
 // ---------------------------------------------------------------------------------------------
-template <typename TIn>
-__global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
-{
-    using E = Elem<TIn>;
-    constexpr int EPV = E::kPerVec;
-    constexpr int ES = E::kBytes;
-    extern __shared__ __align__(128) unsigned char dsmem[];
+struct RowResult {
+    uint32_t key_cut;  // key of the smallest kept logit
+    uint64_t nk;       // kept tokens
+    uint64_t zk;       // their fixed-point mass
+    int32_t token;
+};
 
-    cg::cluster_group cluster = cg::this_cluster();
-    const uint32_t C = cluster.num_blocks();
-    const uint32_t rank = cluster.block_rank();
-    const int64_t row = (int64_t)(blockIdx.x / C);
-    Shared& s = *reinterpret_cast<Shared*>(dsmem + a.slice_cap);
+// Row constants for a maximum zm (the global maximum, or a lower bound of it).
+__device__ __forceinline__ RowCtx make_ctx(float zm, float T, float minp)
+{
+    RowCtx r;
+    r.zmax = zm;
+    r.T = T;
+    r.invT = 1.f / T;
+    if (!(r.invT <= FLT_MAX)) r.invT = FLT_MAX;
+    r.minp = minp;
+    r.L_lo = r.L_hi = 0.f;
+    if (minp > 0.f) {
+        const float L = -logf(minp);
+        const float eps = 4e-6f * (1.f + L) + 1e-6f;
+        r.L_lo = L - eps;
+        r.L_hi = L + eps;
+    }
+    return r;
+}
+
+// zc: every token with z <= zc surely fails min-p (d(zc) > L_hi and d is monotone in z).  -inf when
+// min-p is off or no such value was found.
+__device__ __forceinline__ float minp_threshold(const RowCtx& r)
+{
+    if (!(r.minp > 0.f)) return -INFINITY;
+    float c = r.zmax - r.L_hi * r.T;
+    float step = fmaxf(fabsf(c) * 1e-6f, 1e-30f);
+    int it = 0;
+    while (!(dist(r, c) > r.L_hi) && it < 64) {
+        c -= step;
+        step *= 2.f;
+        ++it;
+    }
+    return (dist(r, c) > r.L_hi) ? c : -INFINITY;
+}
+
+// Resolve a row whose min-p survivors are u.cd.sbuf[0, n) (n <= kCand, any order): top-k, top-p,
+// race.  n <= 32 runs in warp 0 alone; larger n sorts with the whole CTA.
+__device__ __forceinline__ RowResult resolve_candidates(Shared& s, const RowCtx& r, const RaceCtx& rc, uint32_t n,
+                                                        bool topk_on, int32_t K, float P)
+{
     const int tid = threadIdx.x;
     const uint32_t lane = tid & 31;
-
-    // ---- geometry: the aligned interior of the row in 16-byte vectors, split evenly over the CTAs
-    const unsigned char* rowp = static_cast<const unsigned char*>(a.logits) + row * a.ld * ES;
-    const uintptr_t g0 = reinterpret_cast<uintptr_t>(rowp), g1 = g0 + (uintptr_t)a.V * ES;
-    uintptr_t a0 = (g0 + 15) & ~(uintptr_t)15, a1 = g1 & ~(uintptr_t)15;
-    int64_t nhead, ntail;
-    if (a1 <= a0) {
-        a0 = a1 = g1;
-        nhead = a.V;
-        ntail = 0;
-    } else {
-        nhead = (int64_t)(a0 - g0) / ES;
-        ntail = (int64_t)(g1 - a1) / ES;
-    }
-    const int64_t n16 = (int64_t)(a1 - a0) / 16;
-    const int64_t v_lo = n16 * rank / C, v_hi = n16 * (rank + 1) / C;
-    const int nvec = (int)(v_hi - v_lo);
-    const uint32_t bytes = (uint32_t)nvec * 16u;
-    Slice<TIn> sl;
-    sl.vec = reinterpret_cast<const uint4*>(dsmem);
-    sl.nvec = nvec;
-    sl.elem0 = nhead + v_lo * EPV;
-
-    // ---- stage the slice: one bulk copy (in 32 KB pieces) completing on an mbarrier
-    const int my_head = (rank == 0) ? (int)nhead : 0;
-    const int my_tail = (rank == C - 1) ? (int)ntail : 0;
-    if (tid == 0) {
-        s.nx = my_head + my_tail;
-        if (bytes > 0) {
-            mbar_init(&s.mbar, 1);
-            mbar_arrive_expect_tx(&s.mbar, bytes);
-            const unsigned char* src = reinterpret_cast<const unsigned char*>(a0) + v_lo * 16;
-            for (uint32_t off = 0; off < bytes; off += 32768u)
-                bulk_g2s(dsmem + off, src + off, min(32768u, bytes - off), &s.mbar);
-        }
-    }
-    if (tid < my_head) {
-        s.xz[tid] = E::load1(rowp, tid);
-        s.xi[tid] = tid;
-    } else if (tid < my_head + my_tail) {
-        const int64_t i = a.V - ntail + (tid - my_head);
-        s.xz[tid] = E::load1(rowp, i);
-        s.xi[tid] = (int32_t)i;
-    }
-    // per-row parameters (read while the copy is in flight)
-    const float T = a.temperature[row];
-    const float P = a.top_p[row];
-    const float MP = a.min_p[row];
-    const int32_t K = a.top_k[row];
-    const uint64_t seed = a.seed[row];
-    const bool params_ok = isfinite(T) && isfinite(P) && isfinite(MP);
-    const bool sampling = params_ok && T > 0.f;
-    const float minp = (MP > 0.f) ? fminf(MP, 1.f) : 0.f;
-    __syncthreads();  // mbarrier initialised, extras stored
-    uint32_t timed_out = 0;
-    if (bytes > 0 && !mbar_wait_bounded(&s.mbar, 0, kWaitLimitNs)) timed_out = 1;
-    timed_out = __syncthreads_or(timed_out) ? 1u : 0u;
-
-    // ---- A: local maximum with NaN propagation (a NaN anywhere makes the maximum NaN)
-    float vmax = -INFINITY;
-    if (!timed_out) sl.for_each(s, [&](float z, int32_t) { vmax = fmax_nan(vmax, z); });
-    vmax = warp_max_nan(vmax);
-    if (lane == 0) s.rf[tid >> 5] = vmax;
-    __syncthreads();
-    float mloc = s.rf[0];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) mloc = fmax_nan(mloc, s.rf[w]);
-
-    // ---- B (local): list every token above a threshold that min-p relative to the LOCAL maximum
-    //      already rejects; the global maximum is >= the local one, so the lists cover every
-    //      survivor of the row.  Without min-p nothing can be excluded and no list is built.
-    auto make_ctx = [&](float zm) {
-        RowCtx r;
-        r.zmax = zm;
-        r.T = T;
-        r.invT = 1.f / T;
-        if (!(r.invT <= FLT_MAX)) r.invT = FLT_MAX;
-        r.minp = minp;
-        r.L_lo = r.L_hi = 0.f;
-        if (minp > 0.f) {
-            const float L = -logf(minp);
-            const float eps = 4e-6f * (1.f + L) + 1e-6f;
-            r.L_lo = L - eps;
-            r.L_hi = L + eps;
-        }
-        return r;
-    };
-    // zc: every token with z <= zc surely fails min-p (d(zc) > L_hi and d is monotone in z).
-    auto threshold = [&](const RowCtx& r) -> float {
-        if (!(r.minp > 0.f)) return -INFINITY;
-        float c = r.zmax - r.L_hi * r.T;
-        float step = fmaxf(fabsf(c) * 1e-6f, 1e-30f);
-        int it = 0;
-        while (!(dist(r, c) > r.L_hi) && it < 64) {
-            c -= step;
-            step *= 2.f;
-            ++it;
-        }
-        return (dist(r, c) > r.L_hi) ? c : -INFINITY;
-    };
-    const bool local_ok = sampling && !timed_out && minp > 0.f && mloc > -INFINITY && mloc < INFINITY;
-    uint32_t nlisted = 0xFFFFFFFFu;  // "no complete list"
-    if (sampling && !timed_out && minp > 0.f && mloc == -INFINITY) nlisted = 0;  // nothing finite here
-    if (local_ok) {
-        const RowCtx rl = make_ctx(mloc);
-        const float zc_loc = threshold(rl);
-        if (tid == 0) s.ncand = 0;
-        __syncthreads();
-        if (zc_loc > -INFINITY) {
-            sl.for_each(s, [&](float z, int32_t i) {
-                if (!(z > zc_loc)) return;
-                const uint32_t slot = atomicAdd(&s.ncand, 1u);
-                if (slot < (uint32_t)kCand) {
-                    s.ckey[slot] = fkey(z);
-                    s.cidx[slot] = (uint32_t)i;
-                }
-            });
-            __syncthreads();
-            nlisted = s.ncand;
-        }
-    }
-    if (tid == 0) {
-        s.pub_max = mloc;
-        s.pub_timeout = timed_out;
-        s.pub_nsurv = nlisted;  // 0xFFFFFFFF or > kCand: this CTA's list is not complete
-        s.pub_gcnt = min(nlisted, (uint32_t)kCand);
-    }
-    cluster.sync();
-    if (tid < 32) {
-        float m = -INFINITY;
-        uint32_t to = 0, nl = 0, cnt = 0, bad = 0;
-        if (lane < C) {
-            m = *cluster.map_shared_rank(&s.pub_max, lane);
-            to = *cluster.map_shared_rank(&s.pub_timeout, lane);
-            nl = *cluster.map_shared_rank(&s.pub_nsurv, lane);
-            bad = nl > (uint32_t)kCand;
-            cnt = bad ? 0u : nl;
-        }
-        uint32_t inc = cnt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-            if ((int)lane >= o) inc += y;
-        }
-        if (lane < C) {
-            s.goff[lane] = inc - cnt;
-            s.gcnt[lane] = cnt;
-        }
-        m = warp_max_nan(m);
-        to = warp_max_u32(to);
-        bad = warp_max_u32(bad);
-        if (lane == 31) s.gtotal = inc;
-        if (lane == 0) {
-            s.bf[0] = m;
-            s.bu[0] = to;
-            s.bu[1] = bad;
-        }
-    }
-    __syncthreads();
-    const float zmax = s.bf[0];
-    const uint32_t cl_timeout = s.bu[0];
-    const bool lists_complete = (s.bu[1] == 0) && (s.gtotal <= (uint32_t)kCand);
-
-    int32_t status = kRowOk;
-    if (cl_timeout) status = kRowTimeout;
-    else if (isnan(zmax) || zmax == INFINITY) status = kRowNan;
-    else if (!params_ok) status = kRowBadParam;
-    else if (zmax == -INFINITY) status = kRowAllMasked;
-
-    float* prow = a.out_probs ? a.out_probs + row * a.V : nullptr;
-    const bool writer = (rank == 0) && (tid == 0);
-
-    if (status != kRowOk) {
-        if (prow) {
-            for (int64_t i = sl.elem0 + tid; i < sl.elem0 + (int64_t)nvec * EPV; i += kThreads) prow[i] = 0.f;
-            for (int x = tid; x < s.nx; x += kThreads) prow[s.xi[x]] = 0.f;
-        }
-        if (writer) {
-            a.out_token[row] = -1;
-            if (a.out_status) a.out_status[row] = status;
-            if (a.out_cutoff) a.out_cutoff[row] = __uint_as_float(0x7FC00000u);
-            if (a.out_kept) a.out_kept[row] = 0;
-        }
-        // A copy still in flight after a timeout must land before the shared memory is released.
-        if (timed_out && bytes > 0) (void)mbar_wait_bounded(&s.mbar, 0, kWaitLimitNs);
-        cluster.sync();
-        return;
-    }
-
-    // ---- greedy branch: lowest index of the maximum ("Implement batched top-p sampling with
-    //      temperature", 'A strong answer': temperature 0 means greedy, ties to the lowest index)
-    if (T <= 0.f) {
-        uint32_t mi = 0xFFFFFFFFu;
-        sl.for_each(s, [&](float z, int32_t i) {
-            if (z == zmax) mi = min(mi, (uint32_t)i);
-        });
-        mi = block_min_u32(mi, s);
-        if (tid == 0) s.pub_minidx = mi;
-        cluster.sync();
+    RowResult out;
+    if (n <= 32) {
         if (tid < 32) {
-            uint32_t m = (lane < C) ? *cluster.map_shared_rank(&s.pub_minidx, lane) : 0xFFFFFFFFu;
-            m = warp_min_u32(m);
-            if (lane == 0) s.bu[2] = m;
+            const WarpResult wr = warp_resolve(s, r, rc, n, topk_on, K, P);
+            if (lane == 0) {
+                s.bu[4] = wr.key_cut;
+                s.bu[5] = wr.nk;
+                s.b64[0] = wr.zk;
+                s.bu[6] = (uint32_t)wr.token;
+            }
         }
         __syncthreads();
-        const uint32_t arg = s.bu[2];
-        if (prow) sl.for_each(s, [&](float, int32_t i) { prow[i] = ((uint32_t)i == arg) ? 1.f : 0.f; });
-        if (writer) {
-            a.out_token[row] = (int32_t)arg;
-            if (a.out_status) a.out_status[row] = kRowOk;
-            if (a.out_cutoff) a.out_cutoff[row] = zmax;
-            if (a.out_kept) a.out_kept[row] = 1;
-        }
-        cluster.sync();
-        return;
+        out.key_cut = s.bu[4];
+        out.nk = s.bu[5];
+        out.zk = s.b64[0];
+        out.token = (int32_t)s.bu[6];
+        __syncthreads();
+        return out;
     }
-
-    const RowCtx r = make_ctx(zmax);
-    const float zc = threshold(r);
-    const bool topk_on = (K > 0) && ((int64_t)K < a.V);
-
-    RaceCtx rc;
-    rc.k0 = (uint32_t)seed;
-    rc.k1 = (uint32_t)(seed >> 32);
-    rc.row = (uint32_t)row;
-    rc.s_lo = (uint32_t)a.step;
-    rc.s_hi = (uint32_t)(a.step >> 32);
-
-    uint32_t key_cut;
-    uint64_t NK, ZK;
-    int32_t token;
-
-    if (lists_complete) {
-        // ================= fast path: every survivor is on some CTA's list =================
-        // Gather the lists (one entry per thread), keep the survivors of min-p against the global
-        // maximum.  This is the last read of another CTA's shared memory.
-        if (tid == 0) s.ncand = 0;
-        __syncthreads();
-        const uint32_t total = s.gtotal;
-        if ((uint32_t)tid < total) {
-            uint32_t rr = 0;
-            while (rr + 1 < C && s.goff[rr + 1] <= (uint32_t)tid) ++rr;
-            const uint32_t off = (uint32_t)tid - s.goff[rr];
-            const uint32_t key = *cluster.map_shared_rank(&s.ckey[off], rr);
-            const uint32_t idx = *cluster.map_shared_rank(&s.cidx[off], rr);
-            const float z = key_to_float(key);
-            if (z > zc && minp_ok(r, z, dist(r, z))) {
-                const uint32_t slot = atomicAdd(&s.ncand, 1u);
-                s.u.cd.sbuf[slot] = sb_make(key, idx);
-            }
-        }
-        cluster_arrive();  // no more remote reads by this CTA; waited for just before exit
-        __syncthreads();
-        const uint32_t n = s.ncand;
-        if (n <= 32) {
-            if (tid < 32) {
-                const WarpResult wr = warp_resolve(s, r, rc, n, topk_on, K, P);
-                if (lane == 0) {
-                    s.bu[4] = wr.key_cut;
-                    s.bu[5] = wr.nk;
-                    s.b64[0] = wr.zk;
-                    s.bu[6] = (uint32_t)wr.token;
-                }
-            }
-            __syncthreads();
-            key_cut = s.bu[4];
-            NK = s.bu[5];
-            ZK = s.b64[0];
-            token = (int32_t)s.bu[6];
-        } else {
-            block_sort_desc(s, (int)n);
-            prefix_masses(s, r, (int)n);
-            int nS = (int)n;
-            uint64_t ZS = s.u.cd.pre[n];
-            if (topk_on && n > (uint32_t)K) {
-                Crit ck;
-                ck.by_mass = false;
-                ck.tcnt = (uint64_t)K;
-                ck.tmass = 0.0;
-                const Sel sk = walk_classes(s, (int)n, ck, 0, 0);
-                nS = (int)sk.cnt;
-                ZS = sk.mass;
-            }
-            NK = (uint64_t)nS;
-            ZK = ZS;
-            if (P < 1.f) {
-                Crit cp;
-                cp.by_mass = P > 0.f;
-                cp.tcnt = 1;
-                cp.tmass = (double)P * (double)ZS;
-                const Sel sp = walk_classes(s, nS, cp, 0, 0);
-                NK = sp.cnt;
-                ZK = sp.mass;
-            }
-            key_cut = sb_key(s.u.cd.sbuf[NK - 1]);
-            // race over the kept prefix (one entry per thread: n <= kCand == kThreads)
-            float k32 = -INFINITY, u = 0.f, z = 0.f;
-            int32_t idx = 0x7FFFFFFF;
-            if (tid < (int)NK) {
-                const uint64_t v = s.u.cd.sbuf[tid];
-                z = key_to_float(sb_key(v));
-                idx = sb_idx(v);
-                u = race_u(rc, idx);
-                k32 = race_key32(dist(r, z), u);
-            }
-            float m32 = k32;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m32 = fmaxf(m32, __shfl_xor_sync(0xFFFFFFFFu, m32, o));
-            if (lane == 0) s.rf[tid >> 5] = m32;
-            __syncthreads();
-            m32 = s.rf[0];
-#pragma unroll
-            for (int w = 1; w < kWarps; ++w) m32 = fmaxf(m32, s.rf[w]);
-            const float tol = race_tol(dist(r, key_to_float(key_cut)));
-            const bool fin = tid < (int)NK && k32 >= m32 - tol;
-            const int nfin = __syncthreads_count(fin);
-            if (nfin == 1) {
-                if (fin) s.bu[6] = (uint32_t)idx;
-                __syncthreads();
-                token = (int32_t)s.bu[6];
-            } else {
-                ArgBest mine;
-                mine.key = -INFINITY;
-                mine.idx = 0x7FFFFFFF;
-                if (fin) {
-                    mine.key = race_key64(r, z, u);
-                    mine.idx = idx;
-                }
-                token = block_argbest(mine, s).idx;
-            }
-        }
-        if (prow) {
-            const double zk = (double)ZK;
-            const uint32_t kc = key_cut;
-            sl.for_each(s, [&](float z, int32_t i) {
-                float pv = 0.f;
-                if (z > -INFINITY && fkey(z) >= kc) pv = (float)((double)qmass_d(dist(r, z)) / zk);
-                prow[i] = pv;
-            });
-        }
-        if (writer) {
-            a.out_token[row] = token;
-            if (a.out_status) a.out_status[row] = kRowOk;
-            if (a.out_cutoff) a.out_cutoff[row] = key_to_float(key_cut);
-            if (a.out_kept) a.out_kept[row] = (int32_t)NK;
-        }
-        cluster_wait();  // every CTA has finished reading this CTA's lists
-        return;
+    block_sort_desc(s, (int)n);
+    prefix_masses(s, r, (int)n);
+    int nS = (int)n;
+    uint64_t ZS = s.u.cd.pre[n];
+    if (topk_on && n > (uint32_t)K) {
+        Crit ck;
+        ck.by_mass = false;
+        ck.tcnt = (uint64_t)K;
+        ck.tmass = 0.0;
+        const Sel sk = walk_classes(s, (int)n, ck, 0, 0);
+        nS = (int)sk.cnt;
+        ZS = sk.mass;
     }
+    out.nk = (uint64_t)nS;
+    out.zk = ZS;
+    if (P < 1.f) {
+        Crit cp;
+        cp.by_mass = P > 0.f;
+        cp.tcnt = 1;
+        cp.tmass = (double)P * (double)ZS;
+        const Sel sp = walk_classes(s, nS, cp, 0, 0);
+        out.nk = sp.cnt;
+        out.zk = sp.mass;
+    }
+    out.key_cut = sb_key(s.u.cd.sbuf[out.nk - 1]);
+    // race over the kept prefix (one entry per thread: n <= kCand == kThreads)
+    float k32 = -INFINITY, u = 0.f, z = 0.f;
+    int32_t idx = 0x7FFFFFFF;
+    if (tid < (int)out.nk) {
+        const uint64_t v = s.u.cd.sbuf[tid];
+        z = key_to_float(sb_key(v));
+        idx = sb_idx(v);
+        u = race_u(rc, idx);
+        k32 = race_key32(dist(r, z), u);
+    }
+    float m32 = k32;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m32 = fmaxf(m32, __shfl_xor_sync(0xFFFFFFFFu, m32, o));
+    __syncthreads();
+    if (lane == 0) s.rf[tid >> 5] = m32;
+    __syncthreads();
+    m32 = s.rf[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) m32 = fmaxf(m32, s.rf[w]);
+    const float tol = race_tol(dist(r, key_to_float(out.key_cut)));
+    const bool fin = tid < (int)out.nk && k32 >= m32 - tol;
+    const int nfin = __syncthreads_count(fin);
+    if (nfin == 1) {
+        if (fin) s.bu[6] = (uint32_t)idx;
+        __syncthreads();
+        out.token = (int32_t)s.bu[6];
+    } else {
+        ArgBest mine;
+        mine.key = -INFINITY;
+        mine.idx = 0x7FFFFFFF;
+        if (fin) {
+            mine.key = race_key64(r, z, u);
+            mine.idx = idx;
+        }
+        out.token = block_argbest(mine, s).idx;
+    }
+    __syncthreads();
+    return out;
+}
 
-    // ================= general path: survivors against the global maximum =================
-    cluster.sync();  // nobody still reads the local lists or the published values
+// Renormalised probabilities of the kept set over every element a source covers.
+template <typename Src>
+__device__ __forceinline__ void write_probs(const Src& src, const Shared& s, const RowCtx& r, uint32_t key_cut,
+                                            uint64_t zk, float* prow)
+{
+    const double z64 = (double)zk;
+    src.for_each(s, [&](float z, int32_t i) {
+        float pv = 0.f;
+        if (z > -INFINITY && fkey(z) >= key_cut) pv = (float)((double)qmass_d(dist(r, z)) / z64);
+        prow[i] = pv;
+    });
+}
+
+// The general path: min-p survivors counted against the global maximum (threshold zc), then the
+// top-k and top-p cuts -- from a sorted candidate list when there are few survivors, else located by
+// a histogram over d and refined exactly -- then the race over the kept tokens of the source, with
+// the optional probability row written in the same pass.  Starts with a topology barrier, so the
+// caller's published values may still be read by other CTAs when it is entered.
+template <typename Topo, typename Src>
+__device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const RowCtx& r, float zc, bool topk_on,
+                                  int32_t K, float P, const RaceCtx& rc, float* prow)
+{
+    const int tid = threadIdx.x;
+    const uint32_t lane = tid & 31;
+    const uint32_t C = topo.C;
+    topo.sync();  // nobody still reads the caller's lists or published values
     if (tid == 0) s.ncand = 0;
     __syncthreads();
     uint32_t my_minkey = 0xFFFFFFFFu;
     uint32_t my_surv = 0;
-    sl.for_each(s, [&](float z, int32_t i) {
+    src.for_each(s, [&](float z, int32_t i) {
         if (!(z > zc)) return;
         if (!minp_ok(r, z, dist(r, z))) return;
         const uint32_t key = fkey(z);
@@ -1121,12 +944,12 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
         s.pub_gcnt = min(ns, (uint32_t)kCand);
         s.pub_minkey = mk;
     }
-    cluster.sync();
+    topo.sync();
     if (tid < 32) {
         uint32_t ns = 0, mk = 0xFFFFFFFFu;
         if (lane < C) {
-            ns = *cluster.map_shared_rank(&s.pub_nsurv, lane);
-            mk = *cluster.map_shared_rank(&s.pub_minkey, lane);
+            ns = *topo.map(&s.pub_nsurv, lane);
+            mk = *topo.map(&s.pub_minkey, lane);
         }
         ns = warp_sum_u32(ns);
         mk = warp_min_u32(mk);
@@ -1137,12 +960,14 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
     }
     __syncthreads();
     const uint64_t NS0 = s.bu[2];
-    key_cut = s.bu[3];
-    NK = NS0;
-    ZK = 0;
+    RowResult res;
+    res.key_cut = s.bu[3];
+    res.nk = NS0;
+    res.zk = 0;
+
     if (NS0 <= (uint64_t)kCand) {
-        // ---- few survivors after all (the local lists overflowed): sort them in every CTA
-        const int n = gather_and_sort(cluster, s, C);
+        // ---- few survivors: sort them (in every CTA)
+        const int n = gather_and_sort(topo, s);
         prefix_masses(s, r, n);
         int nS = n;
         uint64_t ZS = s.u.cd.pre[n];
@@ -1155,18 +980,18 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
             nS = (int)sk.cnt;
             ZS = sk.mass;
         }
-        NK = (uint64_t)nS;
-        ZK = ZS;
+        res.nk = (uint64_t)nS;
+        res.zk = ZS;
         if (P < 1.f) {
             Crit cp;
             cp.by_mass = P > 0.f;
             cp.tcnt = 1;
             cp.tmass = (double)P * (double)ZS;
             const Sel sp = walk_classes(s, nS, cp, 0, 0);
-            NK = sp.cnt;
-            ZK = sp.mass;
+            res.nk = sp.cnt;
+            res.zk = sp.mass;
         }
-        key_cut = sb_key(s.u.cd.sbuf[NK - 1]);
+        res.key_cut = sb_key(s.u.cd.sbuf[res.nk - 1]);
     } else {
         // ---- many survivors: histogram-located cuts, refined exactly
         for (int b = tid; b < kBins; b += kThreads) {
@@ -1175,7 +1000,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
         }
         __syncthreads();
         auto build_hist = [&](uint32_t key_floor) {
-            sl.for_each(s, [&](float z, int32_t) {
+            src.for_each(s, [&](float z, int32_t) {
                 if (!(z > zc)) return;
                 if (fkey(z) < key_floor) return;
                 const float d = dist(r, z);
@@ -1186,7 +1011,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
             });
         };
         build_hist(0u);
-        cluster_reduce_hist(cluster, s, kBins, C, rank);
+        cluster_reduce_hist(topo, s, kBins);
         uint64_t ZS;
         {
             uint64_t tot;
@@ -1203,23 +1028,23 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
             uint64_t c_at, a_at;
             scan_bins(s, kBins, ck, 0, 0, &bk, &c_at, &a_at);
             if (bk < 0) bk = 0;
-            const Sel sk = refine_bin<TIn>(cluster, s, sl, r, zc, C, bk, 0u, ck, c_at, a_at);
-            key_cut = max(key_cut, sk.key);
+            const Sel sk = refine_bin(topo, s, src, r, zc, bk, 0u, ck, c_at, a_at);
+            res.key_cut = max(res.key_cut, sk.key);
             NS = sk.cnt;
             ZS = sk.mass;
             if (P < 1.f) {  // rebuild the histogram over S = {key >= key_cut} for the top-p scan
-                cluster.sync();
+                topo.sync();
                 for (int b = tid; b < kBins; b += kThreads) {
                     s.hcnt[b] = 0;
                     s.hmass[b] = 0;
                 }
                 __syncthreads();
-                build_hist(key_cut);
-                cluster_reduce_hist(cluster, s, kBins, C, rank);
+                build_hist(res.key_cut);
+                cluster_reduce_hist(topo, s, kBins);
             }
         }
-        NK = NS;
-        ZK = ZS;
+        res.nk = NS;
+        res.zk = ZS;
         if (P < 1.f) {
             Crit cp;
             cp.by_mass = P > 0.f;
@@ -1229,21 +1054,21 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
             uint64_t c_at, a_at;
             scan_bins(s, kBins, cp, 0, 0, &bp, &c_at, &a_at);
             if (bp < 0) bp = 0;
-            const Sel sp = refine_bin<TIn>(cluster, s, sl, r, zc, C, bp, key_cut, cp, c_at, a_at);
-            key_cut = max(key_cut, sp.key);
-            NK = sp.cnt;
-            ZK = sp.mass;
+            const Sel sp = refine_bin(topo, s, src, r, zc, bp, res.key_cut, cp, c_at, a_at);
+            res.key_cut = max(res.key_cut, sp.key);
+            res.nk = sp.cnt;
+            res.zk = sp.mass;
         }
     }
 
-    // ---- race over the kept tokens of the slice (+ probabilities): float keys first; the
-    //      cluster's best two decide whether double precision is needed at all
-    const float tol = race_tol(dist(r, key_to_float(key_cut)));
-    const uint32_t kc = key_cut;
-    const double zk = (double)ZK;
+    // ---- race over the kept tokens of the source (+ probabilities): float keys first; the best
+    //      two decide whether double precision is needed at all
+    const float tol = race_tol(dist(r, key_to_float(res.key_cut)));
+    const uint32_t kc = res.key_cut;
+    const double zk = (double)res.zk;
     Top2 t2;
     t2.init();
-    sl.for_each(s, [&](float z, int32_t i) {
+    src.for_each(s, [&](float z, int32_t i) {
         const bool kept = (z > -INFINITY) && fkey(z) >= kc;
         if (prow) prow[i] = kept ? (float)((double)qmass_d(dist(r, z)) / zk) : 0.f;
         if (!kept) return;
@@ -1267,18 +1092,18 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
             x.k2 = s.rf[w];
             b.merge(x);
         }
-        s.pub_k64 = (double)b.k1;   // published: best float key, its index, second float key
+        s.pub_k64 = (double)b.k1;  // published: best float key, its index, second float key
         s.pub_idx = b.i1;
         s.pub_max = b.k2;
     }
-    cluster.sync();
+    topo.sync();
     if (tid < 32) {
         Top2 x;
         x.init();
         if (lane < C) {
-            x.k1 = (float)*cluster.map_shared_rank(&s.pub_k64, lane);
-            x.i1 = *cluster.map_shared_rank(&s.pub_idx, lane);
-            x.k2 = *cluster.map_shared_rank(&s.pub_max, lane);
+            x.k1 = (float)*topo.map(&s.pub_k64, lane);
+            x.i1 = *topo.map(&s.pub_idx, lane);
+            x.k2 = *topo.map(&s.pub_max, lane);
         }
         x = warp_top2(x);
         if (lane == 0) {
@@ -1289,13 +1114,13 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
     }
     __syncthreads();
     const float M1 = s.bf[1], M2 = s.bf[0];
-    token = (int32_t)s.bu[6];
+    res.token = (int32_t)s.bu[6];
     if (!(M1 - M2 > tol)) {
         // near-tie: every kept token within tol of the best is re-evaluated in double precision
         ArgBest mine;
         mine.key = -INFINITY;
         mine.idx = 0x7FFFFFFF;
-        sl.for_each(s, [&](float z, int32_t i) {
+        src.for_each(s, [&](float z, int32_t i) {
             if (!((z > -INFINITY) && fkey(z) >= kc)) return;
             const float u = race_u(rc, i);
             if (race_key32(dist(r, z), u) >= M1 - tol) {
@@ -1307,33 +1132,38 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
             }
         });
         mine = block_argbest(mine, s);
-        cluster.sync();  // everyone has read the published float keys
+        topo.sync();  // everyone has read the published float keys
         if (tid == 0) {
             s.pub_k64 = mine.key;
             s.pub_idx = mine.idx;
         }
-        cluster.sync();
+        topo.sync();
         if (tid < 32) {
             ArgBest x;
             x.key = -INFINITY;
             x.idx = 0x7FFFFFFF;
             if (lane < C) {
-                x.key = *cluster.map_shared_rank(&s.pub_k64, lane);
-                x.idx = *cluster.map_shared_rank(&s.pub_idx, lane);
+                x.key = *topo.map(&s.pub_k64, lane);
+                x.idx = *topo.map(&s.pub_idx, lane);
             }
             x = warp_argbest(x);
             if (lane == 0) s.bu[6] = (uint32_t)x.idx;
         }
         __syncthreads();
-        token = (int32_t)s.bu[6];
+        res.token = (int32_t)s.bu[6];
     }
-    if (writer) {
-        a.out_token[row] = token;
-        if (a.out_status) a.out_status[row] = kRowOk;
-        if (a.out_cutoff) a.out_cutoff[row] = key_to_float(key_cut);
-        if (a.out_kept) a.out_kept[row] = (int32_t)NK;
-    }
-    cluster.sync();  // keep this CTA's shared memory alive until every remote read is done
+    __syncthreads();
+    return res;
+}
+
+// Per-row outputs (thread 0 of the writing CTA).
+__device__ __forceinline__ void write_row(const Args& a, int64_t row, int32_t token, int32_t status, float cutoff,
+                                          int32_t kept)
+{
+    a.out_token[row] = token;
+    if (a.out_status) a.out_status[row] = status;
+    if (a.out_cutoff) a.out_cutoff[row] = cutoff;
+    if (a.out_kept) a.out_kept[row] = kept;
 }
 
 }  // namespace tps

@@ -11,11 +11,11 @@ TOPP_BAND, MINP_BAND, RACE_BAND = oracle.FLAG_TOPP_BAND, oracle.FLAG_MINP_BAND, 
 PROB_TOL = 1e-5  # absolute, on renormalised probabilities
 
 
-def run_gpu(w, want_probs=True, logits=None):
+def run_gpu(w, want_probs=True, logits=None, kernel="auto"):
     d = w.to("cuda")
     lg = d.logits if logits is None else logits
     r = tps.sample(lg, d.temperature, d.top_k, d.top_p, d.min_p, d.seed, d.step, want_probs=want_probs,
-                   diagnostics=True)
+                   diagnostics=True, kernel=kernel)
     torch.cuda.synchronize()
     return {k: v.cpu() for k, v in r.items()}
 
