@@ -50,6 +50,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-latency", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "cluster", "stream"])
     return ap.parse_args()
 
 
@@ -249,7 +250,7 @@ def main():
     out = {"token": tok}
 
     def step(i):
-        tps.sample(w.logits, w.temperature, w.top_k, w.top_p, w.min_p, w.seed, i, out=out)
+        tps.sample(w.logits, w.temperature, w.top_k, w.top_p, w.min_p, w.seed, i, out=out, kernel=args.kernel)
 
     for i in range(args.warmup):
         step(i)

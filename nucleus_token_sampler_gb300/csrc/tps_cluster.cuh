@@ -93,8 +93,12 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
     timed_out = __syncthreads_or(timed_out) ? 1u : 0u;
 
     // ---- A: local maximum with NaN propagation (a NaN anywhere makes the maximum NaN)
+    auto nolist = [](float, int32_t) {};
     float vmax = -INFINITY;
-    if (!timed_out) sl.for_each(s, [&](float z, int32_t) { vmax = fmax_nan(vmax, z); });
+    if (!timed_out) {
+        vmax = scan_max_list<TIn, false>(sl.vec, sl.nvec, (int32_t)sl.elem0, INFINITY, nolist);
+        for (int x = tid; x < s.nx; x += kThreads) vmax = fmax_nan(vmax, s.xz[x]);
+    }
     vmax = warp_max_nan(vmax);
     if (lane == 0) s.rf[tid >> 5] = vmax;
     __syncthreads();
@@ -109,19 +113,20 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
     uint32_t nlisted = 0xFFFFFFFFu;  // "no complete list"
     if (sampling && !timed_out && minp > 0.f && mloc == -INFINITY) nlisted = 0;  // nothing finite here
     if (local_ok) {
-        const RowCtx rl = make_ctx(mloc, T, minp);
-        const float zc_loc = minp_threshold(rl);
+        const float zc_loc = list_threshold(mloc, make_ctx(0.f, T, minp).L_hi * T * (1.f + 1e-5f));
         if (tid == 0) s.ncand = 0;
         __syncthreads();
         if (zc_loc > -INFINITY) {
-            sl.for_each(s, [&](float z, int32_t i) {
-                if (!(z > zc_loc)) return;
+            auto list_token = [&](float z, int32_t i) {
                 const uint32_t slot = atomicAdd(&s.ncand, 1u);
                 if (slot < (uint32_t)kCand) {
                     s.ckey[slot] = fkey(z);
                     s.cidx[slot] = (uint32_t)i;
                 }
-            });
+            };
+            (void)scan_max_list<TIn, false>(sl.vec, sl.nvec, (int32_t)sl.elem0, zc_loc, list_token);
+            for (int x = tid; x < s.nx; x += kThreads)
+                if (s.xz[x] > zc_loc) list_token(s.xz[x], s.xi[x]);
             __syncthreads();
             nlisted = s.ncand;
         }

@@ -253,6 +253,65 @@ using Slice = VecSource<TIn, false>;
 template <typename TIn>
 using GlobalRow = VecSource<TIn, true>;
 
+// Maximum (NaN-propagating) over nvec 16-byte vectors, listing every element above thr through
+// list(z, i).  Each thread takes 16 elements per step and reduces them with a tree of max
+// operations; only a step whose maximum exceeds thr is looked at element by element, so a pass
+// costs about one instruction per element when little is listed.
+template <typename TIn, bool kGlobal, typename ListF>
+__device__ __forceinline__ float scan_max_list(const uint4* vec, int nvec, int32_t elem0, float thr, ListF&& list)
+{
+    using E = Elem<TIn>;
+    constexpr int EPV = E::kPerVec;
+    constexpr int U = 16 / EPV;  // vectors per step
+    const uint4 neg_inf = (EPV == 4) ? make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u)
+                                     : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+    float cm = -INFINITY;
+    for (int v = threadIdx.x; v < nvec; v += U * kThreads) {
+        uint4 w[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int vi = v + u * kThreads;
+            if (vi < nvec) {
+                if constexpr (kGlobal) w[u] = __ldg(vec + vi);
+                else w[u] = vec[vi];
+            } else {
+                w[u] = neg_inf;
+            }
+        }
+        float z[U * EPV];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            float t[EPV];
+            E::unpack(w[u], t);
+#pragma unroll
+            for (int j = 0; j < EPV; ++j) z[u * EPV + j] = t[j];
+        }
+        float m8[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) m8[j] = fmax_nan(z[j], z[j + 8]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) m8[j] = fmax_nan(m8[j], m8[j + 4]);
+        const float m = fmax_nan(fmax_nan(m8[0], m8[2]), fmax_nan(m8[1], m8[3]));
+        cm = fmax_nan(cm, m);
+        if (m > thr) {
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int j = 0; j < EPV; ++j)
+                    if (z[u * EPV + j] > thr) list(z[u * EPV + j], elem0 + (v + u * kThreads) * EPV + j);
+        }
+    }
+    return cm;
+}
+
+// A listing threshold that min-p, measured against any maximum >= m, surely rejects at or below:
+// m - (L_hi T (1 + 1e-5) + |m| 2^-20).  The margins cover the float rounding of this expression
+// and of d = (zmax - z) / T, so every token at or below it has d > L_hi against the true maximum.
+__device__ __forceinline__ float list_threshold(float m, float lt_hi)
+{
+    return m - (lt_hi + fabsf(m) * 0x1p-20f);
+}
+
 __device__ __forceinline__ int bin_of(float d)
 {
     return min(__float2int_rz(d * kBinScale), kBins - 1);

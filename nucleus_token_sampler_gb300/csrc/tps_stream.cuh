@@ -60,7 +60,6 @@ template <typename TIn>
 __global__ void __launch_bounds__(kThreads, 1) stream_rows_kernel(const Args a, int nstage, uint32_t chunk_bytes)
 {
     using E = Elem<TIn>;
-    constexpr int EPV = E::kPerVec;
     constexpr int ES = E::kBytes;
     extern __shared__ __align__(128) unsigned char dsmem[];
     unsigned char* ring = dsmem;
@@ -133,6 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_rows_kernel(const Args a, 
         const bool sampling = params_ok && T > 0.f;
         const float minp = (MP > 0.f) ? fminf(MP, 1.f) : 0.f;
         const bool listing = sampling && minp > 0.f;
+        const float lt_hi = listing ? make_ctx(0.f, T, minp).L_hi * T * (1.f + 1e-5f) : 0.f;
 
         // ragged head/tail: loads issued now, used after the last chunk
         const int nx = g.nhead + g.ntail;
@@ -148,8 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_rows_kernel(const Args a, 
         float runmax = -INFINITY;  // maximum over the chunks finished so far (same in every thread)
         float thr = INFINITY;      // list tokens with z > thr
         auto set_thr = [&]() {
-            if (listing && runmax > -INFINITY && runmax < INFINITY) thr = minp_threshold(make_ctx(runmax, T, minp));
-            else thr = INFINITY;
+            thr = (listing && runmax > -INFINITY && runmax < INFINITY) ? list_threshold(runmax, lt_hi) : INFINITY;
+            if (isnan(thr)) thr = INFINITY;
         };
         auto list_token = [&](float z, int32_t i) {
             const uint32_t slot = atomicAdd(&s.ncand, 1u);
@@ -171,16 +171,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_rows_kernel(const Args a, 
                 dead = true;
                 break;
             }
-            float cm = -INFINITY;
+            auto nolist = [](float, int32_t) {};
+            float cm;
             if (c == 0) {
                 // first chunk: its own maximum sets the first listing threshold
-                for (int v = tid; v < nv; v += kThreads) {
-                    float z[EPV];
-                    E::unpack(cv[v], z);
-#pragma unroll
-                    for (int j = 0; j < EPV; ++j) cm = fmax_nan(cm, z[j]);
-                }
-                cm = warp_max_nan(cm);
+                cm = warp_max_nan(scan_max_list<TIn, false>(cv, nv, e0, INFINITY, nolist));
                 if (lane == 0) st.cmax[1][warp] = cm;
                 __syncthreads();
                 float m0 = st.cmax[1][0];
@@ -188,44 +183,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_rows_kernel(const Args a, 
                 for (int w = 1; w < kWarps; ++w) m0 = fmax_nan(m0, st.cmax[1][w]);
                 runmax = m0;
                 set_thr();
-                if (listing) {
-                    for (int v = tid; v < nv; v += kThreads) {
-                        float z[EPV];
-                        E::unpack(cv[v], z);
-#pragma unroll
-                        for (int j = 0; j < EPV; ++j)
-                            if (z[j] > thr) list_token(z[j], e0 + v * EPV + j);
-                    }
-                }
+                if (listing) (void)scan_max_list<TIn, false>(cv, nv, e0, thr, list_token);
                 cm = m0;
             } else {
-                constexpr int U = 4;
-                int v = tid;
-                for (; v + (U - 1) * kThreads < nv; v += U * kThreads) {
-                    uint4 w4[U];
-#pragma unroll
-                    for (int u = 0; u < U; ++u) w4[u] = cv[v + u * kThreads];
-#pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        float z[EPV];
-                        E::unpack(w4[u], z);
-#pragma unroll
-                        for (int j = 0; j < EPV; ++j) {
-                            cm = fmax_nan(cm, z[j]);
-                            if (z[j] > thr) list_token(z[j], e0 + (v + u * kThreads) * EPV + j);
-                        }
-                    }
-                }
-                for (; v < nv; v += kThreads) {
-                    float z[EPV];
-                    E::unpack(cv[v], z);
-#pragma unroll
-                    for (int j = 0; j < EPV; ++j) {
-                        cm = fmax_nan(cm, z[j]);
-                        if (z[j] > thr) list_token(z[j], e0 + v * EPV + j);
-                    }
-                }
-                cm = warp_max_nan(cm);
+                cm = warp_max_nan(scan_max_list<TIn, false>(cv, nv, e0, thr, list_token));
             }
             const int par = c & 1;
             if (lane == 0) st.cmax[par][warp] = cm;
