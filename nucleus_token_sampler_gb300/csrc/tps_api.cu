@@ -25,8 +25,8 @@ constexpr int64_t kMaxVocabMass = (int64_t(1) << 20) - 1;  // fixed-point mass s
 constexpr uint32_t kSliceTarget = 64u * 1024u;              // preferred slice per CTA
 constexpr int kMaxCluster = 16;
 
-constexpr int kStreamStages = 6;
-constexpr uint32_t kStreamChunk = 32u * 1024u;
+constexpr int kStreamStages = 3;
+constexpr uint32_t kStreamChunk = 64u * 1024u;
 constexpr int64_t kStreamMinRows = 32;  // batches at least this large use the streaming kernel
 
 struct DeviceInfo {
@@ -145,7 +145,7 @@ cudaError_t launch_stream(const DeviceInfo& d, bool* attrs_done, const tps::Args
         *attrs_done = true;
     }
     const int64_t grid = a.B < (int64_t)d.sms ? a.B : (int64_t)d.sms;
-    k<<<(unsigned)grid, tps::kThreads, smem, stream>>>(a, kStreamStages, kStreamChunk);
+    k<<<(unsigned)grid, tps::kStreamThreads, smem, stream>>>(a, kStreamStages, kStreamChunk);
     return cudaGetLastError();
 }
 

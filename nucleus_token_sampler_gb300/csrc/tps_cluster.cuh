@@ -87,10 +87,10 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
     const bool params_ok = isfinite(T) && isfinite(P) && isfinite(MP);
     const bool sampling = params_ok && T > 0.f;
     const float minp = (MP > 0.f) ? fminf(MP, 1.f) : 0.f;
-    __syncthreads();  // mbarrier initialised, extras stored
+    cta_sync();  // mbarrier initialised, extras stored
     uint32_t timed_out = 0;
     if (bytes > 0 && !mbar_wait_bounded(&s.mbar, 0, kWaitLimitNs)) timed_out = 1;
-    timed_out = __syncthreads_or(timed_out) ? 1u : 0u;
+    timed_out = cta_sync_or(timed_out) ? 1u : 0u;
 
     // ---- A: local maximum with NaN propagation (a NaN anywhere makes the maximum NaN)
     auto nolist = [](float, int32_t) {};
@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
     }
     vmax = warp_max_nan(vmax);
     if (lane == 0) s.rf[tid >> 5] = vmax;
-    __syncthreads();
+    cta_sync();
     float mloc = s.rf[0];
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) mloc = fmax_nan(mloc, s.rf[w]);
@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
     if (local_ok) {
         const float zc_loc = list_threshold(mloc, make_ctx(0.f, T, minp).L_hi * T * (1.f + 1e-5f));
         if (tid == 0) s.ncand = 0;
-        __syncthreads();
+        cta_sync();
         if (zc_loc > -INFINITY) {
             auto list_token = [&](float z, int32_t i) {
                 const uint32_t slot = atomicAdd(&s.ncand, 1u);
@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
             (void)scan_max_list<TIn, false>(sl.vec, sl.nvec, (int32_t)sl.elem0, zc_loc, list_token);
             for (int x = tid; x < s.nx; x += kThreads)
                 if (s.xz[x] > zc_loc) list_token(s.xz[x], s.xi[x]);
-            __syncthreads();
+            cta_sync();
             nlisted = s.ncand;
         }
     }
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
             s.bu[1] = bad;
         }
     }
-    __syncthreads();
+    cta_sync();
     const float zmax = s.bf[0];
     const uint32_t cl_timeout = s.bu[0];
     const bool lists_complete = (s.bu[1] == 0) && (s.gtotal <= (uint32_t)kCand);
@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
             m = warp_min_u32(m);
             if (lane == 0) s.bu[2] = m;
         }
-        __syncthreads();
+        cta_sync();
         const uint32_t arg = s.bu[2];
         if (prow) sl.for_each(s, [&](float, int32_t i) { prow[i] = ((uint32_t)i == arg) ? 1.f : 0.f; });
         if (writer) {
@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
         // Gather the lists (one entry per thread), keep the survivors of min-p against the global
         // maximum.  This is the last read of another CTA's shared memory.
         if (tid == 0) s.ncand = 0;
-        __syncthreads();
+        cta_sync();
         const uint32_t total = s.gtotal;
         if ((uint32_t)tid < total) {
             uint32_t rr = 0;
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
             }
         }
         cluster_arrive();  // no more remote reads by this CTA; waited for just before exit
-        __syncthreads();
+        cta_sync();
         const uint32_t n = s.ncand;
         const RowResult res = resolve_candidates(s, r, rc, n, topk_on, K, P);
         const uint32_t key_cut = res.key_cut;

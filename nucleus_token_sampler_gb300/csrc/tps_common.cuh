@@ -96,15 +96,48 @@ struct Shared {
 };
 
 // ---------------------------------------------------------------------------------------------
+// CTA barriers over the kThreads sampling threads only (named barrier 1).  The streaming kernel
+// adds one producer warp that never joins them; in the cluster kernel they cover the whole CTA.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void cta_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+
+__device__ __forceinline__ int cta_sync_or(int pred)
+{
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.s32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, 1, %2, pi;\n\t"
+        "selp.s32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(pred), "n"(kThreads)
+        : "memory");
+    return r;
+}
+
+__device__ __forceinline__ int cta_sync_count(int pred)
+{
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred pi;\n\t"
+        "setp.ne.s32 pi, %1, 0;\n\t"
+        "bar.red.popc.u32 %0, 1, %2, pi;\n\t}"
+        : "=r"(r)
+        : "r"(pred), "n"(kThreads)
+        : "memory");
+    return r;
+}
+
+// ---------------------------------------------------------------------------------------------
 // Block-level helpers (every thread of the CTA must call them).  Each starts with a barrier so
 // its scratch can be reused right after the previous call.
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, Shared& s)
 {
     v = warp_sum_u32(v);
-    __syncthreads();
+    cta_sync();
     if ((threadIdx.x & 31) == 0) s.ra[threadIdx.x >> 5] = v;
-    __syncthreads();
+    cta_sync();
     uint32_t r = 0;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) r += s.ra[w];
@@ -114,9 +147,9 @@ __device__ __forceinline__ uint32_t block_sum_u32(uint32_t v, Shared& s)
 __device__ __forceinline__ uint32_t block_min_u32(uint32_t v, Shared& s)
 {
     v = warp_min_u32(v);
-    __syncthreads();
+    cta_sync();
     if ((threadIdx.x & 31) == 0) s.rb[threadIdx.x >> 5] = v;
-    __syncthreads();
+    cta_sync();
     uint32_t r = s.rb[0];
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) r = min(r, s.rb[w]);
@@ -126,9 +159,9 @@ __device__ __forceinline__ uint32_t block_min_u32(uint32_t v, Shared& s)
 __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, Shared& s)
 {
     v = warp_max_u32(v);
-    __syncthreads();
+    cta_sync();
     if ((threadIdx.x & 31) == 0) s.rb[threadIdx.x >> 5] = v;
-    __syncthreads();
+    cta_sync();
     uint32_t r = s.rb[0];
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) r = max(r, s.rb[w]);
@@ -138,9 +171,9 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, Shared& s)
 __device__ __forceinline__ ArgBest block_argbest(ArgBest a, Shared& s)
 {
     a = warp_argbest(a);
-    __syncthreads();
+    cta_sync();
     if ((threadIdx.x & 31) == 0) s.rab[threadIdx.x >> 5] = a;
-    __syncthreads();
+    cta_sync();
     ArgBest r = s.rab[0];
 #pragma unroll
     for (int w = 1; w < kWarps; ++w)
@@ -158,9 +191,9 @@ __device__ __forceinline__ uint64_t block_exscan_u64(uint64_t v, Shared& s, uint
         const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
         if (lane >= o) x += y;
     }
-    __syncthreads();
+    cta_sync();
     if (lane == 31) s.r64[warp] = x;
-    __syncthreads();
+    cta_sync();
     uint64_t before = 0, all = 0;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
@@ -194,7 +227,7 @@ struct ClusterTopo {
 
 struct SoloTopo {
     uint32_t C = 1, rank = 0;
-    __device__ __forceinline__ void sync() { __syncthreads(); }
+    __device__ __forceinline__ void sync() { cta_sync(); }
     template <typename T>
     __device__ __forceinline__ T* map(T* p, uint32_t)
     {
@@ -325,7 +358,7 @@ __device__ __forceinline__ void cluster_reduce_hist(Topo& topo, Shared& s, int n
 {
     const uint32_t C = topo.C, rank = topo.rank;
     if (C == 1) {  // a single CTA already holds the full histogram
-        __syncthreads();
+        cta_sync();
         return;
     }
     const int per = (nb + (int)C - 1) / (int)C;
@@ -335,7 +368,7 @@ __device__ __forceinline__ void cluster_reduce_hist(Topo& topo, Shared& s, int n
         s.u.sh.rcnt[b] = 0;
         s.u.sh.rmass[b] = 0;
     }
-    __syncthreads();
+    cta_sync();
     const int npairs = (b1 - b0) * (int)C;
     for (int p = threadIdx.x; p < npairs; p += kThreads) {
         const int b = b0 + p / (int)C;
@@ -353,7 +386,7 @@ __device__ __forceinline__ void cluster_reduce_hist(Topo& topo, Shared& s, int n
         s.hcnt[b] = *topo.map(&s.u.sh.rcnt[b], owner);
         s.hmass[b] = *topo.map(&s.u.sh.rmass[b], owner);
     }
-    __syncthreads();
+    cta_sync();
 }
 
 struct Sel {
@@ -389,11 +422,11 @@ __device__ __forceinline__ void scan_bins(Shared& s, int nb, const Crit& cr, uin
         s.b64[0] = C0 + cpre;
         s.b64[1] = A0 + mpre;
     }
-    __syncthreads();
+    cta_sync();
     *out_bin = (int)bb - 1;
     *out_c = bb ? s.b64[0] : C0;
     *out_a = bb ? s.b64[1] : A0;
-    __syncthreads();
+    cta_sync();
 }
 
 // Sort u.cd.sbuf[0, n) descending (bitonic, padded with zeros to a power of two).
@@ -403,7 +436,7 @@ __device__ __forceinline__ void block_sort_desc(Shared& s, int n)
     int np = 2;
     while (np < n) np <<= 1;
     for (int i = n + (int)threadIdx.x; i < np; i += kThreads) sb[i] = 0;
-    __syncthreads();
+    cta_sync();
     for (int k2 = 2; k2 <= np; k2 <<= 1) {
         for (int j = k2 >> 1; j > 0; j >>= 1) {
             for (int i = threadIdx.x; i < (np >> 1); i += kThreads) {
@@ -415,7 +448,7 @@ __device__ __forceinline__ void block_sort_desc(Shared& s, int n)
                     sb[hi] = x;
                 }
             }
-            __syncthreads();
+            cta_sync();
         }
     }
 }
@@ -436,7 +469,7 @@ __device__ __forceinline__ void prefix_masses(Shared& s, const RowCtx& r, int n)
     const uint64_t run = block_exscan_u64(q, s, &tot);
     if (t < n) s.u.cd.pre[t] = run;
     if (t == 0) s.u.cd.pre[n] = tot;
-    __syncthreads();
+    cta_sync();
 }
 
 // Walk the classes of the sorted candidates sbuf[0, n) and return the last class whose
@@ -458,7 +491,7 @@ __device__ __forceinline__ Sel walk_classes(Shared& s, int n, const Crit& cr, ui
     out.key = sb_key(sb[st]);
     out.cnt = C0 + e;
     out.mass = A0 + s.u.cd.pre[e];
-    __syncthreads();
+    cta_sync();
     return out;
 }
 
@@ -482,7 +515,7 @@ __device__ __forceinline__ int gather_and_sort(Topo& topo, Shared& s)
         }
         if (lane == 31) s.gtotal = inc;
     }
-    __syncthreads();
+    cta_sync();
     const uint32_t n = s.gtotal;
     for (uint32_t rr = 0; rr < C; ++rr) {  // each count <= kCand == kThreads
         const uint32_t off = s.goff[rr], cnt = s.gcnt[rr];
@@ -492,7 +525,7 @@ __device__ __forceinline__ int gather_and_sort(Topo& topo, Shared& s)
             s.u.cd.sbuf[off + threadIdx.x] = sb_make(k, i);
         }
     }
-    __syncthreads();
+    cta_sync();
     block_sort_desc(s, (int)n);
     return (int)n;
 }
@@ -536,7 +569,7 @@ __device__ Sel refine_bin(Topo& topo, Shared& s, const Src& sl, const RowCtx& r,
         // Gather the tokens of the current range (a level-1 bin, or a key interval).
         topo.sync();  // nobody still reads my candidate list, published counts or shares
         if (threadIdx.x == 0) s.ncand = 0;
-        __syncthreads();
+        cta_sync();
         uint32_t lcnt = 0, lmin = 0xFFFFFFFFu, lmax = 0;
         const uint32_t lo = klo, hi = khi;
         sl.for_each(s, [&](float z, int32_t i) {
@@ -584,7 +617,7 @@ __device__ Sel refine_bin(Topo& topo, Shared& s, const Src& sl, const RowCtx& r,
                 s.bu[6] = gmx;
             }
         }
-        __syncthreads();
+        cta_sync();
         const uint64_t total = s.bu[4];
         const uint32_t gmin = s.bu[5], gmax = s.bu[6];
         if (total == 0) {  // cannot happen for a bin chosen as non-empty; keep a valid answer
@@ -618,7 +651,7 @@ __device__ Sel refine_bin(Topo& topo, Shared& s, const Src& sl, const RowCtx& r,
             s.hcnt[b] = 0;
             s.hmass[b] = 0;
         }
-        __syncthreads();
+        cta_sync();
         const uint32_t lo2 = klo, hi2 = khi;
         sl.for_each(s, [&](float z, int32_t) {
             if (!(z > zc)) return;
@@ -868,12 +901,12 @@ __device__ __forceinline__ RowResult resolve_candidates(Shared& s, const RowCtx&
                 s.bu[6] = (uint32_t)wr.token;
             }
         }
-        __syncthreads();
+        cta_sync();
         out.key_cut = s.bu[4];
         out.nk = s.bu[5];
         out.zk = s.b64[0];
         out.token = (int32_t)s.bu[6];
-        __syncthreads();
+        cta_sync();
         return out;
     }
     block_sort_desc(s, (int)n);
@@ -914,18 +947,18 @@ __device__ __forceinline__ RowResult resolve_candidates(Shared& s, const RowCtx&
     float m32 = k32;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m32 = fmaxf(m32, __shfl_xor_sync(0xFFFFFFFFu, m32, o));
-    __syncthreads();
+    cta_sync();
     if (lane == 0) s.rf[tid >> 5] = m32;
-    __syncthreads();
+    cta_sync();
     m32 = s.rf[0];
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) m32 = fmaxf(m32, s.rf[w]);
     const float tol = race_tol(dist(r, key_to_float(out.key_cut)));
     const bool fin = tid < (int)out.nk && k32 >= m32 - tol;
-    const int nfin = __syncthreads_count(fin);
+    const int nfin = cta_sync_count(fin);
     if (nfin == 1) {
         if (fin) s.bu[6] = (uint32_t)idx;
-        __syncthreads();
+        cta_sync();
         out.token = (int32_t)s.bu[6];
     } else {
         ArgBest mine;
@@ -937,7 +970,7 @@ __device__ __forceinline__ RowResult resolve_candidates(Shared& s, const RowCtx&
         }
         out.token = block_argbest(mine, s).idx;
     }
-    __syncthreads();
+    cta_sync();
     return out;
 }
 
@@ -968,7 +1001,7 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
     const uint32_t C = topo.C;
     topo.sync();  // nobody still reads the caller's lists or published values
     if (tid == 0) s.ncand = 0;
-    __syncthreads();
+    cta_sync();
     uint32_t my_minkey = 0xFFFFFFFFu;
     uint32_t my_surv = 0;
     src.for_each(s, [&](float z, int32_t i) {
@@ -991,7 +1024,7 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
         s.ra[tid >> 5] = my_surv;
         s.rb[tid >> 5] = my_minkey;
     }
-    __syncthreads();
+    cta_sync();
     if (tid == 0) {
         uint32_t ns = 0, mk = 0xFFFFFFFFu;
 #pragma unroll
@@ -1017,7 +1050,7 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
             s.bu[3] = mk;
         }
     }
-    __syncthreads();
+    cta_sync();
     const uint64_t NS0 = s.bu[2];
     RowResult res;
     res.key_cut = s.bu[3];
@@ -1057,7 +1090,7 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
             s.hcnt[b] = 0;
             s.hmass[b] = 0;
         }
-        __syncthreads();
+        cta_sync();
         auto build_hist = [&](uint32_t key_floor) {
             src.for_each(s, [&](float z, int32_t) {
                 if (!(z > zc)) return;
@@ -1097,7 +1130,7 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
                     s.hcnt[b] = 0;
                     s.hmass[b] = 0;
                 }
-                __syncthreads();
+                cta_sync();
                 build_hist(res.key_cut);
                 cluster_reduce_hist(topo, s, kBins);
             }
@@ -1134,13 +1167,13 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
         t2.add(race_key32(dist(r, z), race_u(rc, i)), i);
     });
     t2 = warp_top2(t2);
-    __syncthreads();
+    cta_sync();
     if (lane == 0) {
         s.rab[tid >> 5].key = (double)t2.k1;
         s.rab[tid >> 5].idx = t2.i1;
         s.rf[tid >> 5] = t2.k2;
     }
-    __syncthreads();
+    cta_sync();
     if (tid == 0) {
         Top2 b;
         b.init();
@@ -1171,7 +1204,7 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
             s.bu[6] = (uint32_t)x.i1;
         }
     }
-    __syncthreads();
+    cta_sync();
     const float M1 = s.bf[1], M2 = s.bf[0];
     res.token = (int32_t)s.bu[6];
     if (!(M1 - M2 > tol)) {
@@ -1208,10 +1241,10 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
             x = warp_argbest(x);
             if (lane == 0) s.bu[6] = (uint32_t)x.idx;
         }
-        __syncthreads();
+        cta_sync();
         res.token = (int32_t)s.bu[6];
     }
-    __syncthreads();
+    cta_sync();
     return res;
 }
 
