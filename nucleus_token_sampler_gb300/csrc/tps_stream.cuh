@@ -21,6 +21,7 @@ namespace tps {
 
 constexpr int kMaxStages = 8;
 constexpr int kStreamThreads = kThreads + 32;  // consumer warps + one producer warp
+constexpr int kStreamList = 2048;              // candidate list of one streamed row
 
 struct StreamState {
     uint64_t full[kMaxStages];   // stage holds its chunk (arrive + transaction bytes)
@@ -30,6 +31,9 @@ struct StreamState {
     uint32_t dead;               // a bounded wait gave up: streaming stops
     uint32_t producer_done;      // the producer has left its loop
     uint32_t issued_lo;          // chunks issued (low 32 bits), valid once producer_done is set
+    uint32_t lcount;             // tokens listed for the current row (may exceed kStreamList)
+    uint32_t lkey[kStreamList];  // listed tokens: logit key and index
+    uint32_t lidx[kStreamList];
 };
 
 // Geometry of one row: aligned interior in 16-byte vectors plus a ragged head and tail.
@@ -94,7 +98,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
         st.producer_done = 0;
         st.issued_lo = 0;
         st.runkey = key_neg_inf;
-        s.ncand = 0;
+        st.lcount = 0;
     }
     __syncthreads();  // the only barrier the producer warp joins
 
@@ -164,10 +168,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
         }
 
         auto list_token = [&](float z, int32_t i) {
-            const uint32_t slot = atomicAdd(&s.ncand, 1u);
-            if (slot < (uint32_t)kCand) {
-                s.ckey[slot] = fkey(z);
-                s.cidx[slot] = (uint32_t)i;
+            const uint32_t slot = atomicAdd(&st.lcount, 1u);
+            if (slot < (uint32_t)kStreamList) {
+                st.lkey[slot] = fkey(z);
+                st.lidx[slot] = (uint32_t)i;
             }
         };
         auto nolist = [](float, int32_t) {};
@@ -240,7 +244,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
         src.elem0 = geo.nhead;
 
         cta_sync();  // the list and the ragged elements are complete
-        const uint32_t nlisted = s.ncand;
+        const uint32_t nlisted = st.lcount;
         RowResult res;
         res.token = -1;
         if (status != kRowOk) {
@@ -268,20 +272,23 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
             rc.row = (uint32_t)row;
             rc.s_lo = (uint32_t)a.step;
             rc.s_hi = (uint32_t)(a.step >> 32);
-            if (listing && nlisted <= (uint32_t)kCand) {
-                // every survivor is on the list: filter it exactly against the true maximum
-                cta_sync();
+            // every survivor is on the list: filter it exactly against the true maximum
+            bool fast = listing && nlisted <= (uint32_t)kStreamList;
+            if (fast) {
                 if (tid == 0) s.ncand = 0;
                 cta_sync();
-                if ((uint32_t)tid < nlisted) {
-                    const uint32_t key = s.ckey[tid];
+                for (uint32_t t = tid; t < nlisted; t += kThreads) {
+                    const uint32_t key = st.lkey[t];
                     const float z = key_to_float(key);
                     if (z > zc && minp_ok(r, z, dist(r, z))) {
                         const uint32_t slot = atomicAdd(&s.ncand, 1u);
-                        s.u.cd.sbuf[slot] = sb_make(key, s.cidx[tid]);
+                        if (slot < (uint32_t)kCand) s.u.cd.sbuf[slot] = sb_make(key, st.lidx[t]);
                     }
                 }
                 cta_sync();
+                fast = s.ncand <= (uint32_t)kCand;
+            }
+            if (fast) {
                 res = resolve_candidates(s, r, rc, s.ncand, topk_on, K, P);
                 if (prow) write_probs(src, s, r, res.key_cut, res.zk, prow);
             } else {
@@ -292,7 +299,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
         }
         cta_sync();  // everyone is done with the row's shared state
         if (tid == 0) {
-            s.ncand = 0;
+            st.lcount = 0;
             st.runkey = key_neg_inf;
         }
         cta_sync();
