@@ -79,7 +79,7 @@ struct Shared {
     // --- histogram: local, then (after the cluster reduction) the full reduced histogram
     uint32_t hcnt[kBins];
     uint64_t hmass[kBins];
-    union {
+    union alignas(16) {
         struct {  // this CTA's share of the reduced histogram (read by the other CTAs)
             uint32_t rcnt[kBins];
             uint64_t rmass[kBins];
@@ -429,28 +429,30 @@ __device__ __forceinline__ void scan_bins(Shared& s, int nb, const Crit& cr, uin
     cta_sync();
 }
 
-// Sort u.cd.sbuf[0, n) descending (bitonic, padded with zeros to a power of two).
+// Sort u.cd.sbuf[0, n) (n <= kThreads, distinct values) descending: thread t counts the entries
+// larger than its own (broadcast reads, two at a time) and scatters it to that rank.  Two barriers
+// instead of a bitonic network's log^2 n.
 __device__ __forceinline__ void block_sort_desc(Shared& s, int n)
 {
     uint64_t* sb = s.u.cd.sbuf;
-    int np = 2;
-    while (np < n) np <<= 1;
-    for (int i = n + (int)threadIdx.x; i < np; i += kThreads) sb[i] = 0;
-    cta_sync();
-    for (int k2 = 2; k2 <= np; k2 <<= 1) {
-        for (int j = k2 >> 1; j > 0; j >>= 1) {
-            for (int i = threadIdx.x; i < (np >> 1); i += kThreads) {
-                const int lo = 2 * j * (i / j) + (i % j), hi = lo + j;
-                const bool desc = (lo & k2) == 0;
-                const uint64_t x = sb[lo], y = sb[hi];
-                if (desc ? (x < y) : (x > y)) {
-                    sb[lo] = y;
-                    sb[hi] = x;
-                }
-            }
-            cta_sync();
+    uint64_t* tmp = s.u.cd.pre;  // kCand + 1 entries of scratch
+    const int t = threadIdx.x;
+    uint64_t v = 0;
+    int rank = 0;
+    if (t < n) {
+        v = sb[t];
+        int j = 0;
+        for (; j + 1 < n; j += 2) {
+            const ulonglong2 w = *reinterpret_cast<const ulonglong2*>(sb + j);
+            rank += (w.x > v) + (w.y > v);
         }
+        if (j < n) rank += (sb[j] > v);
     }
+    cta_sync();
+    if (t < n) tmp[rank] = v;
+    cta_sync();
+    if (t < n) sb[t] = tmp[t];
+    cta_sync();
 }
 
 __device__ __forceinline__ uint32_t sb_key(uint64_t v) { return (uint32_t)(v >> 32); }
