@@ -699,13 +699,13 @@ struct WarpResult {
     int32_t token;
 };
 
-// Resolve a row whose survivors are u.cd.sbuf[0, n) (n <= 32, unsorted) with one warp.  Every
-// lane returns the same result.
-__device__ __forceinline__ WarpResult warp_resolve(const Shared& s, const RowCtx& r, const RaceCtx& rc, uint32_t n,
+// Resolve a row whose survivors are buf[0, n) (n <= 32, unsorted) with one warp.  Every lane
+// returns the same result.
+__device__ __forceinline__ WarpResult warp_resolve(const uint64_t* buf, const RowCtx& r, const RaceCtx& rc, uint32_t n,
                                                    bool topk_on, int32_t K, float P)
 {
     const uint32_t lane = threadIdx.x & 31;
-    uint64_t v = (lane < n) ? s.u.cd.sbuf[lane] : 0;
+    uint64_t v = (lane < n) ? buf[lane] : 0;
     // bitonic sort across the warp, descending
 #pragma unroll
     for (int k2 = 2; k2 <= 32; k2 <<= 1) {
@@ -785,6 +785,152 @@ __device__ __forceinline__ WarpResult warp_resolve(const Shared& s, const RowCtx
         if (fin) {
             a.key = race_key64(r, z, u);
             a.idx = idx;
+        }
+        token = warp_argbest(a).idx;
+    }
+    WarpResult res;
+    res.key_cut = key_cut;
+    res.nk = nk;
+    res.zk = zk;
+    res.token = token;
+    return res;
+}
+
+// Resolve a row whose survivors are buf[0, n) (32 < n <= 256, distinct, any order) with one warp:
+// rank sort into sorted[], fixed-point mass prefixes in pre[0, n], the top-k and top-p class cuts,
+// then the race.  Lane l owns sorted positions [8 l, 8 l + 8).  Every lane returns the same result.
+__device__ __forceinline__ WarpResult warp_resolve_big(const uint64_t* buf, uint64_t* sorted, uint64_t* pre, uint32_t n,
+                                                       const RowCtx& r, const RaceCtx& rc, bool topk_on, int32_t K,
+                                                       float P)
+{
+    const uint32_t lane = threadIdx.x & 31;
+    // rank sort: every entry counts the entries larger than itself
+#pragma unroll 1
+    for (uint32_t e = lane; e < n; e += 32) {
+        const uint64_t v = buf[e];
+        uint32_t rank = 0, j = 0;
+        for (; j + 1 < n; j += 2) {
+            const ulonglong2 w = *reinterpret_cast<const ulonglong2*>(buf + j);
+            rank += (w.x > v) + (w.y > v);
+        }
+        if (j < n) rank += (buf[j] > v);
+        sorted[rank] = v;
+    }
+    __syncwarp();
+    const uint32_t p0 = 8 * lane;
+    uint64_t q[8];
+    uint32_t kk[8];
+    uint64_t loc = 0;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const uint32_t pos = p0 + m;
+        kk[m] = (pos < n) ? sb_key(sorted[pos]) : 0u;
+        q[m] = (pos < n) ? qmass_d(dist(r, key_to_float(kk[m]))) : 0;
+        loc += q[m];
+    }
+    uint64_t inc = loc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if ((int)lane >= o) inc += y;
+    }
+    uint64_t run = inc - loc;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        if (p0 + m < n) pre[p0 + m] = run;
+        run += q[m];
+    }
+    if (lane == 31) pre[n] = inc;
+    __syncwarp();
+    const uint32_t prevk = __shfl_up_sync(0xFFFFFFFFu, kk[7], 1);
+    bool start[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const uint32_t pos = p0 + m;
+        const uint32_t before = (m == 0) ? prevk : kk[m - 1];
+        start[m] = (pos < n) && (pos == 0 || before != kk[m]);
+    }
+    // last class start in [0, lim) satisfying the criterion, and the end of that class
+    auto cut = [&](uint32_t lim, bool by_mass, uint64_t tcnt, double tmass, uint32_t* st_out, uint32_t* e_out) {
+        uint32_t best = 0;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const uint32_t pos = p0 + m;
+            if (start[m] && pos < lim && (by_mass ? ((double)pre[pos] < tmass) : ((uint64_t)pos < tcnt)))
+                best = pos + 1;
+        }
+        const uint32_t st = __reduce_max_sync(0xFFFFFFFFu, best);
+        const uint32_t s0 = st ? st - 1 : 0;
+        uint32_t end = lim;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const uint32_t pos = p0 + m;
+            if (start[m] && pos < lim && pos > s0) end = min(end, pos);
+        }
+        *st_out = s0;
+        *e_out = __reduce_min_sync(0xFFFFFFFFu, end);
+    };
+    uint32_t ns = n;
+    uint64_t zs = pre[n];
+    if (topk_on && n > (uint32_t)K) {
+        uint32_t st, e;
+        cut(n, false, (uint64_t)K, 0.0, &st, &e);
+        ns = e;
+        zs = pre[e];
+    }
+    uint32_t nk = ns;
+    uint64_t zk = zs;
+    if (P < 1.f) {
+        uint32_t st, e;
+        cut(ns, P > 0.f, 1, (double)P * (double)zs, &st, &e);
+        nk = e;
+        zk = pre[e];
+    }
+    const uint32_t key_cut = sb_key(sorted[nk - 1]);
+    // race over positions < nk
+    float k32[8], uu[8];
+    float m32 = -INFINITY;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const uint32_t pos = p0 + m;
+        k32[m] = -INFINITY;
+        uu[m] = 0.f;
+        if (pos < nk) {
+            uu[m] = race_u(rc, sb_idx(sorted[pos]));
+            k32[m] = race_key32(dist(r, key_to_float(kk[m])), uu[m]);
+            m32 = fmaxf(m32, k32[m]);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m32 = fmaxf(m32, __shfl_xor_sync(0xFFFFFFFFu, m32, o));
+    const float tol = race_tol(dist(r, key_to_float(key_cut)));
+    uint32_t nf = 0, fpos = 0;
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+        if (p0 + m < nk && k32[m] >= m32 - tol) {
+            ++nf;
+            fpos = p0 + m;
+        }
+    const uint32_t nfin = __reduce_add_sync(0xFFFFFFFFu, nf);
+    int32_t token;
+    if (nfin == 1) {
+        const uint32_t who = __ballot_sync(0xFFFFFFFFu, nf != 0);
+        token = sb_idx(sorted[__shfl_sync(0xFFFFFFFFu, fpos, __ffs(who) - 1)]);
+    } else {
+        ArgBest a;
+        a.key = -INFINITY;
+        a.idx = 0x7FFFFFFF;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const uint32_t pos = p0 + m;
+            if (pos < nk && k32[m] >= m32 - tol) {
+                const double k64 = race_key64(r, key_to_float(kk[m]), uu[m]);
+                const int32_t i = sb_idx(sorted[pos]);
+                if (better(k64, i, a.key, a.idx)) {
+                    a.key = k64;
+                    a.idx = i;
+                }
+            }
         }
         token = warp_argbest(a).idx;
     }
@@ -895,7 +1041,7 @@ __device__ __forceinline__ RowResult resolve_candidates(Shared& s, const RowCtx&
     RowResult out;
     if (n <= 32) {
         if (tid < 32) {
-            const WarpResult wr = warp_resolve(s, r, rc, n, topk_on, K, P);
+            const WarpResult wr = warp_resolve(s.u.cd.sbuf, r, rc, n, topk_on, K, P);
             if (lane == 0) {
                 s.bu[4] = wr.key_cut;
                 s.bu[5] = wr.nk;

@@ -1,18 +1,22 @@
 // tps_stream.cuh -- the streaming sampler: one persistent CTA per SM, whole rows streamed through a
 // ring of bulk-copied chunks.  Used when the batch has enough rows to fill the GPU.
 //
-// Warp-specialised pipeline.  One producer warp keeps the ring full: as soon as a stage is released
-// it bulk-copies the next 64 KB chunk of the CTA's next row into it (`cp.async.bulk` into this
-// CTA's shared memory, completed on the stage's "full" mbarrier).  Eight consumer warps scan the
-// chunks and release each stage through its "empty" mbarrier -- no CTA-wide barrier per chunk, so
-// the HBM stream never waits for the arithmetic.  While a row streams, every warp keeps its
-// running maximum (also pooled across warps through an atomic maximum) and lists every token that
-// min-p, measured against that running maximum, does not already reject; the running maximum only
-// grows, so the list is a superset of the row's survivors.  At the end of the row the consumer
-// warps meet once, filter the list exactly against the true maximum and resolve the row (top-k,
-// top-p, race) while the producer already streams the next row.  Rows without min-p, or whose list
-// overflows, take the general path, which re-reads the row from global memory (it was just
-// streamed, so mostly from L2).
+// Three kinds of warps, so that neither the HBM stream nor the scan ever waits for a row's
+// resolution:
+//   * one producer warp keeps a 3 x 64 KB ring full: as soon as a stage is released it bulk-copies
+//     the next chunk of the CTA's next row into it (`cp.async.bulk` into this CTA's shared memory,
+//     completed on the stage's "full" mbarrier);
+//   * eight scanner warps read the chunks and release each stage through its "empty" mbarrier.
+//     While a row streams, each warp keeps its running maximum (pooled across warps through an
+//     atomic maximum) and lists every token that min-p, measured against that running maximum,
+//     does not already reject -- a superset of the row's survivors, since the maximum only grows.
+//     At the end of the row they hand the list and their maxima over in one of two row slots and
+//     go straight on to the next row;
+//   * one resolver warp takes each finished slot: the exact maximum, the exact min-p filter of the
+//     list, the top-k and top-p cuts and the race, then frees the slot.
+// Rows the resolver cannot finish alone (no min-p, an overflowing list, more than 256 survivors,
+// or a probability row to write) are queued back to the scanners, which take them between rows
+// with the block-wide general path over the row in global memory (just streamed, so mostly L2).
 #pragma once
 
 #include "tps_common.cuh"
@@ -20,20 +24,48 @@
 namespace tps {
 
 constexpr int kMaxStages = 8;
-constexpr int kStreamThreads = kThreads + 32;  // consumer warps + one producer warp
-constexpr int kStreamList = 2048;              // candidate list of one streamed row
+constexpr int kStreamThreads = kThreads + 64;  // scanner warps + resolver warp + producer warp
+constexpr int kResolverWarp = kWarps;
+constexpr int kProducerWarp = kWarps + 1;
+constexpr int kSlotList = 1024;                // candidate list of one row slot
+constexpr int kTaskQueue = 16;                 // rows handed back to the scanners
+
+// One row handed from the scanners to the resolver.
+struct RowSlot {
+    uint32_t lcount;             // tokens listed (may exceed kSlotList)
+    uint32_t runkey;             // order-preserving key of the pooled running maximum
+    float wmax[kWarps];          // per-scanner-warp maxima (NaN-propagating)
+    uint32_t lkey[kSlotList];    // listed tokens: logit key and index
+    uint32_t lidx[kSlotList];
+};
+
+// Work the resolver hands back to the scanners.
+enum TaskKind : uint32_t { kTaskGeneral = 1, kTaskGreedy = 2, kTaskProbs = 3, kTaskZero = 4 };
+struct Task {
+    uint32_t kind;
+    uint32_t key_cut;
+    int64_t row;
+    uint64_t zk;
+    float zmax;
+};
 
 struct StreamState {
     uint64_t full[kMaxStages];   // stage holds its chunk (arrive + transaction bytes)
-    uint64_t empty[kMaxStages];  // every consumer warp is done with the stage
-    float wmax[kWarps];          // per-warp maxima of the row (NaN-propagating)
-    uint32_t runkey;             // order-preserving key of the pooled running maximum
+    uint64_t empty[kMaxStages];  // every scanner warp is done with the stage
+    uint64_t slot_full[2];       // every scanner warp has handed the slot over
+    uint64_t slot_free[2];       // the resolver is done with the slot
     uint32_t dead;               // a bounded wait gave up: streaming stops
     uint32_t producer_done;      // the producer has left its loop
     uint32_t issued_lo;          // chunks issued (low 32 bits), valid once producer_done is set
-    uint32_t lcount;             // tokens listed for the current row (may exceed kStreamList)
-    uint32_t lkey[kStreamList];  // listed tokens: logit key and index
-    uint32_t lidx[kStreamList];
+    uint32_t resolver_done;      // the resolver has finished every row of this CTA
+    uint32_t q_head, q_tail;     // task queue (the resolver pushes, the scanners pop)
+    uint32_t q_seen;             // scanners: a value broadcast by thread 0
+    Task q[kTaskQueue];
+    // resolver scratch (one warp): survivors, sorted survivors, mass prefixes
+    alignas(16) uint64_t rbuf[kCand];
+    uint64_t rsorted[kCand];
+    uint64_t rpre[kCand + 1];
+    RowSlot slot[2];
 };
 
 // Geometry of one row: aligned interior in 16-byte vectors plus a ragged head and tail.
@@ -72,6 +104,104 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// The largest float below m (m finite).
+__device__ __forceinline__ float next_down(float m)
+{
+    if (m == 0.f) return -__uint_as_float(1u);
+    const uint32_t b = __float_as_uint(m);
+    return __uint_as_float(m > 0.f ? b - 1u : b + 1u);
+}
+
+struct RowParams {
+    float T, P, MP;
+    int32_t K;
+    uint64_t seed;
+};
+
+__device__ __forceinline__ RowParams load_params(const Args& a, int64_t row)
+{
+    RowParams p;
+    p.T = a.temperature[row];
+    p.P = a.top_p[row];
+    p.MP = a.min_p[row];
+    p.K = a.top_k[row];
+    p.seed = a.seed[row];
+    return p;
+}
+
+__device__ __forceinline__ bool params_ok(const RowParams& p)
+{
+    return isfinite(p.T) && isfinite(p.P) && isfinite(p.MP);
+}
+
+__device__ __forceinline__ float clamp_minp(float MP) { return (MP > 0.f) ? fminf(MP, 1.f) : 0.f; }
+
+__device__ __forceinline__ RaceCtx race_ctx(const Args& a, int64_t row, uint64_t seed)
+{
+    RaceCtx rc;
+    rc.k0 = (uint32_t)seed;
+    rc.k1 = (uint32_t)(seed >> 32);
+    rc.row = (uint32_t)row;
+    rc.s_lo = (uint32_t)a.step;
+    rc.s_hi = (uint32_t)(a.step >> 32);
+    return rc;
+}
+
+// The scanners' block-wide handling of one queued row (all kThreads scanner threads call it).
+template <typename TIn>
+__device__ void run_task(const Args& a, Shared& s, const Task& t, uint32_t chunk_bytes)
+{
+    constexpr int ES = Elem<TIn>::kBytes;
+    const int tid = threadIdx.x;
+    const int64_t row = t.row;
+    const RowGeom geo = row_geom<ES>(a, row, chunk_bytes);
+    const int nx = geo.nhead + geo.ntail;
+    cta_sync();  // the previous user of s.xz / s.nx is done
+    if (tid < nx) {
+        const int32_t xi = (tid < geo.nhead) ? tid : (int32_t)(a.V - geo.ntail + (tid - geo.nhead));
+        s.xz[tid] = Elem<TIn>::load1(geo.rowp, xi);
+        s.xi[tid] = xi;
+    }
+    if (tid == 0) s.nx = nx;
+    cta_sync();
+    GlobalRow<TIn> src;
+    src.vec = reinterpret_cast<const uint4*>(geo.a0);
+    src.nvec = (int)geo.n16;
+    src.elem0 = geo.nhead;
+    float* prow = a.out_probs ? a.out_probs + row * a.V : nullptr;
+    const RowParams p = load_params(a, row);
+    if (t.kind == kTaskZero) {
+        for (int64_t i = tid; i < a.V; i += kThreads) prow[i] = 0.f;
+        return;
+    }
+    if (t.kind == kTaskGreedy) {
+        // greedy: lowest index of the maximum ("Implement batched top-p sampling with temperature",
+        // 'A strong answer': temperature 0 means greedy, ties to the lowest index)
+        uint32_t mi = 0xFFFFFFFFu;
+        const float zmax = t.zmax;
+        src.for_each(s, [&](float z, int32_t i) {
+            if (z == zmax) mi = min(mi, (uint32_t)i);
+        });
+        mi = block_min_u32(mi, s);
+        if (prow)
+            for (int64_t i = tid; i < a.V; i += kThreads) prow[i] = ((uint32_t)i == mi) ? 1.f : 0.f;
+        if (tid == 0) write_row(a, row, (int32_t)mi, kRowOk, zmax, 1);
+        return;
+    }
+    const float minp = clamp_minp(p.MP);
+    const RowCtx r = make_ctx(t.zmax, p.T, minp);
+    if (t.kind == kTaskProbs) {
+        write_probs(src, s, r, t.key_cut, t.zk, prow);
+        return;
+    }
+    // kTaskGeneral
+    const float zc = minp_threshold(r);
+    const bool topk_on = (p.K > 0) && ((int64_t)p.K < a.V);
+    SoloTopo topo;
+    const RowResult res = general_path(topo, s, src, r, zc, topk_on, p.K, p.P, race_ctx(a, row, p.seed), prow);
+    if (tid == 0) write_row(a, row, res.token, kRowOk, key_to_float(res.key_cut), (int32_t)res.nk);
+}
+
 template <typename TIn>
 __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Args a, int nstage, uint32_t chunk_bytes)
 {
@@ -94,16 +224,22 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
             mbar_init(&st.full[i], 1);
             mbar_init(&st.empty[i], kWarps);
         }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&st.slot_full[i], kWarps);
+            mbar_init(&st.slot_free[i], 1);
+            st.slot[i].lcount = 0;
+            st.slot[i].runkey = key_neg_inf;
+        }
         st.dead = 0;
         st.producer_done = 0;
         st.issued_lo = 0;
-        st.runkey = key_neg_inf;
-        st.lcount = 0;
+        st.resolver_done = 0;
+        st.q_head = st.q_tail = 0;
     }
-    __syncthreads();  // the only barrier the producer warp joins
+    __syncthreads();  // the only CTA-wide barrier
 
     // ================= producer warp =================
-    if (warp == kWarps) {
+    if (warp == kProducerWarp) {
         if (lane == 0) {
             uint64_t g = 0;
             for (int64_t row = first; row < B && !*vdead; row += stride) {
@@ -130,35 +266,176 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
         return;
     }
 
-    // ================= consumer warps =================
-    uint64_t g = 0;  // chunks consumed, in the producer's order
-    auto load_params = [&](int64_t row, float& T, float& P, float& MP, int32_t& K, uint64_t& seed) {
-        if (row < B) {
-            T = a.temperature[row];
-            P = a.top_p[row];
-            MP = a.min_p[row];
-            K = a.top_k[row];
-            seed = a.seed[row];
+    // ================= resolver warp =================
+    if (warp == kResolverWarp) {
+        auto push = [&](const Task& t) {  // lane 0 only; waits (bounded) for queue space
+            const uint64_t t0 = globaltimer_ns();
+            while (*(volatile uint32_t*)&st.q_tail - *(volatile uint32_t*)&st.q_head >= (uint32_t)kTaskQueue) {
+                if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                    *vdead = 1u;
+                    return;
+                }
+                __nanosleep(200);
+            }
+            const uint32_t tail = *(volatile uint32_t*)&st.q_tail;
+            st.q[tail % kTaskQueue] = t;
+            __threadfence_block();
+            *(volatile uint32_t*)&st.q_tail = tail + 1;
+        };
+        int64_t j = 0;
+        for (int64_t row = first; row < B; row += stride, ++j) {
+            const int sl = (int)(j & 1);
+            RowSlot& slot = st.slot[sl];
+            bool ok = mbar_wait_bounded(&st.slot_full[sl], (uint32_t)((j >> 1) & 1), kWaitLimitNs);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) *vdead = 1u;
+            float zmax = slot.wmax[0];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) zmax = fmax_nan(zmax, slot.wmax[w]);
+            const RowParams p = load_params(a, row);
+            const uint32_t nlisted = slot.lcount;
+            int32_t status = kRowOk;
+            if (!ok || *vdead) status = kRowTimeout;
+            else if (isnan(zmax) || zmax == INFINITY) status = kRowNan;
+            else if (!params_ok(p)) status = kRowBadParam;
+            else if (zmax == -INFINITY) status = kRowAllMasked;
+            Task t;
+            t.row = row;
+            t.zmax = zmax;
+            t.key_cut = 0;
+            t.zk = 0;
+            t.kind = 0;
+            if (status != kRowOk) {
+                if (lane == 0) write_row(a, row, -1, status, __uint_as_float(0x7FC00000u), 0);
+                if (a.out_probs) t.kind = kTaskZero;
+            } else if (p.T <= 0.f) {
+                // greedy: the lowest listed index holding the maximum (the list holds every token
+                // that reached the running maximum), unless the list overflowed
+                if (nlisted <= (uint32_t)kSlotList && !a.out_probs) {
+                    uint32_t mi = 0xFFFFFFFFu;
+                    for (uint32_t e = lane; e < nlisted; e += 32)
+                        if (key_to_float(slot.lkey[e]) == zmax) mi = min(mi, slot.lidx[e]);
+                    mi = __reduce_min_sync(0xFFFFFFFFu, mi);
+                    if (lane == 0) write_row(a, row, (int32_t)mi, kRowOk, zmax, 1);
+                } else {
+                    t.kind = kTaskGreedy;  // a pass over the row (also writes the one-hot row)
+                }
+            } else {
+                const float minp = clamp_minp(p.MP);
+                const RowCtx r = make_ctx(zmax, p.T, minp);
+                const float zc = minp_threshold(r);
+                const bool topk_on = (p.K > 0) && ((int64_t)p.K < a.V);
+                bool fast = minp > 0.f && nlisted <= (uint32_t)kSlotList;
+                uint32_t n = 0;
+                if (fast) {
+                    // exact min-p filter of the list against the true maximum (ballot compaction)
+                    for (uint32_t e0 = 0; e0 < nlisted; e0 += 32) {
+                        const uint32_t e = e0 + lane;
+                        bool keep = false;
+                        uint32_t key = 0, idx = 0;
+                        if (e < nlisted) {
+                            key = slot.lkey[e];
+                            idx = slot.lidx[e];
+                            const float z = key_to_float(key);
+                            keep = z > zc && minp_ok(r, z, dist(r, z));
+                        }
+                        const uint32_t m = __ballot_sync(0xFFFFFFFFu, keep);
+                        const uint32_t at = n + __popc(m & ((1u << lane) - 1u));
+                        if (keep && at < (uint32_t)kCand) st.rbuf[at] = sb_make(key, idx);
+                        n += __popc(m);
+                    }
+                    __syncwarp();
+                    fast = n <= (uint32_t)kCand;
+                }
+                if (fast) {
+                    const RaceCtx rc = race_ctx(a, row, p.seed);
+                    const WarpResult wr = (n <= 32) ? warp_resolve(st.rbuf, r, rc, n, topk_on, p.K, p.P)
+                                                    : warp_resolve_big(st.rbuf, st.rsorted, st.rpre, n, r, rc, topk_on,
+                                                                       p.K, p.P);
+                    if (lane == 0) write_row(a, row, wr.token, kRowOk, key_to_float(wr.key_cut), (int32_t)wr.nk);
+                    if (a.out_probs) {
+                        t.kind = kTaskProbs;
+                        t.key_cut = wr.key_cut;
+                        t.zk = wr.zk;
+                    }
+                } else {
+                    t.kind = kTaskGeneral;
+                }
+            }
+            // hand back what needs the scanners, then free the slot for row j + 2
+            __syncwarp();
+            if (lane == 0) {
+                if (t.kind) push(t);
+                slot.lcount = 0;
+                slot.runkey = key_neg_inf;
+                __threadfence_block();
+                mbar_arrive(&st.slot_free[sl]);
+            }
+            __syncwarp();
+        }
+        if (lane == 0) {
+            __threadfence_block();
+            *(volatile uint32_t*)&st.resolver_done = 1u;
+        }
+        return;
+    }
+
+    // ================= scanner warps =================
+    // Take every queued row (all scanner threads together) until the queue is seen empty.
+    auto drain = [&]() {
+        for (;;) {
+            if (tid == 0) st.q_seen = *(volatile uint32_t*)&st.q_tail;
+            cta_sync();
+            const uint32_t tail = st.q_seen, head = st.q_head;
+            cta_sync();
+            if (tail == head) break;
+            for (uint32_t h = head; h != tail; ++h) {
+                const Task t = st.q[h % kTaskQueue];
+                run_task<TIn>(a, s, t, chunk_bytes);
+                cta_sync();
+            }
+            if (tid == 0) *(volatile uint32_t*)&st.q_head = tail;
         }
     };
-    float nT = 0.f, nP = 0.f, nMP = 0.f;
-    int32_t nK = 0;
-    uint64_t nSeed = 0;
-    load_params(first, nT, nP, nMP, nK, nSeed);
 
-    for (int64_t row = first; row < B; row += stride) {
-        const float T = nT, P = nP, MP = nMP;
-        const int32_t K = nK;
-        const uint64_t seed = nSeed;
-        load_params(row + stride, nT, nP, nMP, nK, nSeed);  // prefetched one row ahead
+    uint64_t g = 0;  // chunks consumed, in the producer's order
+    RowParams nxt = load_params(a, first);
+    int64_t j = 0;
+    for (int64_t row = first; row < B; row += stride, ++j) {
+        const RowParams p = nxt;
+        if (row + stride < B) nxt = load_params(a, row + stride);  // prefetched one row ahead
+        drain();
+        const int sl = (int)(j & 1);
+        RowSlot& slot = st.slot[sl];
+        bool dead = *vdead != 0;
+        if (j >= 2 && !dead && !mbar_wait_bounded(&st.slot_free[sl], (uint32_t)(((j >> 1) - 1) & 1), kWaitLimitNs)) {
+            dead = true;
+            *vdead = 1u;
+        }
         const RowGeom geo = row_geom<ES>(a, row, chunk_bytes);
-        const bool params_ok = isfinite(T) && isfinite(P) && isfinite(MP);
-        const bool sampling = params_ok && T > 0.f;
-        const float minp = (MP > 0.f) ? fminf(MP, 1.f) : 0.f;
-        const bool listing = sampling && minp > 0.f;
-        const float lt_hi = listing ? make_ctx(0.f, T, minp).L_hi * T * (1.f + 1e-5f) : 0.f;
+        const bool ok = params_ok(p);
+        const float minp = clamp_minp(p.MP);
+        // listing: min-p rows list what min-p against the running maximum cannot exclude; greedy
+        // rows list what reaches the running maximum (a superset of the final maximum's class)
+        const bool greedy = ok && p.T <= 0.f;
+        const bool listing = (ok && p.T > 0.f && minp > 0.f) || greedy;
+        const float lt_hi = (listing && !greedy) ? make_ctx(0.f, p.T, minp).L_hi * p.T * (1.f + 1e-5f) : 0.f;
+        auto thr_of = [&](float m) -> float {
+            if (!(listing && m > -INFINITY && m < INFINITY)) return INFINITY;
+            if (greedy) return next_down(m);
+            const float t = list_threshold(m, lt_hi);
+            return isnan(t) ? INFINITY : t;
+        };
+        auto list_token = [&](float z, int32_t i) {
+            const uint32_t at = atomicAdd(&slot.lcount, 1u);
+            if (at < (uint32_t)kSlotList) {
+                slot.lkey[at] = fkey(z);
+                slot.lidx[at] = (uint32_t)i;
+            }
+        };
+        auto nolist = [](float, int32_t) {};
 
-        // ragged head/tail: loads issued now, used after the last chunk
+        // ragged head/tail (warp 0 lanes): listed unconditionally, the resolver filters them
         const int nx = geo.nhead + geo.ntail;
         float xv = -INFINITY;
         int32_t xidx = 0;
@@ -167,22 +444,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
             xv = E::load1(geo.rowp, xidx);
         }
 
-        auto list_token = [&](float z, int32_t i) {
-            const uint32_t slot = atomicAdd(&st.lcount, 1u);
-            if (slot < (uint32_t)kStreamList) {
-                st.lkey[slot] = fkey(z);
-                st.lidx[slot] = (uint32_t)i;
-            }
-        };
-        auto nolist = [](float, int32_t) {};
-        auto thr_of = [&](float m) -> float {
-            if (!(listing && m > -INFINITY && m < INFINITY)) return INFINITY;
-            const float t = list_threshold(m, lt_hi);
-            return isnan(t) ? INFINITY : t;
-        };
-
         float wrun = -INFINITY;  // this warp's running maximum over the row (same in all its lanes)
-        bool dead = *vdead != 0;
         for (int c = 0; c < geo.nchunks; ++c, ++g) {
             const int stage = (int)(g % (uint64_t)nstage);
             const uint32_t parity = (uint32_t)((g / (uint64_t)nstage) & 1u);
@@ -200,115 +462,49 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
                 if (c == 0) {
                     // first chunk: this warp's own maximum over its part sets its first threshold
                     wrun = warp_max_nan(scan_max_list<TIn, false>(cv, nv, e0, INFINITY, nolist));
-                    const float mref = fmax_nan(wrun, key_to_float(*(volatile uint32_t*)&st.runkey));
+                    const float mref = fmax_nan(wrun, key_to_float(*(volatile uint32_t*)&slot.runkey));
                     if (listing) (void)scan_max_list<TIn, false>(cv, nv, e0, thr_of(mref), list_token);
                     cm = wrun;
                 } else {
-                    const float mref = fmax_nan(wrun, key_to_float(*(volatile uint32_t*)&st.runkey));
+                    const float mref = fmax_nan(wrun, key_to_float(*(volatile uint32_t*)&slot.runkey));
                     cm = warp_max_nan(scan_max_list<TIn, false>(cv, nv, e0, thr_of(mref), list_token));
                 }
                 wrun = fmax_nan(wrun, cm);
-                if (lane == 0 && !isnan(wrun)) atomicMax(&st.runkey, fkey(wrun));
+                if (lane == 0 && !isnan(wrun)) atomicMax(&slot.runkey, fkey(wrun));
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&st.empty[stage]);
         }
-
-        // ---- the ragged elements, then the row's exact maximum
-        float xm = (tid < nx) ? xv : -INFINITY;
-        xm = fmax_nan(wrun, warp_max_nan(xm));
-        if (lane == 0) st.wmax[warp] = xm;
-        if (tid < nx) {
-            s.xz[tid] = xv;
-            s.xi[tid] = xidx;
+        // hand the row over: ragged elements (listed), this warp's maximum, arrive on the slot
+        if (tid < nx) list_token(xv, xidx);
+        const float xm = warp_max_nan((tid < nx) ? xv : -INFINITY);
+        if (lane == 0) slot.wmax[warp] = dead ? __uint_as_float(0x7FC00000u) : fmax_nan(wrun, xm);
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            mbar_arrive(&st.slot_full[sl]);
         }
-        if (tid == 0) s.nx = nx;
-        const bool cta_dead = cta_sync_or(dead || *vdead) != 0;
-        float zmax = st.wmax[0];
-#pragma unroll
-        for (int w = 1; w < kWarps; ++w) zmax = fmax_nan(zmax, st.wmax[w]);
-        // the ragged elements are listed against the exact maximum (a threshold at least as low as
-        // any running one would give, so the list stays a superset of the survivors)
-        if (tid < nx && listing && xv > thr_of(zmax)) list_token(xv, xidx);
-
-        int32_t status = kRowOk;
-        if (cta_dead) status = kRowTimeout;
-        else if (isnan(zmax) || zmax == INFINITY) status = kRowNan;
-        else if (!params_ok) status = kRowBadParam;
-        else if (zmax == -INFINITY) status = kRowAllMasked;
-
-        float* prow = a.out_probs ? a.out_probs + row * a.V : nullptr;
-        GlobalRow<TIn> src;
-        src.vec = reinterpret_cast<const uint4*>(geo.a0);
-        src.nvec = (int)geo.n16;
-        src.elem0 = geo.nhead;
-
-        cta_sync();  // the list and the ragged elements are complete
-        const uint32_t nlisted = st.lcount;
-        RowResult res;
-        res.token = -1;
-        if (status != kRowOk) {
-            if (prow)
-                for (int64_t i = tid; i < a.V; i += kThreads) prow[i] = 0.f;
-            if (tid == 0) write_row(a, row, -1, status, __uint_as_float(0x7FC00000u), 0);
-        } else if (T <= 0.f) {
-            // greedy: lowest index of the maximum ("Implement batched top-p sampling with
-            // temperature", 'A strong answer': temperature 0 means greedy, ties to the lowest index)
-            uint32_t mi = 0xFFFFFFFFu;
-            src.for_each(s, [&](float z, int32_t i) {
-                if (z == zmax) mi = min(mi, (uint32_t)i);
-            });
-            mi = block_min_u32(mi, s);
-            if (prow)
-                for (int64_t i = tid; i < a.V; i += kThreads) prow[i] = ((uint32_t)i == mi) ? 1.f : 0.f;
-            if (tid == 0) write_row(a, row, (int32_t)mi, kRowOk, zmax, 1);
-        } else {
-            const RowCtx r = make_ctx(zmax, T, minp);
-            const float zc = minp_threshold(r);
-            const bool topk_on = (K > 0) && ((int64_t)K < a.V);
-            RaceCtx rc;
-            rc.k0 = (uint32_t)seed;
-            rc.k1 = (uint32_t)(seed >> 32);
-            rc.row = (uint32_t)row;
-            rc.s_lo = (uint32_t)a.step;
-            rc.s_hi = (uint32_t)(a.step >> 32);
-            // every survivor is on the list: filter it exactly against the true maximum
-            bool fast = listing && nlisted <= (uint32_t)kStreamList;
-            if (fast) {
-                if (tid == 0) s.ncand = 0;
-                cta_sync();
-                for (uint32_t t = tid; t < nlisted; t += kThreads) {
-                    const uint32_t key = st.lkey[t];
-                    const float z = key_to_float(key);
-                    if (z > zc && minp_ok(r, z, dist(r, z))) {
-                        const uint32_t slot = atomicAdd(&s.ncand, 1u);
-                        if (slot < (uint32_t)kCand) s.u.cd.sbuf[slot] = sb_make(key, st.lidx[t]);
-                    }
-                }
-                cta_sync();
-                fast = s.ncand <= (uint32_t)kCand;
-            }
-            if (fast) {
-                res = resolve_candidates(s, r, rc, s.ncand, topk_on, K, P);
-                if (prow) write_probs(src, s, r, res.key_cut, res.zk, prow);
-            } else {
-                SoloTopo topo;
-                res = general_path(topo, s, src, r, zc, topk_on, K, P, rc, prow);
-            }
-            if (tid == 0) write_row(a, row, res.token, kRowOk, key_to_float(res.key_cut), (int32_t)res.nk);
-        }
-        cta_sync();  // everyone is done with the row's shared state
-        if (tid == 0) {
-            st.lcount = 0;
-            st.runkey = key_neg_inf;
-        }
+    }
+    // keep taking queued rows until the resolver has finished every row
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        drain();
+        if (tid == 0) st.q_seen = *(volatile uint32_t*)&st.resolver_done;
         cta_sync();
+        const bool rdone = st.q_seen != 0;
+        cta_sync();
+        if (rdone) {
+            drain();
+            break;
+        }
+        if (globaltimer_ns() - t0 > 4 * kWaitLimitNs) break;  // a resolver wait has already given up
+        __nanosleep(500);
     }
 
     // After a timeout, copies still in flight must land before the shared memory is released.
     if (tid == 0 && *vdead) {
-        const uint64_t t0 = globaltimer_ns();
-        while (!*(volatile uint32_t*)&st.producer_done && globaltimer_ns() - t0 < kWaitLimitNs) {
+        const uint64_t t1 = globaltimer_ns();
+        while (!*(volatile uint32_t*)&st.producer_done && globaltimer_ns() - t1 < kWaitLimitNs) {
         }
         // the last phase issued on each stage completes only once every copy into it has landed
         const uint64_t issued = st.issued_lo;
