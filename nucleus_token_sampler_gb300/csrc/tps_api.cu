@@ -71,7 +71,11 @@ uint32_t slice_cap_bytes(int64_t V, int es, int C)
     return (uint32_t)(((per * 16) + 127) / 128 * 128);
 }
 
-size_t smem_bytes(uint32_t slice_cap) { return (size_t)slice_cap + sizeof(tps::Shared); }
+// Slice, shared state, and the cluster-wide fine histogram.
+size_t smem_bytes(uint32_t slice_cap)
+{
+    return (size_t)slice_cap + sizeof(tps::Shared) + (size_t)tps::kFineBins * sizeof(uint32_t);
+}
 
 // Choose the cluster size: the smallest C whose slice fits the preferred size, widened for small
 // batches so one row spreads over more SMs.  Returns 0 if even 16 CTAs cannot hold the row.
@@ -131,6 +135,10 @@ bool wide_cluster_ok(DeviceInfo& d, int dt, int C, size_t smem)
     if ((long)smem > known) slot.store((long)smem);
     return true;
 }
+
+constexpr size_t kSmemPerBlockMax = 232448;  // 227 KB opt-in shared memory per CTA on sm_100/sm_103
+static_assert((size_t)kStreamStages * kStreamChunk + sizeof(tps::Shared) + sizeof(tps::StreamState) <= kSmemPerBlockMax,
+              "the streaming kernel's ring and state must fit one CTA's shared memory");
 
 size_t stream_smem_bytes() { return (size_t)kStreamStages * kStreamChunk + sizeof(tps::Shared) + sizeof(tps::StreamState); }
 

@@ -32,6 +32,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
     const uint32_t rank = topo.rank;
     const int64_t row = (int64_t)(blockIdx.x / C);
     Shared& s = *reinterpret_cast<Shared*>(dsmem + a.slice_cap);
+    topo.hr = reinterpret_cast<uint32_t*>(dsmem + a.slice_cap + sizeof(Shared));  // cluster-wide fine counts
     const int tid = threadIdx.x;
     const uint32_t lane = tid & 31;
 

@@ -19,9 +19,10 @@ namespace cg = cooperative_groups;
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kBins = 256;            // level-1 bins over d, width 1/8 (last bin: d >= 31.875)
-constexpr float kBinScale = 8.f;
-constexpr int kSubBins = 256;         // sub-bins over a key interval
+constexpr int kFineBins = 1024;       // count bins over d, width 1/32 (last bin: d >= 1023/32)
+constexpr float kFineScale = 32.f;
+constexpr int kSubBins = 128;         // sub-bins over a key interval (exact refinement)
+constexpr int kMaxWin = 32;           // groups of fine bins in a top-p window
 constexpr int kCand = 256;            // candidates resolved by sorting, per CTA and per cluster
 constexpr int kMaxExtra = 16;         // ragged head/tail elements fetched with plain loads
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s bound on every wait
@@ -58,6 +59,9 @@ struct Shared {
     uint32_t pub_gkmax;
     double pub_k64;
     int32_t pub_idx;
+    uint32_t pub_ca;  // exact pass: tokens above the top-p window
+    uint64_t pub_z;   // exact pass: fixed-point mass of the survivors
+    uint64_t pub_a;   // exact pass: fixed-point mass above the top-p window
     // --- ragged elements
     int32_t nx;
     float xz[kMaxExtra];
@@ -67,6 +71,7 @@ struct Shared {
     uint32_t ra[kWarps];
     uint32_t rb[kWarps];
     uint64_t r64[kWarps];
+    double rd[kWarps];
     ArgBest rab[kWarps];
     uint32_t bu[8];
     uint64_t b64[4];
@@ -76,13 +81,20 @@ struct Shared {
     uint32_t goff[16];
     uint32_t gcnt[16];
     uint32_t gtotal;
-    // --- histogram: local, then (after the cluster reduction) the full reduced histogram
-    uint32_t hcnt[kBins];
-    uint64_t hmass[kBins];
+    // --- fine count histogram over d of this CTA's survivors (read by the other CTAs)
+    alignas(16) uint32_t hc[kFineBins];
+    // --- top-p window: this CTA's exact mass and count per group (read by the other CTAs), and
+    //     the cluster's sums
+    uint64_t wmass[kMaxWin];
+    uint32_t wcnt[kMaxWin];
+    uint64_t wm_all[kMaxWin];
+    uint32_t wc_all[kMaxWin];
     union alignas(16) {
-        struct {  // this CTA's share of the reduced histogram (read by the other CTAs)
-            uint32_t rcnt[kBins];
-            uint64_t rmass[kBins];
+        struct {  // sub-histogram over a key interval: local, then this CTA's share of the sums
+            uint32_t hcnt[kSubBins];
+            uint64_t hmass[kSubBins];
+            uint32_t rcnt[kSubBins];
+            uint64_t rmass[kSubBins];
         } sh;
         struct {  // gathered candidates (key << 32 | ~index), sorted descending, and mass prefixes
             uint64_t sbuf[kCand];
@@ -205,6 +217,29 @@ __device__ __forceinline__ uint64_t block_exscan_u64(uint64_t v, Shared& s, uint
     return before + x - v;
 }
 
+__device__ __forceinline__ double block_exscan_f64(double v, Shared& s, double* total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    double x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+    }
+    cta_sync();
+    if (lane == 31) s.rd[warp] = x;
+    cta_sync();
+    double before = 0.0, all = 0.0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const double t = s.rd[w];
+        if (w < warp) before += t;
+        all += t;
+    }
+    *total = all;
+    return before + (x - v);
+}
+
 // ---------------------------------------------------------------------------------------------
 // Topologies: the CTAs that share one row.  ClusterTopo is a thread-block cluster exchanging
 // through distributed shared memory; SoloTopo is a single CTA (map() is the identity).
@@ -212,6 +247,8 @@ __device__ __forceinline__ uint64_t block_exscan_u64(uint64_t v, Shared& s, uint
 struct ClusterTopo {
     cg::cluster_group g;
     uint32_t C, rank;
+    uint32_t* hr = nullptr;  // cluster-wide fine histogram (kFineBins counts, set by the kernel)
+    __device__ __forceinline__ uint32_t* fine(Shared&) { return hr; }
     __device__ __forceinline__ ClusterTopo() : g(cg::this_cluster())
     {
         C = g.num_blocks();
@@ -227,6 +264,7 @@ struct ClusterTopo {
 
 struct SoloTopo {
     uint32_t C = 1, rank = 0;
+    __device__ __forceinline__ uint32_t* fine(Shared& s) { return s.hc; }
     __device__ __forceinline__ void sync() { cta_sync(); }
     template <typename T>
     __device__ __forceinline__ T* map(T* p, uint32_t)
@@ -345,14 +383,144 @@ __device__ __forceinline__ float list_threshold(float m, float lt_hi)
     return m - (lt_hi + fabsf(m) * 0x1p-20f);
 }
 
-__device__ __forceinline__ int bin_of(float d)
+// d in fine-bin units: exactly kFineScale * dist(r, z) (a power-of-two scaling).
+__device__ __forceinline__ float dist_fine(const RowCtx& r, float z) { return dist(r, z) * kFineScale; }
+
+// Fine bin of a scaled distance d32 >= 0: floor(min(d32, kFineBins - 1)), with float adds only.
+// For every integer 1 <= b <= kFineBins - 1:  fine_bin(d32) < b  <=>  d32 < b.
+__device__ __forceinline__ int fine_bin(float d32)
 {
-    return min(__float2int_rz(d * kBinScale), kBins - 1);
+    const float c = fminf(d32, (float)(kFineBins - 1));
+    return (int)(__float_as_uint(__fadd_rd(c, 0x1p23f)) - 0x4B000000u);
 }
 
-// Cluster-wide sum of the local histogram hcnt/hmass[0, nb) into hcnt/hmass of every CTA.
+// Cluster-wide sum of the CTAs' fine histograms hc into hr (a copy for a cluster of one CTA; nothing
+// to do when hr is hc itself).
+// Starts with a topology barrier: every CTA's histogram and published values are then complete,
+// and stay readable until the caller's next topology barrier.
+template <typename Topo>
+__device__ __forceinline__ void reduce_fine(Topo& topo, Shared& s, uint32_t* hr)
+{
+    topo.sync();
+    if (topo.C > 1) {
+        for (int v = threadIdx.x; v < kFineBins / 4; v += kThreads) {
+            uint4 acc = make_uint4(0u, 0u, 0u, 0u);
+            for (uint32_t q = 0; q < topo.C; ++q) {
+                const uint4 x = *reinterpret_cast<const uint4*>(topo.map(&s.hc[4 * v], q));
+                acc.x += x.x;
+                acc.y += x.y;
+                acc.z += x.z;
+                acc.w += x.w;
+            }
+            reinterpret_cast<uint4*>(hr)[v] = acc;
+        }
+        cta_sync();
+    } else if (hr != s.hc) {  // a cluster of one CTA keeps its sums apart like a wider one
+        for (int v = threadIdx.x; v < kFineBins / 4; v += kThreads)
+            reinterpret_cast<uint4*>(hr)[v] = reinterpret_cast<const uint4*>(s.hc)[v];
+        cta_sync();
+    }
+}
+
+// Top-k on the fine counts: the last non-empty bin b with (count above b) < K, and that count.
+// Thread t owns bins 4t .. 4t+3 (kFineBins == 4 * kThreads).
+__device__ __forceinline__ void fine_scan_topk(Shared& s, const uint32_t* hr, uint64_t K, int* out_b, uint64_t* out_c)
+{
+    const int t = threadIdx.x;
+    const uint4 c4 = reinterpret_cast<const uint4*>(hr)[t];
+    const uint32_t c[4] = {c4.x, c4.y, c4.z, c4.w};
+    uint64_t tot;
+    const uint64_t pre = block_exscan_u64((uint64_t)c4.x + c4.y + c4.z + c4.w, s, &tot);
+    uint32_t best = 0;
+    uint64_t cum = pre, at = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (c[j] > 0 && cum < K) {
+            best = (uint32_t)(4 * t + j) + 1u;
+            at = cum;
+        }
+        cum += c[j];
+    }
+    const uint32_t bb = block_max_u32(best, s);  // >= 1: the bin of the maximum has nothing above it
+    if (bb != 0 && best == bb) s.b64[0] = at;
+    cta_sync();
+    *out_b = (int)bb - 1;
+    *out_c = s.b64[0];
+    cta_sync();
+}
+
+// The bins of d where the top-p crossing can lie, from the survivor counts alone.  c_b = hr[b] for
+// b < bk, `part` for b == bk, 0 above.  A token of bin b has d in [b, b+1)/32, so its fixed-point
+// mass / 2^44 lies within [e^-(b+1)/32, e^-b/32] up to expf's error and the rounding (the last bin:
+// [0, e^-1023/32]); margins of 1e-5 relative and 2^-44 absolute cover both.  With the masses above
+// bin b bounded by [cum_lo(b), cum_hi(b)] and Z by [Zlo, Zhi], the crossing (the last bin whose
+// mass above is below P Z) is a bin b with cum_lo(b) < P Zhi and cum_hi(b+1) >= P Zlo; every bin
+// before the first such bin is certainly kept.  The window's bins are split into at most kMaxWin
+// groups of 2^sh bins; `list` is set when the window and everything above it holds at most kCand
+// tokens.
+struct Window {
+    int b_lo, b_end, sh, nw;
+    bool list;
+};
+__device__ __forceinline__ Window top_p_window(Shared& s, const uint32_t* hr, int bk, uint32_t part, float P)
+{
+    const int t = threadIdx.x;
+    uint32_t c[4];
+    double lo[4], hi[4];
+    double slo = 0.0, shi = 0.0;
+    uint32_t last = 0;  // 1 + the last non-empty bin of this thread
+    float eb = expf(-(float)(4 * t) * (1.f / kFineScale));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int b = 4 * t + j;
+        c[j] = (b < bk) ? hr[b] : (b == bk ? part : 0u);
+        const float en = (b == kFineBins - 1) ? 0.f : expf(-(float)(b + 1) * (1.f / kFineScale));
+        lo[j] = (double)c[j] * fmax(0.0, (double)en * (1.0 - 1e-5) - 0x1p-44);
+        hi[j] = (double)c[j] * ((double)eb * (1.0 + 1e-5) + 0x1p-44);
+        eb = en;
+        slo += lo[j];
+        shi += hi[j];
+        if (c[j]) last = (uint32_t)b + 1u;
+    }
+    double Zlo, Zhi;
+    const double plo = block_exscan_f64(slo, s, &Zlo);
+    const double phi = block_exscan_f64(shi, s, &Zhi);
+    const double tlo = (double)P * Zlo, thi = (double)P * Zhi;
+    uint32_t b0 = (uint32_t)kFineBins, b1 = 0;
+    double cl = plo, ch = phi;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t b = (uint32_t)(4 * t + j);
+        if (cl < thi) b1 = b;
+        cl += lo[j];
+        ch += hi[j];
+        if (ch >= tlo && b0 == (uint32_t)kFineBins) b0 = b;
+    }
+    b0 = block_min_u32(b0, s);
+    b1 = block_max_u32(b1, s);
+    const uint32_t lastb = block_max_u32(last, s);  // >= 1
+    if (b0 >= (uint32_t)kFineBins) b0 = 0;          // cannot happen with P < 1; keep a valid window
+    b1 = min(b1, lastb - 1u);
+    if (b1 < b0) b1 = b0;
+    uint32_t upto = 0;  // tokens of S in bins <= b1
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        if ((uint32_t)(4 * t + j) <= b1) upto += c[j];
+    upto = block_sum_u32(upto, s);
+    Window w;
+    w.b_lo = (int)b0;
+    w.b_end = (int)b1 + 1;
+    const int nb = w.b_end - w.b_lo;
+    w.sh = 0;
+    while (((nb - 1) >> w.sh) + 1 > kMaxWin) ++w.sh;
+    w.nw = ((nb - 1) >> w.sh) + 1;
+    w.list = upto <= (uint32_t)kCand;
+    return w;
+}
+
+// Cluster-wide sum of the sub-histogram u.sh.hcnt/hmass[0, nb) into u.sh.hcnt/hmass of every CTA.
 // Step 1: CTA c sums its share of the bins over all CTAs (one remote read per thread) into
-// u.sh; step 2: every CTA copies all shares back into its own hcnt/hmass.
+// u.sh.rcnt/rmass; step 2: every CTA copies all shares back into its own hcnt/hmass.
 template <typename Topo>
 __device__ __forceinline__ void cluster_reduce_hist(Topo& topo, Shared& s, int nb)
 {
@@ -373,18 +541,17 @@ __device__ __forceinline__ void cluster_reduce_hist(Topo& topo, Shared& s, int n
     for (int p = threadIdx.x; p < npairs; p += kThreads) {
         const int b = b0 + p / (int)C;
         const uint32_t r = (uint32_t)(p % (int)C);
-        const uint32_t c = *topo.map(&s.hcnt[b], r);
+        const uint32_t c = *topo.map(&s.u.sh.hcnt[b], r);
         if (c) {
             atomicAdd(&s.u.sh.rcnt[b], c);
-            atomicAdd((unsigned long long*)&s.u.sh.rmass[b],
-                      (unsigned long long)*topo.map(&s.hmass[b], r));
+            atomicAdd((unsigned long long*)&s.u.sh.rmass[b], (unsigned long long)*topo.map(&s.u.sh.hmass[b], r));
         }
     }
     topo.sync();  // all shares complete; nobody reads another CTA's hcnt/hmass any more
     for (int b = threadIdx.x; b < nb; b += kThreads) {
         const uint32_t owner = (uint32_t)(b / per);
-        s.hcnt[b] = *topo.map(&s.u.sh.rcnt[b], owner);
-        s.hmass[b] = *topo.map(&s.u.sh.rmass[b], owner);
+        s.u.sh.hcnt[b] = *topo.map(&s.u.sh.rcnt[b], owner);
+        s.u.sh.hmass[b] = *topo.map(&s.u.sh.rmass[b], owner);
     }
     cta_sync();
 }
@@ -405,14 +572,14 @@ struct Crit {
     }
 };
 
-// Scan the (full) histogram hcnt/hmass[0, nb) from bin 0 (largest logits) down and return the
+// Scan the (full) sub-histogram u.sh.hcnt/hmass[0, nb) from bin 0 (largest logits) down and return the
 // last non-empty bin whose (count, mass) above satisfies the criterion.  nb <= kThreads.
 __device__ __forceinline__ void scan_bins(Shared& s, int nb, const Crit& cr, uint64_t C0, uint64_t A0,
                                           int* out_bin, uint64_t* out_c, uint64_t* out_a)
 {
     const int b = threadIdx.x;
-    const uint64_t c = (b < nb) ? s.hcnt[b] : 0;
-    const uint64_t m = (b < nb) ? s.hmass[b] : 0;
+    const uint64_t c = (b < nb) ? s.u.sh.hcnt[b] : 0;
+    const uint64_t m = (b < nb) ? s.u.sh.hmass[b] : 0;
     uint64_t tot;
     const uint64_t cpre = block_exscan_u64(c, s, &tot);
     const uint64_t mpre = block_exscan_u64(m, s, &tot);
@@ -497,9 +664,9 @@ __device__ __forceinline__ Sel walk_classes(Shared& s, int n, const Crit& cr, ui
     return out;
 }
 
-// Copy every CTA's candidate list (counts in pub_gcnt) into u.cd.sbuf and sort it.  Returns n.
+// Copy every CTA's candidate list (counts in pub_gcnt) into u.cd.sbuf (unsorted).  Returns n.
 template <typename Topo>
-__device__ __forceinline__ int gather_and_sort(Topo& topo, Shared& s)
+__device__ __forceinline__ int gather_lists(Topo& topo, Shared& s)
 {
     const uint32_t C = topo.C;
     if (threadIdx.x < 32) {  // lane r reads rank r's count; exclusive prefix over the ranks
@@ -528,8 +695,15 @@ __device__ __forceinline__ int gather_and_sort(Topo& topo, Shared& s)
         }
     }
     cta_sync();
-    block_sort_desc(s, (int)n);
     return (int)n;
+}
+
+template <typename Topo>
+__device__ __forceinline__ int gather_and_sort(Topo& topo, Shared& s)
+{
+    const int n = gather_lists(topo, s);
+    block_sort_desc(s, n);
+    return n;
 }
 
 // Race key in float (for pruning) and in double (for the decision) of kept token i.
@@ -557,16 +731,16 @@ __device__ __forceinline__ double race_key64(const RowCtx& r, float z, float u)
 // kept tokens have d <= dcut.
 __device__ __forceinline__ float race_tol(float dcut) { return 1e-5f + 1e-6f * dcut; }
 
-// Refine the cut inside level-1 bin `bin` (tokens with key >= key_lo that survive min-p), given
-// the (count, mass) of the survivors above the bin.  Exact: ends with a sorted candidate list or
-// with a single logit value.
+// Refine the cut among the survivors (min-p, key >= key_lo) whose scaled distance d32 lies in
+// [flo, fhi), given the (count, mass) of the survivors above that range.  Exact: ends with a sorted
+// candidate list or with a single logit value.  Starts with a topology barrier.
 template <typename Topo, typename Src>
-__device__ Sel refine_bin(Topo& topo, Shared& s, const Src& sl, const RowCtx& r, float zc, int bin, uint32_t key_lo,
-                          const Crit& cr, uint64_t C0, uint64_t A0)
+__device__ Sel refine_range(Topo& topo, Shared& s, const Src& sl, const RowCtx& r, float zc, float flo, float fhi,
+                            uint32_t key_lo, const Crit& cr, uint64_t C0, uint64_t A0)
 {
     const uint32_t C = topo.C;
     uint32_t klo = 0, khi = 0xFFFFFFFFu;
-    bool by_bin = true;
+    bool by_range = true;
     for (int iter = 0; iter < 8; ++iter) {
         // Gather the tokens of the current range (a level-1 bin, or a key interval).
         topo.sync();  // nobody still reads my candidate list, published counts or shares
@@ -579,7 +753,10 @@ __device__ Sel refine_bin(Topo& topo, Shared& s, const Src& sl, const RowCtx& r,
             const uint32_t key = fkey(z);
             if (key < key_lo || key < lo || key > hi) return;
             const float d = dist(r, z);
-            if (by_bin && bin_of(d) != bin) return;
+            if (by_range) {
+                const float d32 = d * kFineScale;
+                if (!(d32 >= flo && d32 < fhi)) return;
+            }
             if (!minp_ok(r, z, d)) return;
             ++lcnt;
             lmin = min(lmin, key);
@@ -645,13 +822,13 @@ __device__ Sel refine_bin(Topo& topo, Shared& s, const Src& sl, const RowCtx& r,
         // Too many: split the key range [gmin, gmax] into sub-bins (sub-bin 0 = largest keys).
         klo = gmin;
         khi = gmax;
-        by_bin = false;
+        by_range = false;
         int sh = 0;
         while (((uint64_t)(khi - klo) >> sh) >= (uint64_t)kSubBins) ++sh;
         const int nsub = (int)((uint64_t)(khi - klo) >> sh) + 1;
         for (int b = threadIdx.x; b < kSubBins; b += kThreads) {
-            s.hcnt[b] = 0;
-            s.hmass[b] = 0;
+            s.u.sh.hcnt[b] = 0;
+            s.u.sh.hmass[b] = 0;
         }
         cta_sync();
         const uint32_t lo2 = klo, hi2 = khi;
@@ -662,8 +839,8 @@ __device__ Sel refine_bin(Topo& topo, Shared& s, const Src& sl, const RowCtx& r,
             const float d = dist(r, z);
             if (!minp_ok(r, z, d)) return;
             const int sb = (int)((hi2 - key) >> sh);
-            atomicAdd(&s.hcnt[sb], 1u);
-            atomicAdd((unsigned long long*)&s.hmass[sb], (unsigned long long)qmass_d(d));
+            atomicAdd(&s.u.sh.hcnt[sb], 1u);
+            atomicAdd((unsigned long long*)&s.u.sh.hmass[sb], (unsigned long long)qmass_d(d));
         });
         cluster_reduce_hist(topo, s, kSubBins);
         int jb;
@@ -678,7 +855,7 @@ __device__ Sel refine_bin(Topo& topo, Shared& s, const Src& sl, const RowCtx& r,
         khi = (uint32_t)top;
         klo = (uint32_t)max((uint64_t)lo2, bot);
     }
-    // Unreachable in practice (each split shrinks the 32-bit range by 2^8); keep a valid answer.
+    // Unreachable in practice (each split shrinks the 32-bit range by 2^7); keep a valid answer.
     Sel o;
     o.key = khi;
     o.cnt = C0;
@@ -701,8 +878,10 @@ struct WarpResult {
 
 // Resolve a row whose survivors are buf[0, n) (n <= 32, unsorted) with one warp.  Every lane
 // returns the same result.
+// z_ext != 0: the list is the top of a larger set whose fixed-point mass is z_ext (top-p is taken
+// against it; top-k must then be off).
 __device__ __forceinline__ WarpResult warp_resolve(const uint64_t* buf, const RowCtx& r, const RaceCtx& rc, uint32_t n,
-                                                   bool topk_on, int32_t K, float P)
+                                                   bool topk_on, int32_t K, float P, uint64_t z_ext = 0)
 {
     const uint32_t lane = threadIdx.x & 31;
     uint64_t v = (lane < n) ? buf[lane] : 0;
@@ -746,7 +925,7 @@ __device__ __forceinline__ WarpResult warp_resolve(const uint64_t* buf, const Ro
         *e_out = ends ? (uint32_t)(__ffs(ends) - 1) : lim;
     };
     uint32_t ns = n;
-    uint64_t zs = total;
+    uint64_t zs = z_ext ? z_ext : total;
     if (topk_on && n > (uint32_t)K) {
         uint32_t st, e;
         cut(n, false, (uint64_t)K, 0.0, &st, &e);
@@ -1032,16 +1211,17 @@ __device__ __forceinline__ float minp_threshold(const RowCtx& r)
 }
 
 // Resolve a row whose min-p survivors are u.cd.sbuf[0, n) (n <= kCand, any order): top-k, top-p,
-// race.  n <= 32 runs in warp 0 alone; larger n sorts with the whole CTA.
+// race.  n <= 32 runs in warp 0 alone; larger n sorts with the whole CTA.  z_ext != 0: the list is
+// the top of the survivors, whose whole fixed-point mass is z_ext (top-k already applied).
 __device__ __forceinline__ RowResult resolve_candidates(Shared& s, const RowCtx& r, const RaceCtx& rc, uint32_t n,
-                                                        bool topk_on, int32_t K, float P)
+                                                        bool topk_on, int32_t K, float P, uint64_t z_ext = 0)
 {
     const int tid = threadIdx.x;
     const uint32_t lane = tid & 31;
     RowResult out;
     if (n <= 32) {
         if (tid < 32) {
-            const WarpResult wr = warp_resolve(s.u.cd.sbuf, r, rc, n, topk_on, K, P);
+            const WarpResult wr = warp_resolve(s.u.cd.sbuf, r, rc, n, topk_on, K, P, z_ext);
             if (lane == 0) {
                 s.bu[4] = wr.key_cut;
                 s.bu[5] = wr.nk;
@@ -1060,7 +1240,7 @@ __device__ __forceinline__ RowResult resolve_candidates(Shared& s, const RowCtx&
     block_sort_desc(s, (int)n);
     prefix_masses(s, r, (int)n);
     int nS = (int)n;
-    uint64_t ZS = s.u.cd.pre[n];
+    uint64_t ZS = z_ext ? z_ext : s.u.cd.pre[n];
     if (topk_on && n > (uint32_t)K) {
         Crit ck;
         ck.by_mass = false;
@@ -1135,185 +1315,43 @@ __device__ __forceinline__ void write_probs(const Src& src, const Shared& s, con
     });
 }
 
-// The general path: min-p survivors counted against the global maximum (threshold zc), then the
-// top-k and top-p cuts -- from a sorted candidate list when there are few survivors, else located by
-// a histogram over d and refined exactly -- then the race over the kept tokens of the source, with
-// the optional probability row written in the same pass.  Starts with a topology barrier, so the
-// caller's published values may still be read by other CTAs when it is entered.
+// Per-thread race over kept tokens: the best two float race keys (and the best's index).  A token
+// is skipped without drawing its uniform when even the largest -ln(-ln u) of the uniform grid
+// (u = 1 - 2^-24 gives 16.6355...) cannot lift its key to this thread's second-best key: such a
+// token can be neither the best nor the second best.  Consecutive tokens share one Philox block.
+struct RaceAcc {
+    Top2 t2;
+    uint32_t ctr;
+    uint4 x;
+    __device__ __forceinline__ void init()
+    {
+        t2.init();
+        ctr = 0xFFFFFFFFu;
+    }
+    __device__ __forceinline__ void add(const RaceCtx& rc, float d, int32_t i)
+    {
+        if (16.64f - d < t2.k2) return;
+        const uint32_t c = (uint32_t)i >> 2;
+        if (c != ctr) {
+            ctr = c;
+            x = philox4x32_10(make_uint4(c, rc.row, rc.s_lo, rc.s_hi), rc.k0, rc.k1);
+        }
+        const float u = (float)uniform_grid(pick_word(x, (uint32_t)i & 3u)) * 0x1p-24f;
+        t2.add(race_key32(d, u), i);
+    }
+};
+
+// Merge the threads' race results over the topology and decide the token exactly: the best float
+// key wins when it leads the second by more than the float/double margin; otherwise every kept
+// token (key >= kc) within the margin of the best is re-evaluated in double precision.
 template <typename Topo, typename Src>
-__device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const RowCtx& r, float zc, bool topk_on,
-                                  int32_t K, float P, const RaceCtx& rc, float* prow)
+__device__ int32_t race_finish(Topo& topo, Shared& s, const Src& src, const RowCtx& r, const RaceCtx& rc, Top2 t2,
+                               uint32_t kc)
 {
     const int tid = threadIdx.x;
     const uint32_t lane = tid & 31;
     const uint32_t C = topo.C;
-    topo.sync();  // nobody still reads the caller's lists or published values
-    if (tid == 0) s.ncand = 0;
-    cta_sync();
-    uint32_t my_minkey = 0xFFFFFFFFu;
-    uint32_t my_surv = 0;
-    src.for_each(s, [&](float z, int32_t i) {
-        if (!(z > zc)) return;
-        if (!minp_ok(r, z, dist(r, z))) return;
-        const uint32_t key = fkey(z);
-        my_minkey = min(my_minkey, key);
-        ++my_surv;
-        if (*(volatile uint32_t*)&s.ncand < (uint32_t)kCand) {
-            const uint32_t slot = atomicAdd(&s.ncand, 1u);
-            if (slot < (uint32_t)kCand) {
-                s.ckey[slot] = key;
-                s.cidx[slot] = (uint32_t)i;
-            }
-        }
-    });
-    my_surv = warp_sum_u32(my_surv);
-    my_minkey = warp_min_u32(my_minkey);
-    if (lane == 0) {
-        s.ra[tid >> 5] = my_surv;
-        s.rb[tid >> 5] = my_minkey;
-    }
-    cta_sync();
-    if (tid == 0) {
-        uint32_t ns = 0, mk = 0xFFFFFFFFu;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            ns += s.ra[w];
-            mk = min(mk, s.rb[w]);
-        }
-        s.pub_nsurv = ns;
-        s.pub_gcnt = min(ns, (uint32_t)kCand);
-        s.pub_minkey = mk;
-    }
-    topo.sync();
-    if (tid < 32) {
-        uint32_t ns = 0, mk = 0xFFFFFFFFu;
-        if (lane < C) {
-            ns = *topo.map(&s.pub_nsurv, lane);
-            mk = *topo.map(&s.pub_minkey, lane);
-        }
-        ns = warp_sum_u32(ns);
-        mk = warp_min_u32(mk);
-        if (lane == 0) {
-            s.bu[2] = ns;
-            s.bu[3] = mk;
-        }
-    }
-    cta_sync();
-    const uint64_t NS0 = s.bu[2];
-    RowResult res;
-    res.key_cut = s.bu[3];
-    res.nk = NS0;
-    res.zk = 0;
-
-    if (NS0 <= (uint64_t)kCand) {
-        // ---- few survivors: sort them (in every CTA)
-        const int n = gather_and_sort(topo, s);
-        prefix_masses(s, r, n);
-        int nS = n;
-        uint64_t ZS = s.u.cd.pre[n];
-        if (topk_on && (uint64_t)n > (uint64_t)K) {
-            Crit ck;
-            ck.by_mass = false;
-            ck.tcnt = (uint64_t)K;
-            ck.tmass = 0.0;
-            const Sel sk = walk_classes(s, n, ck, 0, 0);
-            nS = (int)sk.cnt;
-            ZS = sk.mass;
-        }
-        res.nk = (uint64_t)nS;
-        res.zk = ZS;
-        if (P < 1.f) {
-            Crit cp;
-            cp.by_mass = P > 0.f;
-            cp.tcnt = 1;
-            cp.tmass = (double)P * (double)ZS;
-            const Sel sp = walk_classes(s, nS, cp, 0, 0);
-            res.nk = sp.cnt;
-            res.zk = sp.mass;
-        }
-        res.key_cut = sb_key(s.u.cd.sbuf[res.nk - 1]);
-    } else {
-        // ---- many survivors: histogram-located cuts, refined exactly
-        for (int b = tid; b < kBins; b += kThreads) {
-            s.hcnt[b] = 0;
-            s.hmass[b] = 0;
-        }
-        cta_sync();
-        auto build_hist = [&](uint32_t key_floor) {
-            src.for_each(s, [&](float z, int32_t) {
-                if (!(z > zc)) return;
-                if (fkey(z) < key_floor) return;
-                const float d = dist(r, z);
-                if (!minp_ok(r, z, d)) return;
-                const int b = bin_of(d);
-                atomicAdd(&s.hcnt[b], 1u);
-                atomicAdd((unsigned long long*)&s.hmass[b], (unsigned long long)qmass_d(d));
-            });
-        };
-        build_hist(0u);
-        cluster_reduce_hist(topo, s, kBins);
-        uint64_t ZS;
-        {
-            uint64_t tot;
-            (void)block_exscan_u64(s.hmass[tid], s, &tot);  // kBins == kThreads
-            ZS = tot;
-        }
-        uint64_t NS = NS0;
-        if (topk_on && NS0 > (uint64_t)K) {
-            Crit ck;
-            ck.by_mass = false;
-            ck.tcnt = (uint64_t)K;
-            ck.tmass = 0.0;
-            int bk;
-            uint64_t c_at, a_at;
-            scan_bins(s, kBins, ck, 0, 0, &bk, &c_at, &a_at);
-            if (bk < 0) bk = 0;
-            const Sel sk = refine_bin(topo, s, src, r, zc, bk, 0u, ck, c_at, a_at);
-            res.key_cut = max(res.key_cut, sk.key);
-            NS = sk.cnt;
-            ZS = sk.mass;
-            if (P < 1.f) {  // rebuild the histogram over S = {key >= key_cut} for the top-p scan
-                topo.sync();
-                for (int b = tid; b < kBins; b += kThreads) {
-                    s.hcnt[b] = 0;
-                    s.hmass[b] = 0;
-                }
-                cta_sync();
-                build_hist(res.key_cut);
-                cluster_reduce_hist(topo, s, kBins);
-            }
-        }
-        res.nk = NS;
-        res.zk = ZS;
-        if (P < 1.f) {
-            Crit cp;
-            cp.by_mass = P > 0.f;
-            cp.tcnt = 1;
-            cp.tmass = (double)P * (double)ZS;
-            int bp;
-            uint64_t c_at, a_at;
-            scan_bins(s, kBins, cp, 0, 0, &bp, &c_at, &a_at);
-            if (bp < 0) bp = 0;
-            const Sel sp = refine_bin(topo, s, src, r, zc, bp, res.key_cut, cp, c_at, a_at);
-            res.key_cut = max(res.key_cut, sp.key);
-            res.nk = sp.cnt;
-            res.zk = sp.mass;
-        }
-    }
-
-    // ---- race over the kept tokens of the source (+ probabilities): float keys first; the best
-    //      two decide whether double precision is needed at all
-    const float tol = race_tol(dist(r, key_to_float(res.key_cut)));
-    const uint32_t kc = res.key_cut;
-    const double zk = (double)res.zk;
-    Top2 t2;
-    t2.init();
-    src.for_each(s, [&](float z, int32_t i) {
-        const bool kept = (z > -INFINITY) && fkey(z) >= kc;
-        if (prow) prow[i] = kept ? (float)((double)qmass_d(dist(r, z)) / zk) : 0.f;
-        if (!kept) return;
-        t2.add(race_key32(dist(r, z), race_u(rc, i)), i);
-    });
+    const float tol = race_tol(dist(r, key_to_float(kc)));
     t2 = warp_top2(t2);
     cta_sync();
     if (lane == 0) {
@@ -1354,7 +1392,7 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
     }
     cta_sync();
     const float M1 = s.bf[1], M2 = s.bf[0];
-    res.token = (int32_t)s.bu[6];
+    int32_t token = (int32_t)s.bu[6];
     if (!(M1 - M2 > tol)) {
         // near-tie: every kept token within tol of the best is re-evaluated in double precision
         ArgBest mine;
@@ -1390,9 +1428,352 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
             if (lane == 0) s.bu[6] = (uint32_t)x.idx;
         }
         cta_sync();
-        res.token = (int32_t)s.bu[6];
+        token = (int32_t)s.bu[6];
     }
     cta_sync();
+    return token;
+}
+
+// Sum of one u64 per thread over the CTA (every thread gets it).
+__device__ __forceinline__ uint64_t block_sum_u64(uint64_t v, Shared& s)
+{
+    uint64_t tot;
+    (void)block_exscan_u64(v, s, &tot);
+    return tot;
+}
+
+// The general path, for rows whose survivors are not already listed.  S0 = the min-p survivors
+// against the global maximum (z > zc and minp_ok); S = S0 cut by top-k; the kept set = S cut by
+// top-p.  Every cut is an upper set in z, found exactly:
+//   A. one pass: counts of S0 over fine bins of d (32-bit atomics), the first kCand listed;
+//      few survivors -> sort the lists and resolve them;
+//   B. top-k from the counts, refined exactly inside its crossing bin (or, when everything down to
+//      that bin fits a list, by listing it);
+//   C. top-p: bounds on the bins' masses give a window of bins holding the crossing; one exact
+//      pass sums the fixed-point masses of S (per thread, no atomics), of the tokens above the
+//      window, and per window group (atomics on window tokens only), racing the tokens above the
+//      window, which are certainly kept; then an exact refinement inside the crossing group and
+//      a race over the window's kept tokens.  A window that does not hold the crossing (not
+//      expected: the bounds are rigorous) is replaced by one covering every bin.
+// Starts with a topology barrier, so the caller's published values may still be read by other CTAs
+// when it is entered.
+template <typename Topo, typename Src>
+__device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const RowCtx& r, float zc, bool topk_on,
+                                  int32_t K, float P, const RaceCtx& rc, float* prow)
+{
+    const int tid = threadIdx.x;
+    const uint32_t lane = tid & 31;
+    const uint32_t C = topo.C;
+    uint32_t* hr = topo.fine(s);
+
+    // ---- A: fine counts of S0, the first kCand survivors listed
+    topo.sync();  // nobody still reads the caller's lists or published values
+    for (int b = tid; b < kFineBins; b += kThreads) s.hc[b] = 0;
+    if (tid == 0) s.ncand = 0;
+    cta_sync();
+    uint32_t my_minkey = 0xFFFFFFFFu;
+    bool full = false;
+    src.for_each(s, [&](float z, int32_t i) {
+        if (!(z > zc)) return;
+        const float d = dist(r, z);
+        if (!minp_ok(r, z, d)) return;
+        const uint32_t key = fkey(z);
+        my_minkey = min(my_minkey, key);
+        atomicAdd(&s.hc[fine_bin(d * kFineScale)], 1u);
+        if (!full) {
+            const uint32_t slot = atomicAdd(&s.ncand, 1u);
+            if (slot < (uint32_t)kCand) {
+                s.ckey[slot] = key;
+                s.cidx[slot] = (uint32_t)i;
+            } else {
+                full = true;
+            }
+        }
+    });
+    my_minkey = block_min_u32(my_minkey, s);
+    if (tid == 0) {
+        s.pub_gcnt = min(s.ncand, (uint32_t)kCand);
+        s.pub_minkey = my_minkey;
+    }
+    reduce_fine(topo, s, hr);  // topology barrier first
+    if (tid < 32) {
+        uint32_t mk = (lane < C) ? *topo.map(&s.pub_minkey, lane) : 0xFFFFFFFFu;
+        mk = warp_min_u32(mk);
+        if (lane == 0) s.bu[3] = mk;
+    }
+    uint32_t ns0 = 0;
+    {
+        const uint4 c4 = reinterpret_cast<const uint4*>(hr)[tid];
+        ns0 = block_sum_u32(c4.x + c4.y + c4.z + c4.w, s);  // (its barriers publish bu[3])
+    }
+    const uint32_t min_key = s.bu[3];
+    RowResult res;
+
+    if (ns0 <= (uint32_t)kCand) {
+        // ---- few survivors: every one is on some CTA's list
+        const int n = gather_lists(topo, s);
+        res = resolve_candidates(s, r, rc, (uint32_t)n, topk_on, K, P);
+        if (prow) write_probs(src, s, r, res.key_cut, res.zk, prow);
+        return res;
+    }
+
+    // ---- B: top-k on the counts
+    uint32_t key_k = 0;
+    uint64_t NS = ns0;
+    int bk = kFineBins;  // bins above bk hold no token of S; bin bk holds `part` of them
+    uint32_t part = 0;
+    if (topk_on && (uint64_t)ns0 > (uint64_t)K) {
+        uint64_t ck;
+        fine_scan_topk(s, hr, (uint64_t)K, &bk, &ck);
+        const uint64_t upto = ck + hr[bk];
+        if (upto <= (uint64_t)kCand) {
+            // everything down to the crossing bin fits one list: list it and resolve exactly
+            topo.sync();  // the other CTAs are done with this CTA's published values
+            if (tid == 0) s.ncand = 0;
+            cta_sync();
+            const float fend = (bk >= kFineBins - 1) ? INFINITY : (float)(bk + 1);
+            src.for_each(s, [&](float z, int32_t i) {
+                if (!(z > zc)) return;
+                const float d = dist(r, z);
+                if (!(d * kFineScale < fend) || !minp_ok(r, z, d)) return;
+                const uint32_t slot = atomicAdd(&s.ncand, 1u);
+                s.ckey[slot] = fkey(z);
+                s.cidx[slot] = (uint32_t)i;
+            });
+            cta_sync();
+            if (tid == 0) s.pub_gcnt = s.ncand;
+            topo.sync();
+            const int n = gather_lists(topo, s);
+            res = resolve_candidates(s, r, rc, (uint32_t)n, topk_on, K, P);
+            if (prow) write_probs(src, s, r, res.key_cut, res.zk, prow);
+            return res;
+        }
+        Crit ck2;
+        ck2.by_mass = false;
+        ck2.tcnt = (uint64_t)K;
+        ck2.tmass = 0.0;
+        const float fhi = (bk >= kFineBins - 1) ? INFINITY : (float)(bk + 1);
+        const Sel sk = refine_range(topo, s, src, r, zc, (float)bk, fhi, 0u, ck2, ck, 0);
+        key_k = sk.key;
+        NS = sk.cnt;
+        part = (uint32_t)(sk.cnt - ck);
+    }
+
+    // ---- C: top-p and the race
+    RaceAcc race;
+    race.init();
+    if (!(P > 0.f && P < 1.f)) {
+        if (P <= 0.f) {  // only the top class
+            Crit c1;
+            c1.by_mass = false;
+            c1.tcnt = 1;
+            c1.tmass = 0.0;
+            const Sel s1 = refine_range(topo, s, src, r, zc, 0.f, 1.f, key_k, c1, 0, 0);
+            res.key_cut = s1.key;
+            res.nk = s1.cnt;
+            res.zk = s1.mass;
+        } else {  // no top-p cut: S is kept
+            res.key_cut = max(key_k, min_key);
+            res.nk = NS;
+            res.zk = 0;
+        }
+        const uint32_t kc = res.key_cut;
+        const bool sum_z = prow != nullptr && P >= 1.f;  // the kept mass, for the probabilities
+        uint64_t zhi = 0, zlo = 0;
+        src.for_each(s, [&](float z, int32_t i) {
+            if (!((z > -INFINITY) && fkey(z) >= kc)) return;
+            const float d = dist(r, z);
+            if (sum_z) {
+                const Fixed44 f = fixed44_parts(expf(-d));
+                zhi += f.hi;
+                zlo += f.lo;
+            }
+            race.add(rc, d, i);
+        });
+        if (sum_z) {
+            const uint64_t cta = block_sum_u64((zhi << 22) + zlo, s);
+            if (tid == 0) s.pub_z = cta;
+            topo.sync();
+            if (tid < 32) {
+                uint64_t z = (lane < C) ? *topo.map(&s.pub_z, lane) : 0;
+                z = warp_sum_u64(z);
+                if (lane == 0) s.b64[2] = z;
+            }
+            cta_sync();
+            res.zk = s.b64[2];
+        }
+        res.token = race_finish(topo, s, src, r, rc, race.t2, kc);
+        if (prow) write_probs(src, s, r, res.key_cut, res.zk, prow);
+        return res;
+    }
+
+    Window w = top_p_window(s, hr, bk, part, P);
+    uint64_t Z = 0, A = 0;
+    uint32_t CA = 0;
+    double tmass = 0.0;
+    int nlist = -1;  // list mode: the sorted list of S down to the window's end
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        if (attempt == 1) {  // a window covering every bin
+            w.b_lo = 0;
+            w.b_end = kFineBins;
+            w.sh = 0;
+            while (((kFineBins - 1) >> w.sh) + 1 > kMaxWin) ++w.sh;
+            w.nw = ((kFineBins - 1) >> w.sh) + 1;
+            w.list = false;
+            race.init();
+        }
+        const float flo = (float)w.b_lo;
+        const float fend = (w.b_end >= kFineBins) ? INFINITY : (float)w.b_end;
+        const bool list = w.list;
+        const int b_lo = w.b_lo, sh = w.sh;
+        topo.sync();  // nobody still reads this CTA's window sums, lists or published values
+        if (tid < kMaxWin) {
+            s.wmass[tid] = 0;
+            s.wcnt[tid] = 0;
+        }
+        if (tid == 0) s.ncand = 0;
+        cta_sync();
+        uint64_t zhi = 0, zlo = 0, ahi = 0, alo = 0;  // high (x 2^22) and low parts of the sums
+        uint32_t ca = 0;
+        src.for_each(s, [&](float z, int32_t i) {
+            if (!(z > zc)) return;
+            const uint32_t key = fkey(z);
+            if (key < key_k) return;
+            const float d = dist(r, z);
+            if (!minp_ok(r, z, d)) return;
+            const Fixed44 f = fixed44_parts(expf(-d));
+            zhi += f.hi;
+            zlo += f.lo;
+            const float d32 = d * kFineScale;
+            if (list) {
+                if (d32 < fend) {
+                    const uint32_t slot = atomicAdd(&s.ncand, 1u);
+                    s.ckey[slot] = key;
+                    s.cidx[slot] = (uint32_t)i;
+                }
+            } else if (d32 < flo) {  // certainly kept
+                ahi += f.hi;
+                alo += f.lo;
+                ++ca;
+                race.add(rc, d, i);
+            } else if (d32 < fend) {
+                const int g = (fine_bin(d32) - b_lo) >> sh;
+                atomicAdd((unsigned long long*)&s.wmass[g], (unsigned long long)(((uint64_t)f.hi << 22) + f.lo));
+                atomicAdd(&s.wcnt[g], 1u);
+            }
+        });
+        const uint64_t zc_ = block_sum_u64((zhi << 22) + zlo, s);
+        const uint64_t ac_ = block_sum_u64((ahi << 22) + alo, s);
+        const uint32_t cc_ = block_sum_u32(ca, s);
+        if (tid == 0) {
+            s.pub_z = zc_;
+            s.pub_a = ac_;
+            s.pub_ca = cc_;
+            s.pub_gcnt = s.ncand;
+        }
+        topo.sync();
+        if (tid < 32) {
+            uint64_t z = 0, a = 0;
+            uint32_t c = 0;
+            if (lane < C) {
+                z = *topo.map(&s.pub_z, lane);
+                a = *topo.map(&s.pub_a, lane);
+                c = *topo.map(&s.pub_ca, lane);
+            }
+            z = warp_sum_u64(z);
+            a = warp_sum_u64(a);
+            c = warp_sum_u32(c);
+            if (lane == 0) {
+                s.b64[2] = z;
+                s.b64[3] = a;
+                s.bu[7] = c;
+            }
+        }
+        if (!list && tid < w.nw) {
+            uint64_t m = 0;
+            uint32_t c = 0;
+            for (uint32_t q = 0; q < C; ++q) {
+                m += *topo.map(&s.wmass[tid], q);
+                c += *topo.map(&s.wcnt[tid], q);
+            }
+            s.wm_all[tid] = m;
+            s.wc_all[tid] = c;
+        }
+        cta_sync();
+        Z = s.b64[2];
+        A = s.b64[3];
+        CA = s.bu[7];
+        tmass = (double)P * (double)Z;
+        if (list) {
+            const int n = gather_and_sort(topo, s);
+            prefix_masses(s, r, n);
+            if ((double)s.u.cd.pre[n] >= tmass) {  // the list holds the crossing
+                nlist = n;
+                break;
+            }
+        } else {
+            uint64_t all = A;
+            for (int g = 0; g < w.nw; ++g) all += s.wm_all[g];
+            if ((double)A < tmass && (double)all >= tmass) break;
+        }
+    }
+
+    if (nlist >= 0) {
+        // list mode: the kept set is a prefix of the sorted list
+        Crit cp;
+        cp.by_mass = true;
+        cp.tcnt = 1;
+        cp.tmass = tmass;
+        const Sel sp = walk_classes(s, nlist, cp, 0, 0);
+        res.key_cut = sp.key;
+        res.nk = sp.cnt;
+        res.zk = sp.mass;
+        const uint32_t kc = res.key_cut;
+        for (int e = tid; e < (int)res.nk; e += kThreads) {  // kept entries of the list
+            const uint64_t v = s.u.cd.sbuf[e];
+            race.add(rc, dist(r, key_to_float(sb_key(v))), sb_idx(v));
+        }
+        res.token = race_finish(topo, s, src, r, rc, race.t2, kc);
+        if (prow) write_probs(src, s, r, res.key_cut, res.zk, prow);
+        return res;
+    }
+
+    // the crossing group: the last group whose mass above is below tmass
+    int gs = 0;
+    uint64_t cum = A, C0 = CA, A0 = A;
+    {
+        uint64_t cnt = CA;
+        for (int g = 0; g < w.nw; ++g) {
+            if ((double)cum < tmass) {
+                gs = g;
+                A0 = cum;
+                C0 = cnt;
+            }
+            cum += s.wm_all[g];
+            cnt += s.wc_all[g];
+        }
+    }
+    const int g_lo = w.b_lo + (gs << w.sh), g_end = min(w.b_lo + ((gs + 1) << w.sh), w.b_end);
+    Crit cp;
+    cp.by_mass = true;
+    cp.tcnt = 1;
+    cp.tmass = tmass;
+    const Sel sp = refine_range(topo, s, src, r, zc, (float)g_lo, (g_end >= kFineBins) ? INFINITY : (float)g_end,
+                                key_k, cp, C0, A0);
+    res.key_cut = max(sp.key, key_k);
+    res.nk = sp.cnt;
+    res.zk = sp.mass;
+    // race over the window's kept tokens (those above the window were raced in the exact pass)
+    const uint32_t kc = res.key_cut;
+    const float flo = (float)w.b_lo;
+    src.for_each(s, [&](float z, int32_t i) {
+        if (!((z > -INFINITY) && fkey(z) >= kc)) return;
+        const float d = dist(r, z);
+        if (d * kFineScale < flo) return;
+        race.add(rc, d, i);
+    });
+    res.token = race_finish(topo, s, src, r, rc, race.t2, kc);
+    if (prow) write_probs(src, s, r, res.key_cut, res.zk, prow);
     return res;
 }
 

@@ -70,13 +70,33 @@ struct RowCtx {
 // Scaled distance from the maximum, d = (zmax - z) / T >= 0, monotone non-increasing in z.
 __device__ __forceinline__ float dist(const RowCtx& r, float z) { return (r.zmax - z) * r.invT; }
 
+// round(e * 2^44) to the nearest integer, ties to even, for 0 <= e <= 1, as hi * 2^22 + lo -- with
+// float adds and one fused multiply-add instead of a float-to-64-bit conversion (a slow pipe):
+//   t  = e 2^22 + 2^23 rounded down = 2^23 + floor(e 2^22) exactly (results are integers there);
+//   lo = e 2^44 - floor(e 2^22) 2^22 is exact in one fma and lies in [0, 2^22); adding 2^23 rounds
+//        it to the nearest integer, ties to even.
+// hi 2^22 is an even integer, so adding it back cannot change the direction of a tie.
+struct Fixed44 {
+    uint32_t hi, lo;
+};
+__device__ __forceinline__ Fixed44 fixed44_parts(float e)
+{
+    const float t = __fadd_rd(e * 0x1p22f, 0x1p23f);
+    const float rem = __fmaf_rn(-__fsub_rn(t, 0x1p23f), 0x1p22f, e * 0x1p44f);
+    Fixed44 f;
+    f.hi = __float_as_uint(t) - 0x4B000000u;
+    f.lo = __float_as_uint(__fadd_rn(rem, 0x1p23f)) - 0x4B000000u;
+    return f;
+}
+__device__ __forceinline__ uint64_t fixed44(float e)
+{
+    const Fixed44 f = fixed44_parts(e);
+    return ((uint64_t)f.hi << 22) + f.lo;
+}
+
 // Fixed-point mass of a token: round(exp(-d) * 2^44) as an integer.  Sums of these are exact,
 // order-independent and deterministic; a row of up to 2^20 tokens cannot overflow 64 bits.
-__device__ __forceinline__ uint64_t qmass_d(float d)
-{
-    const float e = expf(-d);
-    return __float2ull_rn(e * 0x1p44f);
-}
+__device__ __forceinline__ uint64_t qmass_d(float d) { return fixed44(expf(-d)); }
 
 // min-p survival, p_i >= min_p * p_max, i.e. exp(-(zmax - z) / T) >= min_p.  Decided in float
 // away from the cut, and in double (the same operations as the float64 definition) within a
