@@ -320,7 +320,11 @@ def main():
 
 
 def latency_b1(args, dev, calls=300):
-    """p50/p90 device time of one call at B=1 (same V and dtype), stream-ordered, events per call."""
+    """B=1 latency at the same V and dtype (the decode distribution), two ways:
+    - graph: one call captured in a CUDA graph and replayed back to back; the interval between
+      consecutive events is the device time of one call (launch to completion, no host gap);
+    - isolated: event, Python call, event, synchronize -- includes the host-side marshalling of the
+      call, i.e. what one unbatched request sees end to end on an idle GPU."""
     import nucleus_token_sampler_gb300 as tps
     from nucleus_token_sampler_gb300 import workloads
     dt = torch.float32 if args.dtype == "f32" else torch.bfloat16
@@ -329,7 +333,13 @@ def latency_b1(args, dev, calls=300):
     s = torch.cuda.current_stream(dev)
     for i in range(20):
         tps.sample(w.logits, w.temperature, w.top_k, w.top_p, w.min_p, w.seed, i, out=tok)
-    ts = []
+    torch.cuda.synchronize()
+
+    def pct(ts):
+        ts = sorted(ts)
+        return round(ts[len(ts) // 2], 2), round(ts[int(len(ts) * 0.9)], 2), round(ts[min(len(ts) - 1, int(len(ts) * 0.99))], 2)
+
+    iso = []
     for i in range(calls):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
@@ -337,10 +347,34 @@ def latency_b1(args, dev, calls=300):
         tps.sample(w.logits, w.temperature, w.top_k, w.top_p, w.min_p, w.seed, i, out=tok)
         b.record(s)
         b.synchronize()
-        ts.append(a.elapsed_time(b) * 1e3)
-    ts.sort()
-    return {"p50_us": round(ts[len(ts) // 2], 2), "p90_us": round(ts[int(len(ts) * 0.9)], 2),
-            "calls": calls, "cluster_size": tps.cluster_size(dt, 1, args.V)}
+        iso.append(a.elapsed_time(b) * 1e3)
+    out = {"cluster_size": tps.cluster_size(dt, 1, args.V), "calls": calls}
+    out["isolated_p50_us"], out["isolated_p90_us"], out["isolated_p99_us"] = pct(iso)
+    try:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                tps.sample(w.logits, w.temperature, w.top_k, w.top_p, w.min_p, w.seed, 12345, out=tok)
+        s.wait_stream(side)
+        for _ in range(20):
+            g.replay()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(calls + 1)]
+        ev[0].record(s)
+        for i in range(calls):
+            g.replay()
+            ev[i + 1].record(s)
+        torch.cuda.synchronize()
+        gt = [ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(calls)]
+        out["p50_us"], out["p90_us"], out["p99_us"] = pct(gt)
+        out["method"] = "CUDA graph replays back to back; events between replays"
+    except Exception as e:  # graph capture unavailable: report the isolated numbers only
+        out["graph_error"] = str(e)[:200]
+        out["p50_us"], out["p90_us"], out["p99_us"] = out["isolated_p50_us"], out["isolated_p90_us"], out["isolated_p99_us"]
+        out["method"] = "isolated calls"
+    return out
 
 
 def e2e(args, w, dev, world, steps=None):

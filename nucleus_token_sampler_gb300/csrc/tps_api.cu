@@ -74,7 +74,7 @@ uint32_t slice_cap_bytes(int64_t V, int es, int C)
 // Slice, shared state, and the cluster-wide fine histogram.
 size_t smem_bytes(uint32_t slice_cap)
 {
-    return (size_t)slice_cap + sizeof(tps::Shared) + (size_t)tps::kFineBins * sizeof(uint32_t);
+    return (size_t)slice_cap + sizeof(tps::Shared) + 2 * (size_t)tps::kFineBins * sizeof(uint32_t);
 }
 
 // Choose the cluster size: the smallest C whose slice fits the preferred size, widened for small

@@ -19,8 +19,9 @@ namespace cg = cooperative_groups;
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kFineBins = 1024;       // count bins over d, width 1/32 (last bin: d >= 1023/32)
-constexpr float kFineScale = 32.f;
+constexpr int kFineBins = 512;        // count bins over d, width 1/16 (last bin: d >= 511/16)
+constexpr float kFineScale = 16.f;
+constexpr int kRaceQueue = 64;        // per-warp queue of vectors with tokens to race
 constexpr int kSubBins = 128;         // sub-bins over a key interval (exact refinement)
 constexpr int kMaxWin = 32;           // groups of fine bins in a top-p window
 constexpr int kCand = 256;            // candidates resolved by sorting, per CTA and per cluster
@@ -71,7 +72,6 @@ struct Shared {
     uint32_t ra[kWarps];
     uint32_t rb[kWarps];
     uint64_t r64[kWarps];
-    double rd[kWarps];
     ArgBest rab[kWarps];
     uint32_t bu[8];
     uint64_t b64[4];
@@ -81,8 +81,9 @@ struct Shared {
     uint32_t goff[16];
     uint32_t gcnt[16];
     uint32_t gtotal;
-    // --- fine count histogram over d of this CTA's survivors (read by the other CTAs)
-    alignas(16) uint32_t hc[kFineBins];
+    // --- fine histogram over d of this CTA's survivors (read by the other CTAs): counts in
+    //     hc[0, kFineBins), sums of the positions inside the bins (units of 2^-16 bin) after them
+    alignas(16) uint32_t hc[2 * kFineBins];
     // --- top-p window: this CTA's exact mass and count per group (read by the other CTAs), and
     //     the cluster's sums
     uint64_t wmass[kMaxWin];
@@ -100,6 +101,7 @@ struct Shared {
             uint64_t sbuf[kCand];
             uint64_t pre[kCand + 1];
         } cd;
+        uint32_t rq[kWarps][kRaceQueue];  // race queues: vector index | (token mask << 24)
     } u;
     // --- this CTA's candidate list (read by the other CTAs)
     uint32_t ncand;
@@ -217,29 +219,6 @@ __device__ __forceinline__ uint64_t block_exscan_u64(uint64_t v, Shared& s, uint
     return before + x - v;
 }
 
-__device__ __forceinline__ double block_exscan_f64(double v, Shared& s, double* total)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    double x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-        if (lane >= o) x += y;
-    }
-    cta_sync();
-    if (lane == 31) s.rd[warp] = x;
-    cta_sync();
-    double before = 0.0, all = 0.0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        const double t = s.rd[w];
-        if (w < warp) before += t;
-        all += t;
-    }
-    *total = all;
-    return before + (x - v);
-}
-
 // ---------------------------------------------------------------------------------------------
 // Topologies: the CTAs that share one row.  ClusterTopo is a thread-block cluster exchanging
 // through distributed shared memory; SoloTopo is a single CTA (map() is the identity).
@@ -247,7 +226,7 @@ __device__ __forceinline__ double block_exscan_f64(double v, Shared& s, double* 
 struct ClusterTopo {
     cg::cluster_group g;
     uint32_t C, rank;
-    uint32_t* hr = nullptr;  // cluster-wide fine histogram (kFineBins counts, set by the kernel)
+    uint32_t* hr = nullptr;  // cluster-wide fine histogram (2 * kFineBins words, set by the kernel)
     __device__ __forceinline__ uint32_t* fine(Shared&) { return hr; }
     __device__ __forceinline__ ClusterTopo() : g(cg::this_cluster())
     {
@@ -280,6 +259,7 @@ struct SoloTopo {
 // ---------------------------------------------------------------------------------------------
 template <typename TIn, bool kGlobal>
 struct VecSource {
+    static constexpr int kEPV = Elem<TIn>::kPerVec;
     const uint4* vec;  // kGlobal: the row's aligned interior in global memory; else a shared slice
     int nvec;
     int64_t elem0;     // row index of the first element of vec[0]
@@ -294,7 +274,7 @@ struct VecSource {
     __device__ __forceinline__ void for_each(const Shared& s, F&& f) const
     {
         using E = Elem<TIn>;
-        constexpr int U = 4;
+        constexpr int U = kGlobal ? 4 : 1;  // global rows: four loads in flight; shared: short loop body
         int v = threadIdx.x;
         for (; v + (U - 1) * kThreads < nvec; v += U * kThreads) {
             uint4 w[U];
@@ -318,9 +298,42 @@ struct VecSource {
         }
         for (int x = threadIdx.x; x < s.nx; x += kThreads) f(s.xz[x], s.xi[x]);
     }
+
+    // Vector by vector with a trip count that is the same for every lane of a warp (a lane past
+    // the end gets ok = false), four vectors loaded at a time from global memory: fv(z[kEPV], v,
+    // ok); then the ragged elements through fx(z, i).  fv may use warp-wide collectives.
+    template <typename FV, typename FX>
+    __device__ __forceinline__ void for_each_vec(const Shared& s, FV&& fv, FX&& fx) const
+    {
+        using E = Elem<TIn>;
+        constexpr int U = kGlobal ? 4 : 1;
+        const int lane = threadIdx.x & 31;
+        for (int vb = (int)threadIdx.x - lane; vb < nvec; vb += U * kThreads) {
+            uint4 w[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int v = vb + u * kThreads + lane;
+                w[u] = (v < nvec) ? load(v) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int v = vb + u * kThreads + lane;
+                float z[kEPV];
+                E::unpack(w[u], z);
+                fv(z, v, v < nvec);
+            }
+        }
+        for (int x = threadIdx.x; x < s.nx; x += kThreads) fx(s.xz[x], s.xi[x]);
+    }
 };
 template <typename TIn>
 using Slice = VecSource<TIn, false>;
+template <typename Src>
+struct ElemOf;
+template <typename TIn, bool kG>
+struct ElemOf<VecSource<TIn, kG>> {
+    using type = TIn;
+};
 template <typename TIn>
 using GlobalRow = VecSource<TIn, true>;
 
@@ -394,6 +407,13 @@ __device__ __forceinline__ int fine_bin(float d32)
     return (int)(__float_as_uint(__fadd_rd(c, 0x1p23f)) - 0x4B000000u);
 }
 
+// Position of d32 inside its bin b (b <= d32 < b + 1, so d32 - b is exact) in units of 2^-16,
+// rounded to nearest: 0 .. 65536.
+__device__ __forceinline__ uint32_t bin_pos16(float d32, int b)
+{
+    return __float_as_uint(__fmaf_rn(d32 - (float)b, 65536.f, 0x1p23f)) - 0x4B000000u;
+}
+
 // Cluster-wide sum of the CTAs' fine histograms hc into hr (a copy for a cluster of one CTA; nothing
 // to do when hr is hc itself).
 // Starts with a topology barrier: every CTA's histogram and published values are then complete,
@@ -403,7 +423,7 @@ __device__ __forceinline__ void reduce_fine(Topo& topo, Shared& s, uint32_t* hr)
 {
     topo.sync();
     if (topo.C > 1) {
-        for (int v = threadIdx.x; v < kFineBins / 4; v += kThreads) {
+        for (int v = threadIdx.x; v < 2 * kFineBins / 4; v += kThreads) {
             uint4 acc = make_uint4(0u, 0u, 0u, 0u);
             for (uint32_t q = 0; q < topo.C; ++q) {
                 const uint4 x = *reinterpret_cast<const uint4*>(topo.map(&s.hc[4 * v], q));
@@ -416,27 +436,27 @@ __device__ __forceinline__ void reduce_fine(Topo& topo, Shared& s, uint32_t* hr)
         }
         cta_sync();
     } else if (hr != s.hc) {  // a cluster of one CTA keeps its sums apart like a wider one
-        for (int v = threadIdx.x; v < kFineBins / 4; v += kThreads)
+        for (int v = threadIdx.x; v < 2 * kFineBins / 4; v += kThreads)
             reinterpret_cast<uint4*>(hr)[v] = reinterpret_cast<const uint4*>(s.hc)[v];
         cta_sync();
     }
 }
 
 // Top-k on the fine counts: the last non-empty bin b with (count above b) < K, and that count.
-// Thread t owns bins 4t .. 4t+3 (kFineBins == 4 * kThreads).
+// Thread t owns bins 2t and 2t+1 (kFineBins == 2 * kThreads).
 __device__ __forceinline__ void fine_scan_topk(Shared& s, const uint32_t* hr, uint64_t K, int* out_b, uint64_t* out_c)
 {
     const int t = threadIdx.x;
-    const uint4 c4 = reinterpret_cast<const uint4*>(hr)[t];
-    const uint32_t c[4] = {c4.x, c4.y, c4.z, c4.w};
+    const uint2 c2 = reinterpret_cast<const uint2*>(hr)[t];
+    const uint32_t c[2] = {c2.x, c2.y};
     uint64_t tot;
-    const uint64_t pre = block_exscan_u64((uint64_t)c4.x + c4.y + c4.z + c4.w, s, &tot);
+    const uint64_t pre = block_exscan_u64((uint64_t)c2.x + c2.y, s, &tot);
     uint32_t best = 0;
     uint64_t cum = pre, at = 0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 2; ++j) {
         if (c[j] > 0 && cum < K) {
-            best = (uint32_t)(4 * t + j) + 1u;
+            best = (uint32_t)(2 * t + j) + 1u;
             at = cum;
         }
         cum += c[j];
@@ -449,15 +469,19 @@ __device__ __forceinline__ void fine_scan_topk(Shared& s, const uint32_t* hr, ui
     cta_sync();
 }
 
-// The bins of d where the top-p crossing can lie, from the survivor counts alone.  c_b = hr[b] for
-// b < bk, `part` for b == bk, 0 above.  A token of bin b has d in [b, b+1)/32, so its fixed-point
-// mass / 2^44 lies within [e^-(b+1)/32, e^-b/32] up to expf's error and the rounding (the last bin:
-// [0, e^-1023/32]); margins of 1e-5 relative and 2^-44 absolute cover both.  With the masses above
-// bin b bounded by [cum_lo(b), cum_hi(b)] and Z by [Zlo, Zhi], the crossing (the last bin whose
-// mass above is below P Z) is a bin b with cum_lo(b) < P Zhi and cum_hi(b+1) >= P Zlo; every bin
-// before the first such bin is certainly kept.  The window's bins are split into at most kMaxWin
-// groups of 2^sh bins; `list` is set when the window and everything above it holds at most kCand
-// tokens.
+// The bins of d where the top-p crossing can lie, from the fine histogram alone.  A token of bin b
+// has d = (b + t) / 16 with t in [0, 1); its mass e^-d lies between (convexity of e^-x) the tangent
+// value at the bin's mean position and the chord across the bin:
+//   n e^-b/16 e^-mean(t)/16  <=  sum over the bin  <=  n e^-b/16 (1 - (1 - e^-1/16) mean(t)),
+// a relative gap below 5e-4.  mean(t) comes from the summed positions (to 2^-17 per token; a bin
+// with 65536 or more tokens, or the partial bin bk, uses t in [0, 1]; the last bin [0, e^-511/16]).
+// Margins of 4e-6 relative and one unit per token cover expf's error and the fixed-point rounding,
+// and the bounds are summed as exact 64-bit fixed-point integers.  With the mass above bin b within
+// [cum_lo(b), cum_hi(b)] and Z within [Zlo, Zhi], the crossing (the last bin whose mass above is
+// below P Z) is a bin b with cum_lo(b) < P Zhi and cum_hi(b+1) >= P Zlo; every bin before the first
+// such bin is certainly kept.  c_b = counts of S: hr[b] below bk, `part` at bk, 0 above.  The
+// window's bins form at most kMaxWin groups of 2^sh bins; `list` is set when the window and
+// everything above it hold at most kCand tokens.
 struct Window {
     int b_lo, b_end, sh, nw;
     bool list;
@@ -465,36 +489,49 @@ struct Window {
 __device__ __forceinline__ Window top_p_window(Shared& s, const uint32_t* hr, int bk, uint32_t part, float P)
 {
     const int t = threadIdx.x;
-    uint32_t c[4];
-    double lo[4], hi[4];
-    double slo = 0.0, shi = 0.0;
+    const float kChord = 1.f - expf(-1.f / kFineScale);
+    uint32_t c[2];
+    uint64_t lo[2], hi[2];
     uint32_t last = 0;  // 1 + the last non-empty bin of this thread
-    float eb = expf(-(float)(4 * t) * (1.f / kFineScale));
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int b = 4 * t + j;
-        c[j] = (b < bk) ? hr[b] : (b == bk ? part : 0u);
-        const float en = (b == kFineBins - 1) ? 0.f : expf(-(float)(b + 1) * (1.f / kFineScale));
-        lo[j] = (double)c[j] * fmax(0.0, (double)en * (1.0 - 1e-5) - 0x1p-44);
-        hi[j] = (double)c[j] * ((double)eb * (1.0 + 1e-5) + 0x1p-44);
-        eb = en;
-        slo += lo[j];
-        shi += hi[j];
-        if (c[j]) last = (uint32_t)b + 1u;
+    for (int j = 0; j < 2; ++j) {
+        const int b = 2 * t + j;
+        const uint32_t n = (b < bk) ? hr[b] : (b == bk ? part : 0u);
+        c[j] = n;
+        lo[j] = hi[j] = 0;
+        if (n == 0) continue;
+        last = (uint32_t)b + 1u;
+        const float eb = expf(-(float)b * (1.f / kFineScale));
+        float mlo = 0.f, mhi = 1.f;  // bounds of the mean position
+        if (b < bk && b < kFineBins - 1 && n < 65536u) {
+            const float F = (float)hr[kFineBins + b], nf = (float)n;
+            mlo = fmaxf(0.f, (F - 0.5f * nf) / (65536.f * nf) - 1e-6f);
+            mhi = fminf(1.f, (F + 0.5f * nf) / (65536.f * nf) + 1e-6f);
+        }
+        float el = 0.f, eh;
+        if (b < kFineBins - 1) {
+            el = eb * expf(-mhi * (1.f / kFineScale)) * (1.f - 4e-6f);
+            eh = eb * (1.f - kChord * mlo) * (1.f + 4e-6f);
+        } else {
+            eh = eb * (1.f + 4e-6f);
+        }
+        const uint64_t ql = fixed44(fminf(el, 1.f)), qh = fixed44(fminf(eh, 1.f));
+        lo[j] = (uint64_t)n * (ql > 0 ? ql - 1 : 0);
+        hi[j] = (uint64_t)n * (qh + 1);
     }
-    double Zlo, Zhi;
-    const double plo = block_exscan_f64(slo, s, &Zlo);
-    const double phi = block_exscan_f64(shi, s, &Zhi);
-    const double tlo = (double)P * Zlo, thi = (double)P * Zhi;
+    uint64_t Zlo, Zhi;
+    const uint64_t plo = block_exscan_u64(lo[0] + lo[1], s, &Zlo);
+    const uint64_t phi = block_exscan_u64(hi[0] + hi[1], s, &Zhi);
+    const double tlo = (double)P * (double)Zlo, thi = (double)P * (double)Zhi;
     uint32_t b0 = (uint32_t)kFineBins, b1 = 0;
-    double cl = plo, ch = phi;
+    uint64_t cl = plo, ch = phi;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t b = (uint32_t)(4 * t + j);
-        if (cl < thi) b1 = b;
+    for (int j = 0; j < 2; ++j) {
+        const uint32_t b = (uint32_t)(2 * t + j);
+        if ((double)cl < thi) b1 = b;
         cl += lo[j];
         ch += hi[j];
-        if (ch >= tlo && b0 == (uint32_t)kFineBins) b0 = b;
+        if ((double)ch >= tlo && b0 == (uint32_t)kFineBins) b0 = b;
     }
     b0 = block_min_u32(b0, s);
     b1 = block_max_u32(b1, s);
@@ -504,8 +541,8 @@ __device__ __forceinline__ Window top_p_window(Shared& s, const uint32_t* hr, in
     if (b1 < b0) b1 = b0;
     uint32_t upto = 0;  // tokens of S in bins <= b1
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-        if ((uint32_t)(4 * t + j) <= b1) upto += c[j];
+    for (int j = 0; j < 2; ++j)
+        if ((uint32_t)(2 * t + j) <= b1) upto += c[j];
     upto = block_sum_u32(upto, s);
     Window w;
     w.b_lo = (int)b0;
@@ -714,18 +751,20 @@ struct RaceCtx {
 
 __device__ __forceinline__ float race_u(const RaceCtx& rc, int32_t i)
 {
-    const uint4 x = philox4x32_10(make_uint4((uint32_t)i >> 2, rc.row, rc.s_lo, rc.s_hi), rc.k0, rc.k1);
+    const uint4 x = philox_block(make_uint4((uint32_t)i >> 2, rc.row, rc.s_lo, rc.s_hi), rc.k0, rc.k1);
     return (float)uniform_grid(pick_word(x, (uint32_t)i & 3u)) * 0x1p-24f;
 }
 
 __device__ __forceinline__ float race_key32(float d, float u) { return -d - logf(-logf(u)); }
 
-__device__ __forceinline__ double race_key64(const RowCtx& r, float z, float u)
+// The race key in double precision (the float64 definition), out of line: only near-ties need it.
+__device__ __noinline__ double race_key64_(float zmax, float T, float z, float u)
 {
-    const double d = __ddiv_rn(__dsub_rn((double)r.zmax, (double)z), (double)r.T);
+    const double d = __ddiv_rn(__dsub_rn((double)zmax, (double)z), (double)T);
     const double g = log(-log((double)u));
     return __dsub_rn(-d, g);
 }
+__device__ __forceinline__ double race_key64(const RowCtx& r, float z, float u) { return race_key64_(r.zmax, r.T, z, u); }
 
 // Margin between the float race key and the double one (both tokens' errors), for a row whose
 // kept tokens have d <= dcut.
@@ -1334,10 +1373,61 @@ struct RaceAcc {
         const uint32_t c = (uint32_t)i >> 2;
         if (c != ctr) {
             ctr = c;
-            x = philox4x32_10(make_uint4(c, rc.row, rc.s_lo, rc.s_hi), rc.k0, rc.k1);
+            x = philox_block(make_uint4(c, rc.row, rc.s_lo, rc.s_hi), rc.k0, rc.k1);
         }
         const float u = (float)uniform_grid(pick_word(x, (uint32_t)i & 3u)) * 0x1p-24f;
         t2.add(race_key32(d, u), i);
+    }
+};
+
+// Per-warp queue of vectors holding tokens to race, so that the Philox blocks and logarithms run
+// for full warps: a lane queues (vector, token mask) when it finds tokens to race, and every 32
+// queued vectors are raced one per lane.  Any lane may race any token: a token skipped against some
+// lane's second-best key cannot be among the two best of the row.
+template <typename Src>
+struct RaceQueue {
+    uint32_t* q;  // this warp's kRaceQueue entries: vector | (mask << 24)
+    uint32_t n;   // queued entries (the same in every lane)
+    __device__ __forceinline__ explicit RaceQueue(Shared& s) : q(s.u.rq[threadIdx.x >> 5]), n(0) {}
+    __device__ __forceinline__ void run(const Src& src, const RowCtx& r, const RaceCtx& rc, RaceAcc& race, uint32_t cnt)
+    {
+        const uint32_t lane = threadIdx.x & 31;
+        if (lane < cnt) {
+            const uint32_t e = q[lane];
+            const int v = (int)(e & 0xFFFFFFu);
+            const uint32_t mask = e >> 24;
+            float z[Src::kEPV];
+            Elem<typename ElemOf<Src>::type>::unpack(src.load(v), z);
+            const int32_t i0 = (int32_t)src.elem0 + v * Src::kEPV;
+#pragma unroll
+            for (int j = 0; j < Src::kEPV; ++j)
+                if ((mask >> j) & 1u) race.add(rc, dist(r, z[j]), i0 + j);
+        }
+    }
+    // Every lane calls this for its vector v (mask 0: nothing to race).
+    __device__ __forceinline__ void push(const Src& src, const RowCtx& r, const RaceCtx& rc, RaceAcc& race, int v,
+                                         uint32_t mask)
+    {
+        const uint32_t lane = threadIdx.x & 31;
+        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, mask != 0u);
+        if (bal == 0u) return;
+        if (mask) q[n + __popc(bal & ((1u << lane) - 1u))] = (uint32_t)v | (mask << 24);
+        n += __popc(bal);
+        if (n >= 32u) {
+            __syncwarp();
+            run(src, r, rc, race, 32u);
+            __syncwarp();
+            if (lane + 32u < n) q[lane] = q[lane + 32u];
+            __syncwarp();
+            n -= 32u;
+        }
+    }
+    __device__ __forceinline__ void drain(const Src& src, const RowCtx& r, const RaceCtx& rc, RaceAcc& race)
+    {
+        __syncwarp();
+        run(src, r, rc, race, n);
+        __syncwarp();
+        n = 0;
     }
 };
 
@@ -1468,7 +1558,7 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
 
     // ---- A: fine counts of S0, the first kCand survivors listed
     topo.sync();  // nobody still reads the caller's lists or published values
-    for (int b = tid; b < kFineBins; b += kThreads) s.hc[b] = 0;
+    for (int b = tid; b < 2 * kFineBins; b += kThreads) s.hc[b] = 0;
     if (tid == 0) s.ncand = 0;
     cta_sync();
     uint32_t my_minkey = 0xFFFFFFFFu;
@@ -1479,7 +1569,10 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
         if (!minp_ok(r, z, d)) return;
         const uint32_t key = fkey(z);
         my_minkey = min(my_minkey, key);
-        atomicAdd(&s.hc[fine_bin(d * kFineScale)], 1u);
+        const float d32 = d * kFineScale;
+        const int b = fine_bin(d32);
+        atomicAdd(&s.hc[b], 1u);
+        if (b < kFineBins - 1) atomicAdd(&s.hc[kFineBins + b], bin_pos16(d32, b));
         if (!full) {
             const uint32_t slot = atomicAdd(&s.ncand, 1u);
             if (slot < (uint32_t)kCand) {
@@ -1503,8 +1596,8 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
     }
     uint32_t ns0 = 0;
     {
-        const uint4 c4 = reinterpret_cast<const uint4*>(hr)[tid];
-        ns0 = block_sum_u32(c4.x + c4.y + c4.z + c4.w, s);  // (its barriers publish bu[3])
+        const uint2 c2 = reinterpret_cast<const uint2*>(hr)[tid];
+        ns0 = block_sum_u32(c2.x + c2.y, s);  // (its barriers publish bu[3])
     }
     const uint32_t min_key = s.bu[3];
     RowResult res;
@@ -1580,16 +1673,31 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
         const uint32_t kc = res.key_cut;
         const bool sum_z = prow != nullptr && P >= 1.f;  // the kept mass, for the probabilities
         uint64_t zhi = 0, zlo = 0;
-        src.for_each(s, [&](float z, int32_t i) {
-            if (!((z > -INFINITY) && fkey(z) >= kc)) return;
+        RaceQueue<Src> rq(s);
+        auto kept = [&](float z) -> bool {  // kept; sums its mass when asked; true if it may race
+            if (!((z > -INFINITY) && fkey(z) >= kc)) return false;
             const float d = dist(r, z);
             if (sum_z) {
                 const Fixed44 f = fixed44_parts(expf(-d));
                 zhi += f.hi;
                 zlo += f.lo;
             }
-            race.add(rc, d, i);
-        });
+            return !(16.64f - d < race.t2.k2);
+        };
+        src.for_each_vec(
+            s,
+            [&](const float* z, int v, bool ok) {
+                uint32_t mask = 0;
+                if (ok)
+#pragma unroll
+                    for (int j = 0; j < Src::kEPV; ++j)
+                        if (kept(z[j])) mask |= 1u << j;
+                rq.push(src, r, rc, race, v, mask);
+            },
+            [&](float z, int32_t i) {
+                if (kept(z)) race.add(rc, dist(r, z), i);
+            });
+        rq.drain(src, r, rc, race);
         if (sum_z) {
             const uint64_t cta = block_sum_u64((zhi << 22) + zlo, s);
             if (tid == 0) s.pub_z = cta;
@@ -1635,12 +1743,14 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
         cta_sync();
         uint64_t zhi = 0, zlo = 0, ahi = 0, alo = 0;  // high (x 2^22) and low parts of the sums
         uint32_t ca = 0;
-        src.for_each(s, [&](float z, int32_t i) {
-            if (!(z > zc)) return;
+        RaceQueue<Src> rq(s);
+        // sums for one token; true when it is certainly kept and may race
+        auto one = [&](float z, int32_t i) -> bool {
+            if (!(z > zc)) return false;
             const uint32_t key = fkey(z);
-            if (key < key_k) return;
+            if (key < key_k) return false;
             const float d = dist(r, z);
-            if (!minp_ok(r, z, d)) return;
+            if (!minp_ok(r, z, d)) return false;
             const Fixed44 f = fixed44_parts(expf(-d));
             zhi += f.hi;
             zlo += f.lo;
@@ -1651,17 +1761,37 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
                     s.ckey[slot] = key;
                     s.cidx[slot] = (uint32_t)i;
                 }
-            } else if (d32 < flo) {  // certainly kept
+                return false;
+            }
+            if (d32 < flo) {  // certainly kept
                 ahi += f.hi;
                 alo += f.lo;
                 ++ca;
-                race.add(rc, d, i);
-            } else if (d32 < fend) {
+                return !(16.64f - d < race.t2.k2);
+            }
+            if (d32 < fend) {
                 const int g = (fine_bin(d32) - b_lo) >> sh;
                 atomicAdd((unsigned long long*)&s.wmass[g], (unsigned long long)(((uint64_t)f.hi << 22) + f.lo));
                 atomicAdd(&s.wcnt[g], 1u);
             }
-        });
+            return false;
+        };
+        src.for_each_vec(
+            s,
+            [&](const float* z, int v, bool ok) {
+                uint32_t mask = 0;
+                if (ok) {
+                    const int32_t i0 = (int32_t)src.elem0 + v * Src::kEPV;
+#pragma unroll
+                    for (int j = 0; j < Src::kEPV; ++j)
+                        if (one(z[j], i0 + j)) mask |= 1u << j;
+                }
+                rq.push(src, r, rc, race, v, mask);
+            },
+            [&](float z, int32_t i) {
+                if (one(z, i)) race.add(rc, dist(r, z), i);
+            });
+        rq.drain(src, r, rc, race);
         const uint64_t zc_ = block_sum_u64((zhi << 22) + zlo, s);
         const uint64_t ac_ = block_sum_u64((ahi << 22) + alo, s);
         const uint32_t cc_ = block_sum_u32(ca, s);
@@ -1766,12 +1896,28 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
     // race over the window's kept tokens (those above the window were raced in the exact pass)
     const uint32_t kc = res.key_cut;
     const float flo = (float)w.b_lo;
-    src.for_each(s, [&](float z, int32_t i) {
-        if (!((z > -INFINITY) && fkey(z) >= kc)) return;
-        const float d = dist(r, z);
-        if (d * kFineScale < flo) return;
-        race.add(rc, d, i);
-    });
+    {
+        RaceQueue<Src> rq(s);
+        auto in_window = [&](float z) -> bool {  // kept, not raced yet, may race
+            if (!((z > -INFINITY) && fkey(z) >= kc)) return false;
+            const float d = dist(r, z);
+            return !(d * kFineScale < flo) && !(16.64f - d < race.t2.k2);
+        };
+        src.for_each_vec(
+            s,
+            [&](const float* z, int v, bool ok) {
+                uint32_t mask = 0;
+                if (ok)
+#pragma unroll
+                    for (int j = 0; j < Src::kEPV; ++j)
+                        if (in_window(z[j])) mask |= 1u << j;
+                rq.push(src, r, rc, race, v, mask);
+            },
+            [&](float z, int32_t i) {
+                if (in_window(z)) race.add(rc, dist(r, z), i);
+            });
+        rq.drain(src, r, rc, race);
+    }
     res.token = race_finish(topo, s, src, r, rc, race.t2, kc);
     if (prow) write_probs(src, s, r, res.key_cut, res.zk, prow);
     return res;
