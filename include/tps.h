@@ -98,11 +98,22 @@ int tps_sample_ex(const void* logits, int dtype, int64_t B, int64_t V, int64_t l
                   float* out_probs, int32_t* out_status, float* out_cutoff, int32_t* out_kept,
                   void* stream);
 
-/* Which kernel samples the rows (tps_sample_kernel). */
+/*
+ * Which kernel samples the rows (tps_sample_kernel).
+ *   AUTO    the library's choice (what tps_sample uses): below 32 rows the cluster kernel; from 32
+ *           rows the batch is split -- the cluster kernel takes the rows that sample without min-p
+ *           (they need several passes over the row, which it makes on-chip), and the streaming
+ *           kernel, launched right behind it, takes every other row.  The split costs a few
+ *           microseconds when no row needs the cluster kernel.
+ *   CLUSTER every row by the cluster kernel (one cluster of up to 16 CTAs per row).
+ *   STREAM  every row by the streaming kernel (one CTA per SM, rows streamed through a ring); the
+ *           fastest choice for a batch whose rows all use min-p or are greedy, e.g. decode batches
+ *           with min-p set, and much slower for rows without min-p.
+ */
 typedef enum {
-    TPS_KERNEL_AUTO = 0,    /* the library's choice for the shape (what tps_sample uses)            */
-    TPS_KERNEL_CLUSTER = 1, /* one thread-block cluster per row, the row held in shared memory      */
-    TPS_KERNEL_STREAM = 2   /* one persistent CTA per SM, rows streamed through a ring of chunks     */
+    TPS_KERNEL_AUTO = 0,
+    TPS_KERNEL_CLUSTER = 1,
+    TPS_KERNEL_STREAM = 2
 } tps_kernel;
 
 /*

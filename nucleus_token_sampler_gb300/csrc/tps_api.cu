@@ -8,6 +8,7 @@
 // memory) spreads each row over up to 16 SMs for small batches.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <mutex>
@@ -38,6 +39,8 @@ struct DeviceInfo {
     // Largest dynamic shared memory per CTA seen to co-schedule a cluster of 9..16 CTAs, per dtype
     // (0 = not known yet).
     std::atomic<long> wide_ok[2][kMaxCluster + 1];
+    // Co-resident clusters per (dtype, cluster size): shared-memory bytes << 20 | count (0 = not known).
+    std::atomic<long> resident[2][kMaxCluster + 1];
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -71,10 +74,11 @@ uint32_t slice_cap_bytes(int64_t V, int es, int C)
     return (uint32_t)(((per * 16) + 127) / 128 * 128);
 }
 
-// Slice, shared state, and the cluster-wide fine histogram.
+// Slice, shared state, the cluster-wide fine histogram and the list of a pass's rows.
 size_t smem_bytes(uint32_t slice_cap)
 {
-    return (size_t)slice_cap + sizeof(tps::Shared) + 2 * (size_t)tps::kFineBins * sizeof(uint32_t);
+    return (size_t)slice_cap + sizeof(tps::Shared) + 2 * (size_t)tps::kFineBins * sizeof(uint32_t) +
+           (size_t)tps::kThreads * sizeof(int32_t);
 }
 
 // Choose the cluster size: the smallest C whose slice fits the preferred size, widened for small
@@ -142,8 +146,12 @@ static_assert((size_t)kStreamStages * kStreamChunk + sizeof(tps::Shared) + sizeo
 
 size_t stream_smem_bytes() { return (size_t)kStreamStages * kStreamChunk + sizeof(tps::Shared) + sizeof(tps::StreamState); }
 
+// The streaming kernel.  `dependent`: launched as a programmatic dependent of the preceding kernel
+// in the stream (the cluster kernel of a split batch), so its CTAs may start on SMs that kernel has
+// already released.
 template <typename TIn>
-cudaError_t launch_stream(const DeviceInfo& d, bool* attrs_done, const tps::Args& a, cudaStream_t stream)
+cudaError_t launch_stream(const DeviceInfo& d, bool* attrs_done, const tps::Args& a, bool dependent,
+                          cudaStream_t stream)
 {
     auto k = tps::stream_rows_kernel<TIn>;
     const size_t smem = stream_smem_bytes();
@@ -153,18 +161,53 @@ cudaError_t launch_stream(const DeviceInfo& d, bool* attrs_done, const tps::Args
         *attrs_done = true;
     }
     const int64_t grid = a.B < (int64_t)d.sms ? a.B : (int64_t)d.sms;
-    k<<<(unsigned)grid, tps::kStreamThreads, smem, stream>>>(a, kStreamStages, kStreamChunk);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(tps::kStreamThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = dependent ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k, a, (int)kStreamStages, (uint32_t)kStreamChunk);
 }
 
+// The cluster kernel over `nclusters` clusters of C CTAs.  `dependent`: launched as a programmatic
+// dependent of the preceding kernel in the stream (the streaming kernel of a split batch), so its
+// CTAs may start on SMs that kernel has already released.
 template <typename TIn>
-cudaError_t launch(const tps::Args& a, int C, size_t smem, cudaStream_t stream)
+cudaError_t launch(const tps::Args& a, int C, size_t smem, int64_t nclusters, bool dependent, cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(a.B * C), 1, 1);
+    cfg.gridDim = dim3((unsigned)(nclusters * C), 1, 1);
     cfg.blockDim = dim3(tps::kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = dependent ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, tps::sample_rows_kernel<TIn>, a);
+}
+
+// Clusters of C CTAs the device holds at once (at least 1), asked once per (dtype, C, shared memory).
+template <typename TIn>
+int64_t resident_clusters(DeviceInfo& d, int dt, int C, size_t smem)
+{
+    std::atomic<long>& slot = d.resident[dt][C];
+    const long known = slot.load();
+    if (known > 0 && (size_t)(known >> 20) == smem) return known & 0xFFFFF;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)C, 1, 1);
+    cfg.blockDim = dim3(tps::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)C;
@@ -172,7 +215,14 @@ cudaError_t launch(const tps::Args& a, int C, size_t smem, cudaStream_t stream)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tps::sample_rows_kernel<TIn>, a);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tps::sample_rows_kernel<TIn>, &cfg) != cudaSuccess || n < 1) {
+        (void)cudaGetLastError();
+        n = 1;
+    }
+    if (n > 0xFFFFF) n = 0xFFFFF;
+    slot.store(((long)smem << 20) | (long)n);
+    return n;
 }
 
 int fail_cuda(cudaError_t e)
@@ -250,11 +300,15 @@ int tps_sample_kernel(const void* logits, int dtype, int64_t B, int64_t V, int64
 
     DeviceInfo* d = nullptr;
     if (!device_info(&d)) return fail_cuda(cudaGetLastError());
+    const int Cfit = choose_cluster(*d, es, B, V);
     const bool use_stream = kernel == TPS_KERNEL_STREAM || (kernel == TPS_KERNEL_AUTO && B >= kStreamMinRows) ||
-                            (kernel == TPS_KERNEL_AUTO && choose_cluster(*d, es, B, V) == 0);
-    const int C = use_stream ? 1 : choose_cluster(*d, es, B, V);
+                            (kernel == TPS_KERNEL_AUTO && Cfit == 0);
+    // A large batch is split: the streaming kernel takes the rows with min-p (and greedy and failed
+    // rows), the cluster kernel, launched right behind it, the rows that need the general path.
+    const bool split = kernel == TPS_KERNEL_AUTO && use_stream && Cfit != 0;
+    const int C = use_stream ? (split ? Cfit : 1) : Cfit;
     if (C == 0) return TPS_ERR_UNSUPPORTED_V;
-    const uint32_t cap = use_stream ? 0u : slice_cap_bytes(V, es, C);
+    const uint32_t cap = (use_stream && !split) ? 0u : slice_cap_bytes(V, es, C);
     const size_t smem = smem_bytes(cap);
 
     tps::Args a;
@@ -274,12 +328,13 @@ int tps_sample_kernel(const void* logits, int dtype, int64_t B, int64_t V, int64
     a.out_cutoff = out_cutoff;
     a.out_kept = out_kept;
     a.slice_cap = cap;
+    a.route = split ? tps::kRouteCluster : tps::kRouteAll;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (use_stream) {
-        e = (dtype == TPS_F32) ? launch_stream<float>(*d, &d->sattrs_f32, a, st)
-                               : launch_stream<__nv_bfloat16>(*d, &d->sattrs_bf16, a, st);
+    if (use_stream && !split) {
+        e = (dtype == TPS_F32) ? launch_stream<float>(*d, &d->sattrs_f32, a, false, st)
+                               : launch_stream<__nv_bfloat16>(*d, &d->sattrs_bf16, a, false, st);
         if (e != cudaSuccess) return fail_cuda(e);
         return TPS_OK;
     }
@@ -300,7 +355,8 @@ int tps_sample_kernel(const void* logits, int dtype, int64_t B, int64_t V, int64
             d->attrs_f32 = true;
         }
         if (Cl > 8 && !wide_cluster_ok<float>(*d, 0, Cl, sm) && !use_portable()) return TPS_ERR_UNSUPPORTED_V;
-        e = launch<float>(a, Cl, sm, st);
+        const int64_t ncl = split ? std::min<int64_t>(B, resident_clusters<float>(*d, 0, Cl, sm)) : B;
+        e = launch<float>(a, Cl, sm, ncl, false, st);
     } else {
         if (!d->attrs_bf16) {
             e = prepare_kernel<__nv_bfloat16>(*d);
@@ -309,9 +365,17 @@ int tps_sample_kernel(const void* logits, int dtype, int64_t B, int64_t V, int64
         }
         if (Cl > 8 && !wide_cluster_ok<__nv_bfloat16>(*d, 1, Cl, sm) && !use_portable())
             return TPS_ERR_UNSUPPORTED_V;
-        e = launch<__nv_bfloat16>(a, Cl, sm, st);
+        const int64_t ncl = split ? std::min<int64_t>(B, resident_clusters<__nv_bfloat16>(*d, 1, Cl, sm)) : B;
+        e = launch<__nv_bfloat16>(a, Cl, sm, ncl, false, st);
     }
     if (e != cudaSuccess) return fail_cuda(e);
+    if (split) {  // the rest of the batch, behind the cluster kernel
+        a.route = tps::kRouteStream;
+        a.slice_cap = 0;
+        e = (dtype == TPS_F32) ? launch_stream<float>(*d, &d->sattrs_f32, a, true, st)
+                               : launch_stream<__nv_bfloat16>(*d, &d->sattrs_bf16, a, true, st);
+        if (e != cudaSuccess) return fail_cuda(e);
+    }
     return TPS_OK;
 }
 

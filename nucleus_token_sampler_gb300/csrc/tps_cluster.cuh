@@ -1,5 +1,7 @@
-// tps_cluster.cuh -- the cluster sampler: one thread-block cluster per row, the row held in the
-// cluster's shared memory.  Used when the batch is too small to fill the GPU with whole rows.
+// tps_cluster.cuh -- the cluster sampler: a thread-block cluster per row, the row held in the
+// cluster's shared memory.  Used when the batch is too small to fill the GPU with whole rows, and
+// for the rows without min-p of a large batch (next to the streaming kernel), whose general path
+// makes several passes over the row: on-chip here.
 //
 // Each of the C CTAs bulk-copies one contiguous 16-byte-aligned slice of the row from HBM into its
 // own shared memory (one read of the row, no multicast); the ragged head and tail of an unaligned
@@ -16,23 +18,20 @@
 namespace tps {
 
 // ---------------------------------------------------------------------------------------------
-// The kernel.  Grid: B * C CTAs in clusters of C along x; cluster q samples row q.
+// One row sampled by the cluster (every thread of every CTA of the cluster calls it with the same
+// row).  Returns false when a bounded wait gave up: the row is reported TIMEOUT and the caller must
+// not reuse the shared memory for another row.
 // ---------------------------------------------------------------------------------------------
 template <typename TIn>
-__global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
+__device__ __forceinline__ bool cluster_row(const Args& a, ClusterTopo& topo, Shared& s, unsigned char* dsmem,
+                                            int64_t row)
 {
     using E = Elem<TIn>;
     constexpr int EPV = E::kPerVec;
     constexpr int ES = E::kBytes;
-    extern __shared__ __align__(128) unsigned char dsmem[];
-
-    ClusterTopo topo;
     cg::cluster_group& cluster = topo.g;
     const uint32_t C = topo.C;
     const uint32_t rank = topo.rank;
-    const int64_t row = (int64_t)(blockIdx.x / C);
-    Shared& s = *reinterpret_cast<Shared*>(dsmem + a.slice_cap);
-    topo.hr = reinterpret_cast<uint32_t*>(dsmem + a.slice_cap + sizeof(Shared));  // cluster-wide fine counts
     const int tid = threadIdx.x;
     const uint32_t lane = tid & 31;
 
@@ -64,6 +63,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
     if (tid == 0) {
         s.nx = my_head + my_tail;
         if (bytes > 0) {
+            fence_proxy_async();  // the previous row's reads of this slice come first
             mbar_init(&s.mbar, 1);
             mbar_arrive_expect_tx(&s.mbar, bytes);
             const unsigned char* src = reinterpret_cast<const unsigned char*>(a0) + v_lo * 16;
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
         // A copy still in flight after a timeout must land before the shared memory is released.
         if (timed_out && bytes > 0) (void)mbar_wait_bounded(&s.mbar, 0, kWaitLimitNs);
         cluster.sync();
-        return;
+        return !cl_timeout;
     }
 
     // ---- greedy branch: lowest index of the maximum ("Implement batched top-p sampling with
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
             if (a.out_kept) a.out_kept[row] = 1;
         }
         cluster.sync();
-        return;
+        return true;
     }
 
     const RowCtx r = make_ctx(zmax, T, minp);
@@ -269,13 +269,61 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
         if (prow) write_probs(sl, s, r, key_cut, ZK, prow);
         if (writer) write_row(a, row, token, kRowOk, key_to_float(key_cut), (int32_t)NK);
         cluster_wait();  // every CTA has finished reading this CTA's lists
-        return;
+        return true;
     }
 
     // ================= general path: survivors against the global maximum =================
     const RowResult res = general_path(topo, s, sl, r, zc, topk_on, K, P, rc, prow);
     if (writer) write_row(a, row, res.token, kRowOk, key_to_float(res.key_cut), (int32_t)res.nk);
     topo.sync();  // keep this CTA's shared memory alive until every remote read is done
+    return true;
+}
+
+// A failed row's outputs (token -1, cutoff NaN, kept 0, zero probabilities); all CTA threads call it.
+__device__ __forceinline__ void fail_row(const Args& a, int64_t row, int32_t status)
+{
+    if (a.out_probs)
+        for (int64_t i = threadIdx.x; i < a.V; i += kThreads) a.out_probs[row * a.V + i] = 0.f;
+    if (threadIdx.x == 0) write_row(a, row, -1, status, __uint_as_float(0x7FC00000u), 0);
+}
+
+// ---------------------------------------------------------------------------------------------
+// The kernel.  Grid: ncl clusters of C CTAs along x; cluster q samples rows q, q + ncl, ...  With
+// a.route == kRouteAll every row is sampled (ncl = B: one row per cluster); with kRouteCluster
+// only the rows routed_to_cluster() selects, found by one parallel read of the rows' parameters
+// (the grid then holds as many clusters as the GPU keeps resident).
+// ---------------------------------------------------------------------------------------------
+template <typename TIn>
+__global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
+{
+    extern __shared__ __align__(128) unsigned char dsmem[];
+    ClusterTopo topo;
+    const uint32_t C = topo.C;
+    Shared& s = *reinterpret_cast<Shared*>(dsmem + a.slice_cap);
+    topo.hr = reinterpret_cast<uint32_t*>(dsmem + a.slice_cap + sizeof(Shared));  // cluster-wide fine counts
+    int32_t* rows = reinterpret_cast<int32_t*>(dsmem + a.slice_cap + sizeof(Shared) + 2 * kFineBins * sizeof(uint32_t));
+    const int64_t ncl = (int64_t)(gridDim.x / C), cid = (int64_t)(blockIdx.x / C);
+    const int tid = threadIdx.x;
+    // A kernel launched as this one's programmatic dependent (the streaming kernel of a split batch)
+    // may be scheduled from now on: it samples the other rows and waits for this grid before it exits.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    bool alive = true;
+    for (int64_t base = cid; base < a.B; base += (int64_t)kThreads * ncl) {
+        // this pass's rows: base + t * ncl for t < kThreads, kept in order
+        const int64_t r = base + (int64_t)tid * ncl;
+        bool mine = r < a.B;
+        if (mine && a.route == kRouteCluster) mine = routed_to_cluster(a.temperature[r], a.top_p[r], a.min_p[r]);
+        uint64_t total;
+        const uint32_t at = (uint32_t)block_exscan_u64(mine ? 1u : 0u, s, &total);
+        if (mine) rows[at] = (int32_t)r;
+        cta_sync();
+        for (uint32_t k = 0; k < (uint32_t)total; ++k) {
+            const int64_t row = rows[k];
+            if (alive) alive = cluster_row<TIn>(a, topo, s, dsmem, row);
+            else if (topo.rank == 0) fail_row(a, row, kRowTimeout);
+        }
+        cta_sync();  // rows[] is rewritten by the next pass
+    }
 }
 
 }  // namespace tps

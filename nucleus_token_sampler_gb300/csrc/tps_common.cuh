@@ -45,7 +45,21 @@ struct Args {
     float* out_cutoff;
     int32_t* out_kept;
     uint32_t slice_cap;  // bytes reserved for the slice at the start of dynamic shared memory
+    uint32_t route;      // which rows the kernel samples (RowRoute)
 };
+
+// Which rows a kernel samples.  A large batch is split between the two kernels: the streaming
+// kernel takes every row but those routed_to_cluster() selects, which the cluster kernel takes.
+enum RowRoute : uint32_t { kRouteAll = 0, kRouteStream = 1, kRouteCluster = 2 };
+
+// Rows left to the cluster kernel in a split batch: sampling with min-p off.  They need the general
+// path, which takes several passes over the row: on-chip in the cluster kernel, from global memory
+// in the streaming kernel.  (Failed parameters, greedy rows and min-p rows stay with the streaming
+// kernel.)
+__device__ __forceinline__ bool routed_to_cluster(float T, float P, float MP)
+{
+    return isfinite(T) && isfinite(P) && isfinite(MP) && T > 0.f && !(MP > 0.f);
+}
 
 struct Shared {
     uint64_t mbar;

@@ -147,6 +147,12 @@ __device__ __forceinline__ RaceCtx race_ctx(const Args& a, int64_t row, uint64_t
     return rc;
 }
 
+// Whether this kernel leaves the row to the cluster kernel (a split batch).
+__device__ __forceinline__ bool skip_row(const Args& a, int64_t row)
+{
+    return a.route == kRouteStream && routed_to_cluster(a.temperature[row], a.top_p[row], a.min_p[row]);
+}
+
 // The scanners' block-wide handling of one queued row (all kThreads scanner threads call it).
 template <typename TIn>
 __device__ void run_task(const Args& a, Shared& s, const Task& t, uint32_t chunk_bytes)
@@ -242,7 +248,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
     if (warp == kProducerWarp) {
         if (lane == 0) {
             uint64_t g = 0;
+            bool skip_next = skip_row(a, first);
             for (int64_t row = first; row < B && !*vdead; row += stride) {
+                const bool skip = skip_next;
+                if (row + stride < B) skip_next = skip_row(a, row + stride);
+                if (skip) continue;
                 const RowGeom geo = row_geom<ES>(a, row, chunk_bytes);
                 for (int c = 0; c < geo.nchunks; ++c, ++g) {
                     const int stage = (int)(g % (uint64_t)nstage);
@@ -282,8 +292,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
             __threadfence_block();
             *(volatile uint32_t*)&st.q_tail = tail + 1;
         };
-        int64_t j = 0;
-        for (int64_t row = first; row < B; row += stride, ++j) {
+        int64_t j = 0;  // rows of this CTA sampled so far
+        for (int64_t row = first; row < B; row += stride) {
+            if (skip_row(a, row)) continue;
             const int sl = (int)(j & 1);
             RowSlot& slot = st.slot[sl];
             bool ok = mbar_wait_bounded(&st.slot_full[sl], (uint32_t)((j >> 1) & 1), kWaitLimitNs);
@@ -372,6 +383,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
                 mbar_arrive(&st.slot_free[sl]);
             }
             __syncwarp();
+            ++j;
         }
         if (lane == 0) {
             __threadfence_block();
@@ -400,10 +412,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
 
     uint64_t g = 0;  // chunks consumed, in the producer's order
     RowParams nxt = load_params(a, first);
-    int64_t j = 0;
-    for (int64_t row = first; row < B; row += stride, ++j) {
+    int64_t j = 0;  // rows of this CTA sampled so far
+    for (int64_t row = first; row < B; row += stride) {
         const RowParams p = nxt;
         if (row + stride < B) nxt = load_params(a, row + stride);  // prefetched one row ahead
+        if (a.route == kRouteStream && routed_to_cluster(p.T, p.P, p.MP)) continue;
         drain();
         const int sl = (int)(j & 1);
         RowSlot& slot = st.slot[sl];
@@ -484,6 +497,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
             __threadfence_block();
             mbar_arrive(&st.slot_full[sl]);
         }
+        ++j;
     }
     // keep taking queued rows until the resolver has finished every row
     const uint64_t t0 = globaltimer_ns();
@@ -513,6 +527,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
             (void)mbar_wait_bounded(&st.full[q % (uint64_t)nstage], (uint32_t)((q / (uint64_t)nstage) & 1u),
                                     kWaitLimitNs);
     }
+    // Launched as the programmatic dependent of the cluster kernel (a split batch): this CTA -- so
+    // this grid -- completes only after that kernel has, so later work in the stream sees both.
+    // A no-op for an ordinary launch.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace tps

@@ -20,7 +20,7 @@ pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA device")]
 
 
-KERNELS = ["cluster", "stream"]
+KERNELS = ["cluster", "stream", "auto"]  # auto: a batch of 32+ rows is split between the two kernels
 
 
 def check(w, rows=None, want_probs=True, logits=None, max_band_frac=0.05, kernels=KERNELS):
