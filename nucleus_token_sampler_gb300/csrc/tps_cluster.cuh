@@ -172,7 +172,7 @@ __device__ __forceinline__ bool cluster_row(const Args& a, ClusterTopo& topo, Sh
     cta_sync();
     const float zmax = s.bf[0];
     const uint32_t cl_timeout = s.bu[0];
-    const bool lists_complete = (s.bu[1] == 0) && (s.gtotal <= (uint32_t)kCand);
+    const bool lists_complete = s.bu[1] == 0;  // every CTA listed all its candidates
 
     int32_t status = kRowOk;
     if (cl_timeout) status = kRowTimeout;
@@ -242,25 +242,28 @@ __device__ __forceinline__ bool cluster_row(const Args& a, ClusterTopo& topo, Sh
 
     if (lists_complete) {
         // ================= fast path: every survivor is on some CTA's list =================
-        // Gather the lists (one entry per thread), keep the survivors of min-p against the global
-        // maximum.  This is the last read of another CTA's shared memory.
+        // Gather the lists, keeping the survivors of min-p against the global maximum (the lists
+        // were cut against each CTA's own maximum, so they may be longer).  Every CTA gathers the
+        // same union, so all take the same branch below.
         if (tid == 0) s.ncand = 0;
         cta_sync();
         const uint32_t total = s.gtotal;
-        if ((uint32_t)tid < total) {
+        for (uint32_t e = (uint32_t)tid; e < total; e += kThreads) {
             uint32_t rr = 0;
-            while (rr + 1 < C && s.goff[rr + 1] <= (uint32_t)tid) ++rr;
-            const uint32_t off = (uint32_t)tid - s.goff[rr];
+            while (rr + 1 < C && s.goff[rr + 1] <= e) ++rr;
+            const uint32_t off = e - s.goff[rr];
             const uint32_t key = *cluster.map_shared_rank(&s.ckey[off], rr);
             const uint32_t idx = *cluster.map_shared_rank(&s.cidx[off], rr);
             const float z = key_to_float(key);
             if (z > zc && minp_ok(r, z, dist(r, z))) {
                 const uint32_t slot = atomicAdd(&s.ncand, 1u);
-                s.u.cd.sbuf[slot] = sb_make(key, idx);
+                if (slot < (uint32_t)kCand) s.u.cd.sbuf[slot] = sb_make(key, idx);
             }
         }
-        cluster_arrive();  // no more remote reads by this CTA; waited for just before exit
         cta_sync();
+    }
+    if (lists_complete && s.ncand <= (uint32_t)kCand) {
+        cluster_arrive();  // no more remote reads by this CTA; waited for just before exit
         const uint32_t n = s.ncand;
         const RowResult res = resolve_candidates(s, r, rc, n, topk_on, K, P);
         const uint32_t key_cut = res.key_cut;
@@ -273,6 +276,7 @@ __device__ __forceinline__ bool cluster_row(const Args& a, ClusterTopo& topo, Sh
     }
 
     // ================= general path: survivors against the global maximum =================
+    // (also when more than kCand listed tokens survive; its first barrier is a cluster barrier)
     const RowResult res = general_path(topo, s, sl, r, zc, topk_on, K, P, rc, prow);
     if (writer) write_row(a, row, res.token, kRowOk, key_to_float(res.key_cut), (int32_t)res.nk);
     topo.sync();  // keep this CTA's shared memory alive until every remote read is done
