@@ -299,7 +299,8 @@ def main():
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32" if args.dtype == "f32" else "bf16", "data": "synthetic",
-            "config": workload_config(args), "roofline": roof, "gpu_launches": args.steps,
+            "config": workload_config(args), "roofline": roof,
+            "gpu_launches": args.steps * tps.kernels_per_call(w.logits.dtype, B, V, args.kernel),
             "hbm_gbs": round(achieved, 1), "us_per_step": round(1e3 * ms_per_step, 2),
             "wall_s_timed": round(t_wall, 3), "cluster_size": tps.cluster_size(w.logits.dtype, B, V)}
     if clk:

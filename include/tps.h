@@ -127,6 +127,10 @@ int tps_sample_kernel(const void* logits, int dtype, int64_t B, int64_t V, int64
                       float* out_probs, int32_t* out_status, float* out_cutoff, int32_t* out_kept,
                       int kernel, void* stream);
 
+/* Kernels one tps_sample_kernel call with these arguments launches (1 or 2; 0 for arguments the call
+ * would reject).  Host-only query. */
+int tps_kernels_per_call(int dtype, int64_t B, int64_t V, int kernel);
+
 /* Largest V the library accepts for `dtype` on the current device (0 for an unknown dtype or
  * when no device is usable); the exact 64-bit mass sums bound it at 2^20 - 1.  Host-only query;
  * enqueues nothing. */

@@ -15,7 +15,7 @@ import threading
 import torch
 
 __all__ = ["build", "load", "sample", "TPS_F32", "TPS_BF16", "ROW_STATUS", "library_path", "max_vocab",
-           "cluster_size", "version"]
+           "cluster_size", "kernels_per_call", "version"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _CSRC = os.path.join(_HERE, "csrc")
@@ -77,6 +77,8 @@ def load():
             lib.tps_max_vocab.argtypes = [I32]
             lib.tps_cluster_size.restype = I32
             lib.tps_cluster_size.argtypes = [I32, I64, I64]
+            lib.tps_kernels_per_call.restype = I32
+            lib.tps_kernels_per_call.argtypes = [I32, I64, I64, I32]
             lib.tps_status_string.restype = ctypes.c_char_p
             lib.tps_status_string.argtypes = [I32]
             lib.tps_last_cuda_error.restype = I32
@@ -97,6 +99,11 @@ def max_vocab(dtype: torch.dtype = torch.float32) -> int:
 
 def cluster_size(dtype: torch.dtype, B: int, V: int) -> int:
     return int(load().tps_cluster_size(_dtype_code(dtype), B, V))
+
+
+def kernels_per_call(dtype: torch.dtype, B: int, V: int, kernel: str = "auto") -> int:
+    """Kernels one call launches for this shape and kernel choice (1, or 2 for a split batch)."""
+    return int(load().tps_kernels_per_call(_dtype_code(dtype), B, V, KERNELS[kernel]))
 
 
 def _dtype_code(dt: torch.dtype) -> int:

@@ -269,6 +269,19 @@ int64_t tps_max_vocab(int dtype)
     return kMaxVocabMass;
 }
 
+int tps_kernels_per_call(int dtype, int64_t B, int64_t V, int kernel)
+{
+    const int es = elem_bytes(dtype);
+    if (!es || V < 1 || B < 0 || V > kMaxVocabMass || kernel < TPS_KERNEL_AUTO || kernel > TPS_KERNEL_STREAM) return 0;
+    if (B == 0) return 0;
+    DeviceInfo* d = nullptr;
+    if (!device_info(&d)) return 0;
+    const int Cfit = choose_cluster(*d, es, B, V);
+    if (kernel == TPS_KERNEL_CLUSTER) return Cfit ? 1 : 0;
+    if (kernel == TPS_KERNEL_STREAM) return 1;
+    return (B >= kStreamMinRows && Cfit != 0) ? 2 : 1;  // auto: a large batch is split over both kernels
+}
+
 int tps_cluster_size(int dtype, int64_t B, int64_t V)
 {
     const int es = elem_bytes(dtype);

@@ -65,3 +65,12 @@ def test_argument_validation(kw, rc):
 def test_empty_batch_is_a_noop():
     # B = 0 returns OK before touching any pointer or the GPU.
     assert call(B=0, logits=None, T=None, K=None, P=None, M=None, S=None, out=None) == 0
+
+
+def test_kernels_per_call_rejects_bad_arguments():
+    lib = tps.load()
+    assert lib.tps_kernels_per_call(7, 4, 100, 0) == 0      # unknown dtype
+    assert lib.tps_kernels_per_call(0, -1, 100, 0) == 0     # negative B
+    assert lib.tps_kernels_per_call(0, 4, 0, 0) == 0        # empty vocabulary
+    assert lib.tps_kernels_per_call(0, 4, 100, 9) == 0      # unknown kernel
+    assert lib.tps_kernels_per_call(0, 0, 100, 0) == 0      # an empty batch launches nothing

@@ -205,3 +205,12 @@ def test_empty_batch(kernel):
     e = torch.empty(0, device="cuda")
     out = tps.sample(x, e, e.int(), e, e, e.long(), kernel=kernel)
     assert out.shape == (0,)
+
+
+@pytest.mark.gpu
+def test_kernels_per_call_follows_the_split_rule():
+    f32 = torch.float32
+    assert tps.kernels_per_call(f32, 1024, 128256, "auto") == 2   # a large batch is split over both kernels
+    assert tps.kernels_per_call(f32, 1024, 128256, "stream") == 1
+    assert tps.kernels_per_call(f32, 1024, 128256, "cluster") == 1
+    assert tps.kernels_per_call(f32, 8, 32000, "auto") == 1       # a small batch: the cluster kernel alone
