@@ -74,11 +74,11 @@ uint32_t slice_cap_bytes(int64_t V, int es, int C)
     return (uint32_t)(((per * 16) + 127) / 128 * 128);
 }
 
-// Slice, shared state, the cluster-wide fine histogram and the list of a pass's rows.
+// Slice, shared state, the cluster-wide fine histogram, the list of a pass's rows and the exchange inbox.
 size_t smem_bytes(uint32_t slice_cap)
 {
     return (size_t)slice_cap + sizeof(tps::Shared) + 2 * (size_t)tps::kFineBins * sizeof(uint32_t) +
-           (size_t)tps::kThreads * sizeof(int32_t);
+           (size_t)tps::kThreads * sizeof(int32_t) + sizeof(tps::Inbox);
 }
 
 // Choose the cluster size: the smallest C whose slice fits the preferred size, widened for small

@@ -17,14 +17,26 @@
 
 namespace tps {
 
+// Per-CTA inbox of the cluster exchange: slot q holds CTA q's maximum, timeout flag, list size
+// (0xFFFFFFFF: no complete list) and, for lists of at most kInbox tokens, the listed tokens.
+constexpr int kInbox = 64;
+constexpr int kMaxClusterCTAs = 16;
+struct Inbox {
+    float max[kMaxClusterCTAs];
+    uint32_t timeout[kMaxClusterCTAs];
+    uint32_t cnt[kMaxClusterCTAs];
+    uint32_t key[kMaxClusterCTAs][kInbox];
+    uint32_t idx[kMaxClusterCTAs][kInbox];
+};
+
 // ---------------------------------------------------------------------------------------------
 // One row sampled by the cluster (every thread of every CTA of the cluster calls it with the same
 // row).  Returns false when a bounded wait gave up: the row is reported TIMEOUT and the caller must
 // not reuse the shared memory for another row.
 // ---------------------------------------------------------------------------------------------
 template <typename TIn>
-__device__ __forceinline__ bool cluster_row(const Args& a, ClusterTopo& topo, Shared& s, unsigned char* dsmem,
-                                            int64_t row)
+__device__ __forceinline__ bool cluster_row(const Args& a, ClusterTopo& topo, Shared& s, Inbox* inbox,
+                                            unsigned char* dsmem, int64_t row)
 {
     using E = Elem<TIn>;
     constexpr int EPV = E::kPerVec;
@@ -132,20 +144,34 @@ __device__ __forceinline__ bool cluster_row(const Args& a, ClusterTopo& topo, Sh
             nlisted = s.ncand;
         }
     }
-    if (tid == 0) {
-        s.pub_max = mloc;
-        s.pub_timeout = timed_out;
-        s.pub_nsurv = nlisted;  // 0xFFFFFFFF or > kCand: this CTA's list is not complete
-        s.pub_gcnt = min(nlisted, (uint32_t)kCand);
+    if (tid == 0) s.pub_gcnt = min(nlisted, (uint32_t)kCand);
+    // Push this CTA's maximum, timeout flag, list size and (a list of at most kInbox tokens) the
+    // listed tokens into slot `rank` of every CTA's inbox: after the barrier each CTA has the whole
+    // exchange in its own shared memory (longer lists are read remotely after the barrier).
+    {
+        const uint32_t np = (nlisted <= (uint32_t)kInbox) ? nlisted : 0u;
+        const uint32_t per = np + 1u, items = C * per;
+        for (uint32_t it = (uint32_t)tid; it < items; it += kThreads) {
+            const uint32_t d = it / per, i = it - d * per;
+            Inbox* ib = cluster.map_shared_rank(inbox, d);
+            if (i == np) {
+                ib->max[rank] = mloc;
+                ib->timeout[rank] = timed_out;
+                ib->cnt[rank] = nlisted;
+            } else {
+                ib->key[rank][i] = s.ckey[i];
+                ib->idx[rank][i] = s.cidx[i];
+            }
+        }
     }
     cluster.sync();
     if (tid < 32) {
         float m = -INFINITY;
         uint32_t to = 0, nl = 0, cnt = 0, bad = 0;
         if (lane < C) {
-            m = *cluster.map_shared_rank(&s.pub_max, lane);
-            to = *cluster.map_shared_rank(&s.pub_timeout, lane);
-            nl = *cluster.map_shared_rank(&s.pub_nsurv, lane);
+            m = inbox->max[lane];
+            to = inbox->timeout[lane];
+            nl = inbox->cnt[lane];
             bad = nl > (uint32_t)kCand;
             cnt = bad ? 0u : nl;
         }
@@ -252,8 +278,9 @@ __device__ __forceinline__ bool cluster_row(const Args& a, ClusterTopo& topo, Sh
             uint32_t rr = 0;
             while (rr + 1 < C && s.goff[rr + 1] <= e) ++rr;
             const uint32_t off = e - s.goff[rr];
-            const uint32_t key = *cluster.map_shared_rank(&s.ckey[off], rr);
-            const uint32_t idx = *cluster.map_shared_rank(&s.cidx[off], rr);
+            const bool local = inbox->cnt[rr] <= (uint32_t)kInbox;  // pushed before the barrier
+            const uint32_t key = local ? inbox->key[rr][off] : *cluster.map_shared_rank(&s.ckey[off], rr);
+            const uint32_t idx = local ? inbox->idx[rr][off] : *cluster.map_shared_rank(&s.cidx[off], rr);
             const float z = key_to_float(key);
             if (z > zc && minp_ok(r, z, dist(r, z))) {
                 const uint32_t slot = atomicAdd(&s.ncand, 1u);
@@ -306,12 +333,17 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
     Shared& s = *reinterpret_cast<Shared*>(dsmem + a.slice_cap);
     topo.hr = reinterpret_cast<uint32_t*>(dsmem + a.slice_cap + sizeof(Shared));  // cluster-wide fine counts
     int32_t* rows = reinterpret_cast<int32_t*>(dsmem + a.slice_cap + sizeof(Shared) + 2 * kFineBins * sizeof(uint32_t));
+    Inbox* inbox = reinterpret_cast<Inbox*>(reinterpret_cast<unsigned char*>(rows) + kThreads * sizeof(int32_t));
     const int64_t ncl = (int64_t)(gridDim.x / C), cid = (int64_t)(blockIdx.x / C);
     const int tid = threadIdx.x;
     // A kernel launched as this one's programmatic dependent (the streaming kernel of a split batch)
     // may be scheduled from now on: it samples the other rows and waits for this grid before it exits.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     bool alive = true;
+    if (a.route == kRouteAll && ncl >= a.B) {  // one row per cluster: no list to build
+        if (cid < a.B) (void)cluster_row<TIn>(a, topo, s, inbox, dsmem, cid);
+        return;
+    }
     for (int64_t base = cid; base < a.B; base += (int64_t)kThreads * ncl) {
         // this pass's rows: base + t * ncl for t < kThreads, kept in order
         const int64_t r = base + (int64_t)tid * ncl;
@@ -323,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
         cta_sync();
         for (uint32_t k = 0; k < (uint32_t)total; ++k) {
             const int64_t row = rows[k];
-            if (alive) alive = cluster_row<TIn>(a, topo, s, dsmem, row);
+            if (alive) alive = cluster_row<TIn>(a, topo, s, inbox, dsmem, row);
             else if (topo.rank == 0) fail_row(a, row, kRowTimeout);
         }
         cta_sync();  // rows[] is rewritten by the next pass
