@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--no-latency", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--kernel", default="auto", choices=["auto", "cluster", "stream"])
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the sweep grid (B x V x dtype, sweep workload) and print one JSON table instead")
     return ap.parse_args()
 
 
@@ -228,10 +230,59 @@ def workload_config(args):
                 args.B * args.V * (4 if args.dtype == "f32" else 2) / 1e6)}
 
 
+def run_sweep(args):
+    """The sweep grid: every B x V x dtype point of the sweep workload (top-p ~ U[.1, 1], T ~ U[.3, 2],
+    no top-k, no min-p), timed like the main run (warm-up, then CUDA events around args.steps calls)
+    through the chosen kernel; inputs larger than L2 are not flushed, smaller ones are re-read from
+    L2 (a point's `l2` field says which).  Prints one JSON object with a row per point."""
+    import nucleus_token_sampler_gb300 as tps
+    from nucleus_token_sampler_gb300 import workloads
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    tps.load()
+    peak, peak_kind = measured_peaks()
+    rows = []
+    for dt_name, dt in (("f32", torch.float32), ("bf16", torch.bfloat16)):
+        es = 4 if dt == torch.float32 else 2
+        for V in workloads.SWEEP_V:
+            for B in workloads.SWEEP_B:
+                w = workloads.make("sweep", device=dev, B=B, V=V, dtype=dt)
+                out = {"token": torch.empty(B, dtype=torch.int32, device=dev)}
+
+                def call(i):
+                    tps.sample(w.logits, w.temperature, w.top_k, w.top_p, w.min_p, w.seed, i, out=out, kernel=args.kernel)
+
+                for i in range(args.warmup):
+                    call(i)
+                torch.cuda.synchronize()
+                s = torch.cuda.current_stream(dev)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+                for i in range(args.steps):
+                    call(args.warmup + i)
+                e1.record(s)
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1) / args.steps
+                alg = B * (V * es + ROW_PARAM_BYTES)
+                gbs = alg / (ms / 1e3) / 1e9
+                rows.append({"dtype": dt_name, "B": B, "V": V, "us_per_step": round(ms * 1e3, 2),
+                             "rows_per_s": round(B / (ms / 1e3), 1), "gbs": round(gbs, 1),
+                             "frac": round(gbs / peak, 4), "kernels": tps.kernels_per_call(dt, B, V, args.kernel),
+                             "l2": "larger than L2" if B * V * es > 129e6 else "fits L2 (re-read)"})
+                del w, out
+                torch.cuda.empty_cache()
+    print(json.dumps({"sweep": rows, "kernel": args.kernel, "steps": args.steps, "warmup": args.warmup,
+                      "peak_gbs": peak, "peak_kind": peak_kind,
+                      "workload": "sweep: logits ~ N(0, 2^2), top_p ~ U[.1, 1], T ~ U[.3, 2], no top-k, no min-p"}))
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
     import nucleus_token_sampler_gb300 as tps
 
     rank, world, local = dist_env()
