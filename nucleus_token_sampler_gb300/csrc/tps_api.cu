@@ -2,10 +2,13 @@
 // choice, and the launch.  No allocation, no host synchronisation, no state kept between calls
 // beyond a per-device cache of queried limits.
 //
-// Two kernels sample the rows.  The streaming kernel (one persistent CTA per SM, rows streamed
-// through a ring of bulk-copied chunks) is used when the batch can occupy the GPU with whole rows;
-// the cluster kernel (one thread-block cluster per row, the row held in the cluster's shared
-// memory) spreads each row over up to 16 SMs for small batches.
+// Two kernels sample the rows.  The cluster kernel (a thread-block cluster per row, the row held in
+// the cluster's shared memory) spreads each row over up to 16 SMs; it samples small batches.  The
+// streaming kernel (one persistent CTA per SM, rows streamed through a ring of bulk-copied chunks)
+// reads each row once at HBM speed and resolves rows with min-p (and greedy rows) on the fly.  A
+// large batch is split: the cluster kernel takes the rows without min-p, whose general path makes
+// several passes over the row, and the streaming kernel, launched behind it as its programmatic
+// dependent, takes the rest.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -174,26 +177,22 @@ cudaError_t launch_stream(const DeviceInfo& d, bool* attrs_done, const tps::Args
     return cudaLaunchKernelEx(&cfg, k, a, (int)kStreamStages, (uint32_t)kStreamChunk);
 }
 
-// The cluster kernel over `nclusters` clusters of C CTAs.  `dependent`: launched as a programmatic
-// dependent of the preceding kernel in the stream (the streaming kernel of a split batch), so its
-// CTAs may start on SMs that kernel has already released.
+// The cluster kernel over `nclusters` clusters of C CTAs.
 template <typename TIn>
-cudaError_t launch(const tps::Args& a, int C, size_t smem, int64_t nclusters, bool dependent, cudaStream_t stream)
+cudaError_t launch(const tps::Args& a, int C, size_t smem, int64_t nclusters, cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(nclusters * C), 1, 1);
     cfg.blockDim = dim3(tps::kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = dependent ? 2 : 1;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, tps::sample_rows_kernel<TIn>, a);
 }
 
@@ -369,7 +368,7 @@ int tps_sample_kernel(const void* logits, int dtype, int64_t B, int64_t V, int64
         }
         if (Cl > 8 && !wide_cluster_ok<float>(*d, 0, Cl, sm) && !use_portable()) return TPS_ERR_UNSUPPORTED_V;
         const int64_t ncl = split ? std::min<int64_t>(B, resident_clusters<float>(*d, 0, Cl, sm)) : B;
-        e = launch<float>(a, Cl, sm, ncl, false, st);
+        e = launch<float>(a, Cl, sm, ncl, st);
     } else {
         if (!d->attrs_bf16) {
             e = prepare_kernel<__nv_bfloat16>(*d);
@@ -379,7 +378,7 @@ int tps_sample_kernel(const void* logits, int dtype, int64_t B, int64_t V, int64
         if (Cl > 8 && !wide_cluster_ok<__nv_bfloat16>(*d, 1, Cl, sm) && !use_portable())
             return TPS_ERR_UNSUPPORTED_V;
         const int64_t ncl = split ? std::min<int64_t>(B, resident_clusters<__nv_bfloat16>(*d, 1, Cl, sm)) : B;
-        e = launch<__nv_bfloat16>(a, Cl, sm, ncl, false, st);
+        e = launch<__nv_bfloat16>(a, Cl, sm, ncl, st);
     }
     if (e != cudaSuccess) return fail_cuda(e);
     if (split) {  // the rest of the batch, behind the cluster kernel

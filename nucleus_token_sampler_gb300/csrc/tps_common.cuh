@@ -410,9 +410,6 @@ __device__ __forceinline__ float list_threshold(float m, float lt_hi)
     return m - (lt_hi + fabsf(m) * 0x1p-20f);
 }
 
-// d in fine-bin units: exactly kFineScale * dist(r, z) (a power-of-two scaling).
-__device__ __forceinline__ float dist_fine(const RowCtx& r, float z) { return dist(r, z) * kFineScale; }
-
 // Fine bin of a scaled distance d32 >= 0: floor(min(d32, kFineBins - 1)), with float adds only.
 // For every integer 1 <= b <= kFineBins - 1:  fine_bin(d32) < b  <=>  d32 < b.
 __device__ __forceinline__ int fine_bin(float d32)
