@@ -127,6 +127,19 @@ int tps_sample_kernel(const void* logits, int dtype, int64_t B, int64_t V, int64
                       float* out_probs, int32_t* out_status, float* out_cutoff, int32_t* out_kept,
                       int kernel, void* stream);
 
+/*
+ * tps_sample_full -- tps_sample_kernel plus the processed log-probability of the sampled token.
+ *
+ *   out_logprob  [B] float, or NULL: ln P(token) under the renormalised kept distribution (the one
+ *                out_probs holds), i.e. -(zmax - z_token)/T - ln(sum over kept i of e^{-(zmax - z_i)/T});
+ *                0 for greedy rows, NaN for failed rows.
+ * Every other argument is as in tps_sample_kernel.
+ */
+int tps_sample_full(const void* logits, int dtype, int64_t B, int64_t V, int64_t ld, const float* temperature,
+                    const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seed,
+                    uint64_t step, int32_t* out_token, float* out_probs, int32_t* out_status, float* out_cutoff,
+                    int32_t* out_kept, float* out_logprob, int kernel, void* stream);
+
 /* Kernels one tps_sample_kernel call with these arguments launches (1 or 2; 0 for arguments the call
  * would reject).  Host-only query. */
 int tps_kernels_per_call(int dtype, int64_t B, int64_t V, int kernel);

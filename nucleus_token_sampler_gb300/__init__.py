@@ -73,6 +73,8 @@ def load():
             lib.tps_sample_ex.argtypes = [P, I32, I64, I64, I64, P, P, P, P, P, U64, P, P, P, P, P, P]
             lib.tps_sample_kernel.restype = I32
             lib.tps_sample_kernel.argtypes = [P, I32, I64, I64, I64, P, P, P, P, P, U64, P, P, P, P, P, I32, P]
+            lib.tps_sample_full.restype = I32
+            lib.tps_sample_full.argtypes = [P, I32, I64, I64, I64, P, P, P, P, P, U64, P, P, P, P, P, P, I32, P]
             lib.tps_max_vocab.restype = I64
             lib.tps_max_vocab.argtypes = [I32]
             lib.tps_cluster_size.restype = I32
@@ -140,7 +142,8 @@ KERNELS = {"auto": 0, "cluster": 1, "stream": 2}
 
 
 def sample(logits: torch.Tensor, temperature, top_k, top_p, min_p, seed, step: int = 0, *,
-           want_probs: bool = False, diagnostics: bool = False, out=None, stream=None, kernel: str = "auto"):
+           want_probs: bool = False, diagnostics: bool = False, want_logprob: bool = False, out=None, stream=None,
+           kernel: str = "auto"):
     """Sample one token per row of ``logits`` ([B, V] float32/bfloat16 CUDA tensor; the row stride
     may exceed V).
 
@@ -150,6 +153,8 @@ def sample(logits: torch.Tensor, temperature, top_k, top_p, min_p, seed, step: i
     ``token``, ``status``, ``cutoff``, ``kept`` (and ``probs``) when ``diagnostics`` or
     ``want_probs`` is set.  Work is enqueued on ``stream`` (default: the current stream).
     ``kernel`` picks the sampler kernel ("auto", "cluster" or "stream"); results do not depend on it.
+    ``want_logprob`` adds ``logprob``: ln P(token) under the renormalised kept distribution (0 for
+    greedy rows, NaN for failed rows).
     """
     if not logits.is_cuda:
         raise ValueError("logits must be a CUDA tensor (the sampler has no CPU path)")
@@ -179,15 +184,21 @@ def sample(logits: torch.Tensor, temperature, top_k, top_p, min_p, seed, step: i
         cut = cut if cut is not None else torch.empty(B, dtype=torch.float32, device=dev)
         kept = res.get("kept", None)
         kept = kept if kept is not None else torch.empty(B, dtype=torch.int32, device=dev)
+    lp = None
+    if want_logprob:
+        lp = res.get("logprob", None)
+        lp = lp if lp is not None else torch.empty(B, dtype=torch.float32, device=dev)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     with torch.cuda.device(dev):
-        rc = load().tps_sample_kernel(_ptr(logits), code, B, V, ld, _ptr(T), _ptr(K), _ptr(P), _ptr(M), _ptr(S),
-                                      int(step) & ((1 << 64) - 1), _ptr(tok), _ptr(probs), _ptr(st), _ptr(cut),
-                                      _ptr(kept), KERNELS[kernel], ctypes.c_void_p(s.cuda_stream))
+        rc = load().tps_sample_full(_ptr(logits), code, B, V, ld, _ptr(T), _ptr(K), _ptr(P), _ptr(M), _ptr(S),
+                                    int(step) & ((1 << 64) - 1), _ptr(tok), _ptr(probs), _ptr(st), _ptr(cut),
+                                    _ptr(kept), _ptr(lp), KERNELS[kernel], ctypes.c_void_p(s.cuda_stream))
     _check(rc)
-    if not (diagnostics or want_probs):
+    if not (diagnostics or want_probs or want_logprob):
         return tok
     r = {"token": tok}
+    if want_logprob:
+        r["logprob"] = lp
     if diagnostics:
         r.update(status=st, cutoff=cut, kept=kept)
     if want_probs:

@@ -291,10 +291,10 @@ int tps_cluster_size(int dtype, int64_t B, int64_t V)
     return choose_cluster(*d, es, B, V);
 }
 
-int tps_sample_kernel(const void* logits, int dtype, int64_t B, int64_t V, int64_t ld, const float* temperature,
-                      const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seed,
-                      uint64_t step, int32_t* out_token, float* out_probs, int32_t* out_status, float* out_cutoff,
-                      int32_t* out_kept, int kernel, void* stream)
+int tps_sample_full(const void* logits, int dtype, int64_t B, int64_t V, int64_t ld, const float* temperature,
+                    const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seed,
+                    uint64_t step, int32_t* out_token, float* out_probs, int32_t* out_status, float* out_cutoff,
+                    int32_t* out_kept, float* out_logprob, int kernel, void* stream)
 {
     if (kernel < TPS_KERNEL_AUTO || kernel > TPS_KERNEL_STREAM) return TPS_ERR_ARG;
     if (B < 0 || V < 1 || ld < V) return TPS_ERR_ARG;
@@ -305,7 +305,7 @@ int tps_sample_kernel(const void* logits, int dtype, int64_t B, int64_t V, int64
     if (!aligned(logits, es) || !aligned(temperature, 4) || !aligned(top_k, 4) || !aligned(top_p, 4) ||
         !aligned(min_p, 4) || !aligned(seed, 8) || !aligned(out_token, 4) || (out_probs && !aligned(out_probs, 4)) ||
         (out_status && !aligned(out_status, 4)) || (out_cutoff && !aligned(out_cutoff, 4)) ||
-        (out_kept && !aligned(out_kept, 4)))
+        (out_kept && !aligned(out_kept, 4)) || (out_logprob && !aligned(out_logprob, 4)))
         return TPS_ERR_ALIGN;
     if (V > kMaxVocabMass || V > INT32_MAX) return TPS_ERR_UNSUPPORTED_V;
     if (B > (int64_t)INT32_MAX / kMaxCluster) return TPS_ERR_ARG;
@@ -339,6 +339,7 @@ int tps_sample_kernel(const void* logits, int dtype, int64_t B, int64_t V, int64
     a.out_status = out_status;
     a.out_cutoff = out_cutoff;
     a.out_kept = out_kept;
+    a.out_logprob = out_logprob;
     a.slice_cap = cap;
     a.route = split ? tps::kRouteCluster : tps::kRouteAll;
 
@@ -389,6 +390,15 @@ int tps_sample_kernel(const void* logits, int dtype, int64_t B, int64_t V, int64
         if (e != cudaSuccess) return fail_cuda(e);
     }
     return TPS_OK;
+}
+
+int tps_sample_kernel(const void* logits, int dtype, int64_t B, int64_t V, int64_t ld, const float* temperature,
+                      const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seed,
+                      uint64_t step, int32_t* out_token, float* out_probs, int32_t* out_status, float* out_cutoff,
+                      int32_t* out_kept, int kernel, void* stream)
+{
+    return tps_sample_full(logits, dtype, B, V, ld, temperature, top_k, top_p, min_p, seed, step, out_token, out_probs,
+                           out_status, out_cutoff, out_kept, nullptr, kernel, stream);
 }
 
 int tps_sample_ex(const void* logits, int dtype, int64_t B, int64_t V, int64_t ld, const float* temperature,

@@ -214,12 +214,7 @@ __device__ __forceinline__ bool cluster_row(const Args& a, ClusterTopo& topo, Sh
             for (int64_t i = sl.elem0 + tid; i < sl.elem0 + (int64_t)nvec * EPV; i += kThreads) prow[i] = 0.f;
             for (int x = tid; x < s.nx; x += kThreads) prow[s.xi[x]] = 0.f;
         }
-        if (writer) {
-            a.out_token[row] = -1;
-            if (a.out_status) a.out_status[row] = status;
-            if (a.out_cutoff) a.out_cutoff[row] = __uint_as_float(0x7FC00000u);
-            if (a.out_kept) a.out_kept[row] = 0;
-        }
+        if (writer) write_row(a, row, -1, status, __uint_as_float(0x7FC00000u), 0);
         // A copy still in flight after a timeout must land before the shared memory is released.
         if (timed_out && bytes > 0) (void)mbar_wait_bounded(&s.mbar, 0, kWaitLimitNs);
         cluster.sync();
@@ -244,12 +239,7 @@ __device__ __forceinline__ bool cluster_row(const Args& a, ClusterTopo& topo, Sh
         cta_sync();
         const uint32_t arg = s.bu[2];
         if (prow) sl.for_each(s, [&](float, int32_t i) { prow[i] = ((uint32_t)i == arg) ? 1.f : 0.f; });
-        if (writer) {
-            a.out_token[row] = (int32_t)arg;
-            if (a.out_status) a.out_status[row] = kRowOk;
-            if (a.out_cutoff) a.out_cutoff[row] = zmax;
-            if (a.out_kept) a.out_kept[row] = 1;
-        }
+        if (writer) write_row(a, row, (int32_t)arg, kRowOk, zmax, 1, 0.f);  // one-hot: ln P = 0
         cluster.sync();
         return true;
     }
@@ -297,15 +287,17 @@ __device__ __forceinline__ bool cluster_row(const Args& a, ClusterTopo& topo, Sh
         const uint64_t NK = res.nk, ZK = res.zk;
         const int32_t token = res.token;
         if (prow) write_probs(sl, s, r, key_cut, ZK, prow);
-        if (writer) write_row(a, row, token, kRowOk, key_to_float(key_cut), (int32_t)NK);
+        if (writer) write_row(a, row, token, kRowOk, key_to_float(key_cut), (int32_t)NK, token_logprob<TIn>(a, r, row, token, ZK));
         cluster_wait();  // every CTA has finished reading this CTA's lists
         return true;
     }
 
     // ================= general path: survivors against the global maximum =================
     // (also when more than kCand listed tokens survive; its first barrier is a cluster barrier)
-    const RowResult res = general_path(topo, s, sl, r, zc, topk_on, K, P, rc, prow);
-    if (writer) write_row(a, row, res.token, kRowOk, key_to_float(res.key_cut), (int32_t)res.nk);
+    const RowResult res = general_path(topo, s, sl, r, zc, topk_on, K, P, rc, prow, a.out_logprob != nullptr);
+    if (writer)
+        write_row(a, row, res.token, kRowOk, key_to_float(res.key_cut), (int32_t)res.nk,
+                  token_logprob<TIn>(a, r, row, res.token, res.zk));
     topo.sync();  // keep this CTA's shared memory alive until every remote read is done
     return true;
 }

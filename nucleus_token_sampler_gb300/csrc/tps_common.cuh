@@ -44,6 +44,7 @@ struct Args {
     int32_t* out_status;
     float* out_cutoff;
     int32_t* out_kept;
+    float* out_logprob;  // ln P(token) under the renormalised kept distribution, or null
     uint32_t slice_cap;  // bytes reserved for the slice at the start of dynamic shared memory
     uint32_t route;      // which rows the kernel samples (RowRoute)
 };
@@ -1560,7 +1561,7 @@ __device__ __forceinline__ uint64_t block_sum_u64(uint64_t v, Shared& s)
 // when it is entered.
 template <typename Topo, typename Src>
 __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const RowCtx& r, float zc, bool topk_on,
-                                  int32_t K, float P, const RaceCtx& rc, float* prow)
+                                  int32_t K, float P, const RaceCtx& rc, float* prow, bool need_zk = false)
 {
     const int tid = threadIdx.x;
     const uint32_t lane = tid & 31;
@@ -1682,7 +1683,7 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
             res.zk = 0;
         }
         const uint32_t kc = res.key_cut;
-        const bool sum_z = prow != nullptr && P >= 1.f;  // the kept mass, for the probabilities
+        const bool sum_z = (prow != nullptr || need_zk) && P >= 1.f;  // the kept mass (probabilities, log-probability)
         uint64_t zhi = 0, zlo = 0;
         RaceQueue<Src> rq(s);
         auto kept = [&](float z) -> bool {  // kept; sums its mass when asked; true if it may race
@@ -1934,14 +1935,36 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
     return res;
 }
 
-// Per-row outputs (thread 0 of the writing CTA).
+// Per-row outputs (one thread of the writing CTA).  logprob: ln P(token); NaN for a failed row.
 __device__ __forceinline__ void write_row(const Args& a, int64_t row, int32_t token, int32_t status, float cutoff,
-                                          int32_t kept)
+                                          int32_t kept, float logprob)
 {
     a.out_token[row] = token;
     if (a.out_status) a.out_status[row] = status;
     if (a.out_cutoff) a.out_cutoff[row] = cutoff;
     if (a.out_kept) a.out_kept[row] = kept;
+    if (a.out_logprob) a.out_logprob[row] = logprob;
+}
+__device__ __forceinline__ void write_row(const Args& a, int64_t row, int32_t token, int32_t status, float cutoff,
+                                          int32_t kept)
+{
+    write_row(a, row, token, status, cutoff, kept, __int_as_float(0x7FC00000));
+}
+
+// ln P(token) of a sampled row under the renormalised kept distribution: -(zmax - z)/T - ln(Z_kept)
+// in double, the token's logit z read back from the row and Z_kept = zk 2^-44 (the exact fixed-point
+// sum of the kept tokens' masses, relative to the maximum's).  Out of line: one call per row.
+__device__ __noinline__ float logprob_of(float zmax, float T, float z, uint64_t zk)
+{
+    const double dd = __ddiv_rn(__dsub_rn((double)zmax, (double)z), (double)T);
+    return (float)(-dd - (log((double)zk) - 44.0 * 0.69314718055994530942));
+}
+template <typename TIn>
+__device__ __forceinline__ float token_logprob(const Args& a, const RowCtx& r, int64_t row, int32_t token, uint64_t zk)
+{
+    if (!a.out_logprob) return 0.f;
+    const float z = Elem<TIn>::load1(static_cast<const unsigned char*>(a.logits) + row * a.ld * Elem<TIn>::kBytes, token);
+    return logprob_of(r.zmax, r.T, z, zk);
 }
 
 }  // namespace tps

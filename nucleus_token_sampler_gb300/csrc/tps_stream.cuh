@@ -191,7 +191,7 @@ __device__ void run_task(const Args& a, Shared& s, const Task& t, uint32_t chunk
         mi = block_min_u32(mi, s);
         if (prow)
             for (int64_t i = tid; i < a.V; i += kThreads) prow[i] = ((uint32_t)i == mi) ? 1.f : 0.f;
-        if (tid == 0) write_row(a, row, (int32_t)mi, kRowOk, zmax, 1);
+        if (tid == 0) write_row(a, row, (int32_t)mi, kRowOk, zmax, 1, 0.f);
         return;
     }
     const float minp = clamp_minp(p.MP);
@@ -204,8 +204,11 @@ __device__ void run_task(const Args& a, Shared& s, const Task& t, uint32_t chunk
     const float zc = minp_threshold(r);
     const bool topk_on = (p.K > 0) && ((int64_t)p.K < a.V);
     SoloTopo topo;
-    const RowResult res = general_path(topo, s, src, r, zc, topk_on, p.K, p.P, race_ctx(a, row, p.seed), prow);
-    if (tid == 0) write_row(a, row, res.token, kRowOk, key_to_float(res.key_cut), (int32_t)res.nk);
+    const RowResult res =
+        general_path(topo, s, src, r, zc, topk_on, p.K, p.P, race_ctx(a, row, p.seed), prow, a.out_logprob != nullptr);
+    if (tid == 0)
+        write_row(a, row, res.token, kRowOk, key_to_float(res.key_cut), (int32_t)res.nk,
+                  token_logprob<TIn>(a, r, row, res.token, res.zk));
 }
 
 template <typename TIn>
@@ -327,7 +330,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
                     for (uint32_t e = lane; e < nlisted; e += 32)
                         if (key_to_float(slot.lkey[e]) == zmax) mi = min(mi, slot.lidx[e]);
                     mi = __reduce_min_sync(0xFFFFFFFFu, mi);
-                    if (lane == 0) write_row(a, row, (int32_t)mi, kRowOk, zmax, 1);
+                    if (lane == 0) write_row(a, row, (int32_t)mi, kRowOk, zmax, 1, 0.f);
                 } else {
                     t.kind = kTaskGreedy;  // a pass over the row (also writes the one-hot row)
                 }
@@ -363,7 +366,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
                     const WarpResult wr = (n <= 32) ? warp_resolve(st.rbuf, r, rc, n, topk_on, p.K, p.P)
                                                     : warp_resolve_big(st.rbuf, st.rsorted, st.rpre, n, r, rc, topk_on,
                                                                        p.K, p.P);
-                    if (lane == 0) write_row(a, row, wr.token, kRowOk, key_to_float(wr.key_cut), (int32_t)wr.nk);
+                    if (lane == 0)
+                        write_row(a, row, wr.token, kRowOk, key_to_float(wr.key_cut), (int32_t)wr.nk,
+                                  token_logprob<TIn>(a, r, row, wr.token, wr.zk));
                     if (a.out_probs) {
                         t.kind = kTaskProbs;
                         t.key_cut = wr.key_cut;

@@ -9,13 +9,20 @@ import oracle
 
 TOPP_BAND, MINP_BAND, RACE_BAND = oracle.FLAG_TOPP_BAND, oracle.FLAG_MINP_BAND, oracle.FLAG_RACE_BAND
 PROB_TOL = 1e-5  # absolute, on renormalised probabilities
+# absolute, on ln P(token) (plus 1e-6 relative): the kept mass is an exact sum of float expf values
+# (relative error ~3e-7 -> ~3e-7 in the log) and the result is stored as a float (ulp 2e-6 at |ln P| = 30)
+LOGPROB_TOL = 1e-5
 
 
-def run_gpu(w, want_probs=True, logits=None, kernel="auto"):
+def run_gpu(w, want_probs=True, logits=None, kernel="auto", want_logprob=None):
+    """The library on the GPU.  The log-probability output is requested for the auto kernel (unless
+    want_logprob says otherwise), so the explicit kernels keep covering the path without it."""
     d = w.to("cuda")
     lg = d.logits if logits is None else logits
+    if want_logprob is None:
+        want_logprob = kernel == "auto"
     r = tps.sample(lg, d.temperature, d.top_k, d.top_p, d.min_p, d.seed, d.step, want_probs=want_probs,
-                   diagnostics=True, kernel=kernel)
+                   diagnostics=True, want_logprob=want_logprob, kernel=kernel)
     torch.cuda.synchronize()
     return {k: v.cpu() for k, v in r.items()}
 
@@ -58,6 +65,19 @@ def compare(w, g, o, rows=None, check_probs=True):
     bad = np.nonzero(tchk & (tok_g != o["token"]))[0]
     if len(bad):
         fails.append(f"token differs on {len(bad)} rows, e.g. row {rows[bad[0]]}: gpu {tok_g[bad[0]]} oracle {o['token'][bad[0]]}")
+    if "logprob" in g and "probs" in o:
+        # ln P(token) against the float64 oracle's renormalised probability of the same token
+        lp = g["logprob"].numpy()[rows].astype(np.float64)
+        m = okrow & ~tokband
+        if m.any():
+            ref = np.log(o["probs"][np.nonzero(m)[0], o["token"][m]])
+            err = np.abs(lp[m] - ref)
+            tol = LOGPROB_TOL + 1e-6 * np.abs(ref)
+            if (err > tol).any():
+                i = int(np.argmax(err - tol))
+                fails.append(f"logprob differs by {err[i]:.3e} at a row with ln P = {ref[i]:.6f}")
+        if (~okrow).any() and not np.isnan(lp[~okrow]).all():
+            fails.append("failed rows have a non-NaN logprob")
     maxdp = 0.0
     if check_probs and "probs" in g and "probs" in o:
         pg = g["probs"].numpy()[rows].astype(np.float64)

@@ -74,3 +74,12 @@ def test_kernels_per_call_rejects_bad_arguments():
     assert lib.tps_kernels_per_call(0, 4, 0, 0) == 0        # empty vocabulary
     assert lib.tps_kernels_per_call(0, 4, 100, 9) == 0      # unknown kernel
     assert lib.tps_kernels_per_call(0, 0, 100, 0) == 0      # an empty batch launches nothing
+
+
+def test_sample_full_checks_the_logprob_pointer():
+    lib = tps.load()
+    v = lambda p: None if p is None else ctypes.c_void_p(p)
+    # a misaligned out_logprob is rejected before anything is launched
+    rc = lib.tps_sample_full(v(FAKE), 0, 4, 100, 100, v(FAKE), v(FAKE), v(FAKE), v(FAKE), v(FAKE), 0, v(FAKE), None,
+                             None, None, None, v(FAKE + 2), 0, None)
+    assert rc == 4
