@@ -33,6 +33,11 @@ KERNEL_SOURCES = ["nucleus_token_sampler_gb300/csrc/tps_stream.cuh",
                   "nucleus_token_sampler_gb300/csrc/tps_cluster.cuh",
                   "nucleus_token_sampler_gb300/csrc/tps_common.cuh",
                   "nucleus_token_sampler_gb300/csrc/tps_device.cuh",
+                  "nucleus_token_sampler_gb300/csrc/tps_kernels.h",
+                  "nucleus_token_sampler_gb300/csrc/tps_k_stream_f32.cu",
+                  "nucleus_token_sampler_gb300/csrc/tps_k_stream_bf16.cu",
+                  "nucleus_token_sampler_gb300/csrc/tps_k_cluster_f32.cu",
+                  "nucleus_token_sampler_gb300/csrc/tps_k_cluster_bf16.cu",
                   "nucleus_token_sampler_gb300/csrc/tps_api.cu"]
 
 

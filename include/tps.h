@@ -127,18 +127,32 @@ int tps_sample_kernel(const void* logits, int dtype, int64_t B, int64_t V, int64
                       float* out_probs, int32_t* out_status, float* out_cutoff, int32_t* out_kept,
                       int kernel, void* stream);
 
+/* Most top tokens tps_sample_full reports per row. */
+#define TPS_MAX_TOP 32
+
 /*
- * tps_sample_full -- tps_sample_kernel plus the processed log-probability of the sampled token.
+ * tps_sample_full -- tps_sample_kernel plus processed log-probabilities: those of the sampled
+ * token and of the row's most probable kept tokens ("processed": under the renormalised kept
+ * distribution that out_probs holds, not the raw softmax).
  *
- *   out_logprob  [B] float, or NULL: ln P(token) under the renormalised kept distribution (the one
- *                out_probs holds), i.e. -(zmax - z_token)/T - ln(sum over kept i of e^{-(zmax - z_i)/T});
- *                0 for greedy rows, NaN for failed rows.
- * Every other argument is as in tps_sample_kernel.
+ *   out_logprob      [B] float, or NULL: ln P(token) = -(zmax - z_token)/T - ln(sum over kept i of
+ *                    e^{-(zmax - z_i)/T}); 0 for greedy rows, NaN for failed rows.
+ *   n_top            0 .. TPS_MAX_TOP top tokens per row (0: none, and the two pointers below are
+ *                    ignored); any other value is TPS_ERR_ARG.
+ *   out_top_idx      [B, n_top] int32 (row-major, caller-owned device memory): the n_top most
+ *                    probable kept tokens of each row, by probability descending and then index
+ *                    ascending; slots past the row's kept count hold -1.  A greedy row holds its
+ *                    token then -1s; a failed row holds -1s.  NULL with n_top > 0 is TPS_ERR_ARG.
+ *   out_top_logprob  [B, n_top] float: ln P of those tokens (0 for a greedy row's token, -inf for
+ *                    empty slots, NaN for every slot of a failed row).
+ * Every other argument is as in tps_sample_kernel.  Asking for top tokens on rows that take the
+ * general path (more than 256 survivors) costs one or more extra passes over those rows.
  */
 int tps_sample_full(const void* logits, int dtype, int64_t B, int64_t V, int64_t ld, const float* temperature,
                     const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seed,
                     uint64_t step, int32_t* out_token, float* out_probs, int32_t* out_status, float* out_cutoff,
-                    int32_t* out_kept, float* out_logprob, int kernel, void* stream);
+                    int32_t* out_kept, float* out_logprob, int32_t n_top, int32_t* out_top_idx,
+                    float* out_top_logprob, int kernel, void* stream);
 
 /* Kernels one tps_sample_kernel call with these arguments launches (1 or 2; 0 for arguments the call
  * would reject).  Host-only query. */

@@ -21,8 +21,12 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _CSRC = os.path.join(_HERE, "csrc")
 _LIB = os.path.join(_HERE, "libtps.so")
 _INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
-_SOURCES = ["tps_api.cu"]
-_HEADERS = ["tps_device.cuh", "tps_common.cuh", "tps_cluster.cuh", "tps_stream.cuh"]
+# The ABI and launch code, and one translation unit per (kernel, element type): compiled in parallel.
+_SOURCES = ["tps_api.cu", "tps_k_cluster_f32.cu", "tps_k_cluster_bf16.cu", "tps_k_stream_f32.cu",
+            "tps_k_stream_bf16.cu"]
+_HEADERS = ["tps_device.cuh", "tps_common.cuh", "tps_cluster.cuh", "tps_stream.cuh", "tps_kernels.h"]
+_NVCC = ["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
+         "-Xcompiler", "-fPIC"]
 
 TPS_F32, TPS_BF16 = 0, 1
 ROW_STATUS = {0: "ok", 1: "nan", 2: "all_masked", 3: "bad_param", 4: "timeout"}
@@ -46,16 +50,26 @@ def _stale() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile ``libtps.so`` for sm_103a with nvcc (one translation unit, a few seconds)."""
+    """Compile ``libtps.so`` for sm_103a with nvcc: the translation units in parallel, then one link."""
     if not force and not _stale():
         return _LIB
+    objdir = os.path.join(_HERE, "_build", f"obj{os.getpid()}")
+    os.makedirs(objdir, exist_ok=True)
+    objs, procs = [], []
+    for f in _SOURCES:
+        o = os.path.join(objdir, f.replace(".cu", ".o"))
+        cmd = _NVCC + (["-Xptxas=-v"] if verbose else []) + ["-c", "-o", o, os.path.join(_CSRC, f)]
+        procs.append((f, subprocess.Popen(cmd)))
+        objs.append(o)
+    failed = [f for f, p in procs if p.wait() != 0]
+    if failed:
+        raise RuntimeError(f"nvcc failed on {', '.join(failed)}")
     tmp = _LIB + f".tmp{os.getpid()}"
-    cmd = ["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
-           "-Xcompiler", "-fPIC", "-shared", "-o", tmp] + [os.path.join(_CSRC, f) for f in _SOURCES]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    subprocess.run(cmd, check=True)
+    subprocess.run(_NVCC + ["-shared", "-o", tmp] + objs, check=True)
     os.replace(tmp, _LIB)
+    for o in objs:
+        os.remove(o)
+    os.rmdir(objdir)
     return _LIB
 
 
@@ -74,7 +88,8 @@ def load():
             lib.tps_sample_kernel.restype = I32
             lib.tps_sample_kernel.argtypes = [P, I32, I64, I64, I64, P, P, P, P, P, U64, P, P, P, P, P, I32, P]
             lib.tps_sample_full.restype = I32
-            lib.tps_sample_full.argtypes = [P, I32, I64, I64, I64, P, P, P, P, P, U64, P, P, P, P, P, P, I32, P]
+            lib.tps_sample_full.argtypes = [P, I32, I64, I64, I64, P, P, P, P, P, U64, P, P, P, P, P, P, I32, P, P,
+                                            I32, P]
             lib.tps_max_vocab.restype = I64
             lib.tps_max_vocab.argtypes = [I32]
             lib.tps_cluster_size.restype = I32
@@ -139,11 +154,12 @@ def _param(x, B, dtype, device):
 
 
 KERNELS = {"auto": 0, "cluster": 1, "stream": 2}
+MAX_TOP = 32  # TPS_MAX_TOP
 
 
 def sample(logits: torch.Tensor, temperature, top_k, top_p, min_p, seed, step: int = 0, *,
-           want_probs: bool = False, diagnostics: bool = False, want_logprob: bool = False, out=None, stream=None,
-           kernel: str = "auto"):
+           want_probs: bool = False, diagnostics: bool = False, want_logprob: bool = False, top_logprobs: int = 0,
+           out=None, stream=None, kernel: str = "auto"):
     """Sample one token per row of ``logits`` ([B, V] float32/bfloat16 CUDA tensor; the row stride
     may exceed V).
 
@@ -154,7 +170,9 @@ def sample(logits: torch.Tensor, temperature, top_k, top_p, min_p, seed, step: i
     ``want_probs`` is set.  Work is enqueued on ``stream`` (default: the current stream).
     ``kernel`` picks the sampler kernel ("auto", "cluster" or "stream"); results do not depend on it.
     ``want_logprob`` adds ``logprob``: ln P(token) under the renormalised kept distribution (0 for
-    greedy rows, NaN for failed rows).
+    greedy rows, NaN for failed rows).  ``top_logprobs`` = n (0..32) adds ``top_idx`` and
+    ``top_logprob`` ([B, n]): each row's n most probable kept tokens (probability descending, then
+    index ascending) and their ln P; empty slots hold -1 and -inf, a failed row -1 and NaN.
     """
     if not logits.is_cuda:
         raise ValueError("logits must be a CUDA tensor (the sampler has no CPU path)")
@@ -188,17 +206,29 @@ def sample(logits: torch.Tensor, temperature, top_k, top_p, min_p, seed, step: i
     if want_logprob:
         lp = res.get("logprob", None)
         lp = lp if lp is not None else torch.empty(B, dtype=torch.float32, device=dev)
+    n_top = int(top_logprobs)
+    if not 0 <= n_top <= MAX_TOP:
+        raise ValueError(f"top_logprobs must lie in [0, {MAX_TOP}]")
+    ti = tl = None
+    if n_top:
+        ti = res.get("top_idx", None)
+        ti = ti if ti is not None else torch.empty((B, n_top), dtype=torch.int32, device=dev)
+        tl = res.get("top_logprob", None)
+        tl = tl if tl is not None else torch.empty((B, n_top), dtype=torch.float32, device=dev)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     with torch.cuda.device(dev):
         rc = load().tps_sample_full(_ptr(logits), code, B, V, ld, _ptr(T), _ptr(K), _ptr(P), _ptr(M), _ptr(S),
                                     int(step) & ((1 << 64) - 1), _ptr(tok), _ptr(probs), _ptr(st), _ptr(cut),
-                                    _ptr(kept), _ptr(lp), KERNELS[kernel], ctypes.c_void_p(s.cuda_stream))
+                                    _ptr(kept), _ptr(lp), n_top, _ptr(ti), _ptr(tl), KERNELS[kernel],
+                                    ctypes.c_void_p(s.cuda_stream))
     _check(rc)
-    if not (diagnostics or want_probs or want_logprob):
+    if not (diagnostics or want_probs or want_logprob or n_top):
         return tok
     r = {"token": tok}
     if want_logprob:
         r["logprob"] = lp
+    if n_top:
+        r.update(top_idx=ti, top_logprob=tl)
     if diagnostics:
         r.update(status=st, cutoff=cut, kept=kept)
     if want_probs:

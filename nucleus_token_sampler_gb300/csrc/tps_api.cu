@@ -15,12 +15,26 @@
 #include <atomic>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "../../include/tps.h"
 #include "tps_cluster.cuh"
+#include "tps_kernels.h"
 #include "tps_stream.cuh"
 
 namespace {
+
+// The kernels for an element type (instantiated in their own translation units).
+template <typename TIn>
+tps::ClusterKernel cluster_kernel()
+{
+    return std::is_same<TIn, float>::value ? tps::cluster_kernel_f32() : tps::cluster_kernel_bf16();
+}
+template <typename TIn>
+tps::StreamKernel stream_kernel()
+{
+    return std::is_same<TIn, float>::value ? tps::stream_kernel_f32() : tps::stream_kernel_bf16();
+}
 
 thread_local int g_last_cuda_error = 0;
 
@@ -108,7 +122,7 @@ int choose_cluster(const DeviceInfo& d, int es, int64_t B, int64_t V)
 template <typename TIn>
 cudaError_t prepare_kernel(const DeviceInfo& d)
 {
-    auto k = tps::sample_rows_kernel<TIn>;
+    auto k = cluster_kernel<TIn>();
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, d.smem_optin);
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -134,7 +148,7 @@ bool wide_cluster_ok(DeviceInfo& d, int dt, int C, size_t smem)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, tps::sample_rows_kernel<TIn>, &cfg);
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, cluster_kernel<TIn>(), &cfg);
     if (e != cudaSuccess || n < 1) {
         (void)cudaGetLastError();
         return false;
@@ -156,7 +170,7 @@ template <typename TIn>
 cudaError_t launch_stream(const DeviceInfo& d, bool* attrs_done, const tps::Args& a, bool dependent,
                           cudaStream_t stream)
 {
-    auto k = tps::stream_rows_kernel<TIn>;
+    auto k = stream_kernel<TIn>();
     const size_t smem = stream_smem_bytes();
     if (!*attrs_done) {
         const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -193,7 +207,7 @@ cudaError_t launch(const tps::Args& a, int C, size_t smem, int64_t nclusters, cu
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tps::sample_rows_kernel<TIn>, a);
+    return cudaLaunchKernelEx(&cfg, cluster_kernel<TIn>(), a);
 }
 
 // Clusters of C CTAs the device holds at once (at least 1), asked once per (dtype, C, shared memory).
@@ -215,7 +229,7 @@ int64_t resident_clusters(DeviceInfo& d, int dt, int C, size_t smem)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tps::sample_rows_kernel<TIn>, &cfg) != cudaSuccess || n < 1) {
+    if (cudaOccupancyMaxActiveClusters(&n, cluster_kernel<TIn>(), &cfg) != cudaSuccess || n < 1) {
         (void)cudaGetLastError();
         n = 1;
     }
@@ -294,10 +308,12 @@ int tps_cluster_size(int dtype, int64_t B, int64_t V)
 int tps_sample_full(const void* logits, int dtype, int64_t B, int64_t V, int64_t ld, const float* temperature,
                     const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seed,
                     uint64_t step, int32_t* out_token, float* out_probs, int32_t* out_status, float* out_cutoff,
-                    int32_t* out_kept, float* out_logprob, int kernel, void* stream)
+                    int32_t* out_kept, float* out_logprob, int32_t n_top, int32_t* out_top_idx,
+                    float* out_top_logprob, int kernel, void* stream)
 {
     if (kernel < TPS_KERNEL_AUTO || kernel > TPS_KERNEL_STREAM) return TPS_ERR_ARG;
-    if (B < 0 || V < 1 || ld < V) return TPS_ERR_ARG;
+    if (B < 0 || V < 1 || ld < V || n_top < 0 || n_top > TPS_MAX_TOP) return TPS_ERR_ARG;
+    if (n_top > 0 && (!out_top_idx || !out_top_logprob)) return TPS_ERR_ARG;
     const int es = elem_bytes(dtype);
     if (!es) return TPS_ERR_DTYPE;
     if (B == 0) return TPS_OK;
@@ -305,7 +321,8 @@ int tps_sample_full(const void* logits, int dtype, int64_t B, int64_t V, int64_t
     if (!aligned(logits, es) || !aligned(temperature, 4) || !aligned(top_k, 4) || !aligned(top_p, 4) ||
         !aligned(min_p, 4) || !aligned(seed, 8) || !aligned(out_token, 4) || (out_probs && !aligned(out_probs, 4)) ||
         (out_status && !aligned(out_status, 4)) || (out_cutoff && !aligned(out_cutoff, 4)) ||
-        (out_kept && !aligned(out_kept, 4)) || (out_logprob && !aligned(out_logprob, 4)))
+        (out_kept && !aligned(out_kept, 4)) || (out_logprob && !aligned(out_logprob, 4)) ||
+        (n_top > 0 && (!aligned(out_top_idx, 4) || !aligned(out_top_logprob, 4))))
         return TPS_ERR_ALIGN;
     if (V > kMaxVocabMass || V > INT32_MAX) return TPS_ERR_UNSUPPORTED_V;
     if (B > (int64_t)INT32_MAX / kMaxCluster) return TPS_ERR_ARG;
@@ -340,6 +357,9 @@ int tps_sample_full(const void* logits, int dtype, int64_t B, int64_t V, int64_t
     a.out_cutoff = out_cutoff;
     a.out_kept = out_kept;
     a.out_logprob = out_logprob;
+    a.n_top = n_top;
+    a.out_top_idx = n_top > 0 ? out_top_idx : nullptr;
+    a.out_top_logprob = n_top > 0 ? out_top_logprob : nullptr;
     a.slice_cap = cap;
     a.route = split ? tps::kRouteCluster : tps::kRouteAll;
 
@@ -398,7 +418,7 @@ int tps_sample_kernel(const void* logits, int dtype, int64_t B, int64_t V, int64
                       int32_t* out_kept, int kernel, void* stream)
 {
     return tps_sample_full(logits, dtype, B, V, ld, temperature, top_k, top_p, min_p, seed, step, out_token, out_probs,
-                           out_status, out_cutoff, out_kept, nullptr, kernel, stream);
+                           out_status, out_cutoff, out_kept, nullptr, 0, nullptr, nullptr, kernel, stream);
 }
 
 int tps_sample_ex(const void* logits, int dtype, int64_t B, int64_t V, int64_t ld, const float* temperature,

@@ -215,6 +215,7 @@ __device__ __forceinline__ bool cluster_row(const Args& a, ClusterTopo& topo, Sh
             for (int x = tid; x < s.nx; x += kThreads) prow[s.xi[x]] = 0.f;
         }
         if (writer) write_row(a, row, -1, status, __uint_as_float(0x7FC00000u), 0);
+        if (rank == 0) write_top_single(a, row, -1, tid, kThreads);
         // A copy still in flight after a timeout must land before the shared memory is released.
         if (timed_out && bytes > 0) (void)mbar_wait_bounded(&s.mbar, 0, kWaitLimitNs);
         cluster.sync();
@@ -240,6 +241,7 @@ __device__ __forceinline__ bool cluster_row(const Args& a, ClusterTopo& topo, Sh
         const uint32_t arg = s.bu[2];
         if (prow) sl.for_each(s, [&](float, int32_t i) { prow[i] = ((uint32_t)i == arg) ? 1.f : 0.f; });
         if (writer) write_row(a, row, (int32_t)arg, kRowOk, zmax, 1, 0.f);  // one-hot: ln P = 0
+        if (rank == 0) write_top_single(a, row, (int32_t)arg, tid, kThreads);
         cluster.sync();
         return true;
     }
@@ -288,16 +290,18 @@ __device__ __forceinline__ bool cluster_row(const Args& a, ClusterTopo& topo, Sh
         const int32_t token = res.token;
         if (prow) write_probs(sl, s, r, key_cut, ZK, prow);
         if (writer) write_row(a, row, token, kRowOk, key_to_float(key_cut), (int32_t)NK, token_logprob<TIn>(a, r, row, token, ZK));
+        if (rank == 0) write_top(a, r, row, s.u.cd.sbuf, NK, ZK, tid, kThreads);  // sbuf is sorted
         cluster_wait();  // every CTA has finished reading this CTA's lists
         return true;
     }
 
     // ================= general path: survivors against the global maximum =================
     // (also when more than kCand listed tokens survive; its first barrier is a cluster barrier)
-    const RowResult res = general_path(topo, s, sl, r, zc, topk_on, K, P, rc, prow, a.out_logprob != nullptr);
+    const RowResult res = general_path(topo, s, sl, r, zc, topk_on, K, P, rc, prow, wants_zk(a));
     if (writer)
         write_row(a, row, res.token, kRowOk, key_to_float(res.key_cut), (int32_t)res.nk,
                   token_logprob<TIn>(a, r, row, res.token, res.zk));
+    general_top(topo, s, sl, r, zc, res.nk, res.zk, a, row, rank == 0);
     topo.sync();  // keep this CTA's shared memory alive until every remote read is done
     return true;
 }
@@ -308,6 +312,7 @@ __device__ __forceinline__ void fail_row(const Args& a, int64_t row, int32_t sta
     if (a.out_probs)
         for (int64_t i = threadIdx.x; i < a.V; i += kThreads) a.out_probs[row * a.V + i] = 0.f;
     if (threadIdx.x == 0) write_row(a, row, -1, status, __uint_as_float(0x7FC00000u), 0);
+    write_top_single(a, row, -1, threadIdx.x, kThreads);
 }
 
 // ---------------------------------------------------------------------------------------------

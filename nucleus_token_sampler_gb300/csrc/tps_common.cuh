@@ -24,6 +24,7 @@ constexpr float kFineScale = 16.f;
 constexpr int kRaceQueue = 64;        // per-warp queue of vectors with tokens to race
 constexpr int kSubBins = 128;         // sub-bins over a key interval (exact refinement)
 constexpr int kMaxWin = 32;           // groups of fine bins in a top-p window
+constexpr int kMaxTop = 32;           // top tokens a call may report per row
 constexpr int kCand = 256;            // candidates resolved by sorting, per CTA and per cluster
 constexpr int kMaxExtra = 16;         // ragged head/tail elements fetched with plain loads
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s bound on every wait
@@ -45,6 +46,9 @@ struct Args {
     float* out_cutoff;
     int32_t* out_kept;
     float* out_logprob;  // ln P(token) under the renormalised kept distribution, or null
+    int32_t n_top;           // top tokens reported per row (0 .. kMaxTop)
+    int32_t* out_top_idx;    // [B, n_top]: the most probable kept tokens, or null
+    float* out_top_logprob;  // [B, n_top]: their ln P
     uint32_t slice_cap;  // bytes reserved for the slice at the start of dynamic shared memory
     uint32_t route;      // which rows the kernel samples (RowRoute)
 };
@@ -770,7 +774,7 @@ __device__ __forceinline__ float race_u(const RaceCtx& rc, int32_t i)
 __device__ __forceinline__ float race_key32(float d, float u) { return -d - logf(-logf(u)); }
 
 // The race key in double precision (the float64 definition), out of line: only near-ties need it.
-__device__ __noinline__ double race_key64_(float zmax, float T, float z, float u)
+static __device__ __noinline__ double race_key64_(float zmax, float T, float z, float u)
 {
     const double d = __ddiv_rn(__dsub_rn((double)zmax, (double)z), (double)T);
     const double g = log(-log((double)u));
@@ -931,7 +935,8 @@ struct WarpResult {
 // returns the same result.
 // z_ext != 0: the list is the top of a larger set whose fixed-point mass is z_ext (top-p is taken
 // against it; top-k must then be off).
-__device__ __forceinline__ WarpResult warp_resolve(const uint64_t* buf, const RowCtx& r, const RaceCtx& rc, uint32_t n,
+// The sorted survivors are left in buf[0, n) (descending).
+__device__ __forceinline__ WarpResult warp_resolve(uint64_t* buf, const RowCtx& r, const RaceCtx& rc, uint32_t n,
                                                    bool topk_on, int32_t K, float P, uint64_t z_ext = 0)
 {
     const uint32_t lane = threadIdx.x & 31;
@@ -946,6 +951,8 @@ __device__ __forceinline__ WarpResult warp_resolve(const uint64_t* buf, const Ro
             v = take_max ? (v > o ? v : o) : (v < o ? v : o);
         }
     }
+    __syncwarp();  // every lane has read its entry of buf
+    if (lane < n) buf[lane] = v;
     const uint32_t key = sb_key(v);
     const int32_t idx = sb_idx(v);
     const bool valid = lane < n;
@@ -1954,17 +1961,131 @@ __device__ __forceinline__ void write_row(const Args& a, int64_t row, int32_t to
 // ln P(token) of a sampled row under the renormalised kept distribution: -(zmax - z)/T - ln(Z_kept)
 // in double, the token's logit z read back from the row and Z_kept = zk 2^-44 (the exact fixed-point
 // sum of the kept tokens' masses, relative to the maximum's).  Out of line: one call per row.
-__device__ __noinline__ float logprob_of(float zmax, float T, float z, uint64_t zk)
+static __device__ __noinline__ float logprob_of(float zmax, float T, float z, uint64_t zk)
 {
     const double dd = __ddiv_rn(__dsub_rn((double)zmax, (double)z), (double)T);
     return (float)(-dd - (log((double)zk) - 44.0 * 0.69314718055994530942));
 }
+// The general path sums the kept mass for a log-probability output even when no cut needs it.
+__device__ __forceinline__ bool wants_zk(const Args& a) { return a.out_logprob != nullptr || a.out_top_idx != nullptr; }
+
 template <typename TIn>
 __device__ __forceinline__ float token_logprob(const Args& a, const RowCtx& r, int64_t row, int32_t token, uint64_t zk)
 {
     if (!a.out_logprob) return 0.f;
     const float z = Elem<TIn>::load1(static_cast<const unsigned char*>(a.logits) + row * a.ld * Elem<TIn>::kBytes, token);
     return logprob_of(r.zmax, r.T, z, zk);
+}
+
+// The row's top tokens from its survivors sorted descending (key << 32 | ~index), the first nk of
+// them kept: the most probable kept tokens with their ln P; slots past the kept ones get -1 and
+// -inf.  Threads t, t + nthr, ... write slots t, t + nthr, ...
+__device__ __forceinline__ void write_top(const Args& a, const RowCtx& r, int64_t row, const uint64_t* sorted,
+                                          uint64_t nk, uint64_t zk, int t, int nthr)
+{
+    if (!a.out_top_idx) return;
+    const int n = a.n_top;
+    for (int j = t; j < n; j += nthr) {
+        int32_t idx = -1;
+        float lp = -INFINITY;
+        if ((uint64_t)j < nk) {
+            const uint64_t v = sorted[j];
+            idx = sb_idx(v);
+            lp = logprob_of(r.zmax, r.T, key_to_float(sb_key(v)), zk);
+        }
+        a.out_top_idx[row * n + j] = idx;
+        a.out_top_logprob[row * n + j] = lp;
+    }
+}
+// A greedy row: the token alone, ln P = 0.  A failed row: every slot -1 and NaN (token < 0).
+__device__ __forceinline__ void write_top_single(const Args& a, int64_t row, int32_t token, int t, int nthr)
+{
+    if (!a.out_top_idx) return;
+    const int n = a.n_top;
+    for (int j = t; j < n; j += nthr) {
+        const bool first = j == 0 && token >= 0;
+        a.out_top_idx[row * n + j] = first ? token : -1;
+        a.out_top_logprob[row * n + j] = first ? 0.f : (token >= 0 ? -INFINITY : __int_as_float(0x7FC00000));
+    }
+}
+
+// The row's top kept tokens for the general path: the nk kept tokens are the top of the min-p
+// survivors S0, so the first min(n_top, nk) of S0 in (logit desc, index asc) order are wanted.  The
+// fine counts locate the bins that hold them; when those bins hold at most kCand survivors they are
+// listed and sorted, otherwise the count cut is refined to the K-th largest logit first.  A tie
+// class too large to list at that logit is resolved by extracting its lowest indices one pass at a
+// time.  Every thread of every CTA of the topology calls it; `writer` threads write the outputs.
+template <typename Topo, typename Src>
+__device__ __noinline__ void general_top(Topo& topo, Shared& s, const Src& src, const RowCtx& r, float zc, uint64_t nk,
+                           uint64_t zk, const Args& a, int64_t row, bool writer)
+{
+    if (!a.out_top_idx || a.n_top <= 0) return;
+    cta_sync();  // the caller's block reductions are complete
+    const uint64_t Kt = min((uint64_t)a.n_top, nk);
+    const uint32_t* hr = topo.fine(s);
+    int bn;
+    uint64_t cn;
+    fine_scan_topk(s, hr, Kt, &bn, &cn);
+    uint32_t key_lo = 0;  // list the survivors with key >= key_lo inside bins <= bn
+    if (cn + hr[bn] > (uint64_t)kCand) {
+        Crit ck;
+        ck.by_mass = false;
+        ck.tcnt = Kt;
+        ck.tmass = 0.0;
+        const float fhi = (bn >= kFineBins - 1) ? INFINITY : (float)(bn + 1);
+        const Sel sk = refine_range(topo, s, src, r, zc, (float)bn, fhi, 0u, ck, cn, 0);
+        key_lo = sk.key;
+        if (sk.cnt > (uint64_t)kCand) key_lo = sk.key + 1u;  // the tie class at sk.key is resolved below
+    }
+    const float fend = (bn >= kFineBins - 1) ? INFINITY : (float)(bn + 1);
+    topo.sync();  // nobody still reads this CTA's lists or published values
+    if (threadIdx.x == 0) s.ncand = 0;
+    cta_sync();
+    src.for_each(s, [&](float z, int32_t i) {
+        if (!(z > zc)) return;
+        const uint32_t key = fkey(z);
+        if (key < key_lo) return;
+        const float d = dist(r, z);
+        if (!(d * kFineScale < fend) || !minp_ok(r, z, d)) return;
+        const uint32_t slot = atomicAdd(&s.ncand, 1u);
+        if (slot < (uint32_t)kCand) {
+            s.ckey[slot] = key;
+            s.cidx[slot] = (uint32_t)i;
+        }
+    });
+    cta_sync();
+    if (threadIdx.x == 0) s.pub_gcnt = min(s.ncand, (uint32_t)kCand);
+    topo.sync();
+    int n = gather_and_sort(topo, s);
+    // A tie class too large to list: append its lowest indices, one pass each.
+    if ((uint64_t)n < Kt && key_lo > 0) {
+        const uint32_t tkey = key_lo - 1u;
+        uint32_t last = 0;
+        bool any = false;
+        for (uint64_t j = (uint64_t)n; j < Kt; ++j) {
+            uint32_t mi = 0xFFFFFFFFu;
+            src.for_each(s, [&](float z, int32_t i) {
+                if (z > -INFINITY && fkey(z) == tkey && (!any || (uint32_t)i > last)) mi = min(mi, (uint32_t)i);
+            });
+            mi = block_min_u32(mi, s);
+            if (threadIdx.x == 0) s.pub_minidx = mi;
+            topo.sync();
+            if (threadIdx.x < 32) {
+                uint32_t m = (threadIdx.x < topo.C) ? *topo.map(&s.pub_minidx, threadIdx.x) : 0xFFFFFFFFu;
+                m = warp_min_u32(m);
+                if (threadIdx.x == 0) s.bu[2] = m;
+            }
+            cta_sync();
+            last = s.bu[2];
+            any = true;
+            if (threadIdx.x == 0) s.u.cd.sbuf[j] = sb_make(tkey, last);
+            topo.sync();  // everyone has read pub_minidx
+        }
+        n = (int)Kt;
+        cta_sync();
+    }
+    if (writer) write_top(a, r, row, s.u.cd.sbuf, min((uint64_t)n, Kt), zk, threadIdx.x, kThreads);
+    cta_sync();
 }
 
 }  // namespace tps

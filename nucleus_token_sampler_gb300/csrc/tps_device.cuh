@@ -31,7 +31,7 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 }
 
 // One block out of line: the race code that draws it stays small inside unrolled loops.
-__device__ __noinline__ uint4 philox_block(uint4 c, uint32_t k0, uint32_t k1) { return philox4x32_10(c, k0, k1); }
+static __device__ __noinline__ uint4 philox_block(uint4 c, uint32_t k0, uint32_t k1) { return philox4x32_10(c, k0, k1); }
 
 // Uniform in (0, 1): an odd multiple of 2^-24, exact in float and double.
 __device__ __forceinline__ uint32_t uniform_grid(uint32_t x) { return 2u * (x >> 9) + 1u; }
@@ -104,7 +104,7 @@ __device__ __forceinline__ uint64_t qmass_d(float d) { return fixed44(expf(-d));
 // The double-precision min-p decision (the same operations as the float64 definition), out of
 // line: it runs only for tokens within a narrow margin of the cut, and inlining it into every
 // element of an unrolled loop would crowd the instruction cache.
-__device__ __noinline__ bool minp_ok_double(float zmax, float T, float minp, float z)
+static __device__ __noinline__ bool minp_ok_double(float zmax, float T, float minp, float z)
 {
     const double dd = __ddiv_rn(__dsub_rn((double)zmax, (double)z), (double)T);
     return exp(-dd) >= (double)minp;

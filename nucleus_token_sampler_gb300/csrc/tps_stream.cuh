@@ -192,6 +192,7 @@ __device__ void run_task(const Args& a, Shared& s, const Task& t, uint32_t chunk
         if (prow)
             for (int64_t i = tid; i < a.V; i += kThreads) prow[i] = ((uint32_t)i == mi) ? 1.f : 0.f;
         if (tid == 0) write_row(a, row, (int32_t)mi, kRowOk, zmax, 1, 0.f);
+        write_top_single(a, row, (int32_t)mi, tid, kThreads);
         return;
     }
     const float minp = clamp_minp(p.MP);
@@ -205,10 +206,11 @@ __device__ void run_task(const Args& a, Shared& s, const Task& t, uint32_t chunk
     const bool topk_on = (p.K > 0) && ((int64_t)p.K < a.V);
     SoloTopo topo;
     const RowResult res =
-        general_path(topo, s, src, r, zc, topk_on, p.K, p.P, race_ctx(a, row, p.seed), prow, a.out_logprob != nullptr);
+        general_path(topo, s, src, r, zc, topk_on, p.K, p.P, race_ctx(a, row, p.seed), prow, wants_zk(a));
     if (tid == 0)
         write_row(a, row, res.token, kRowOk, key_to_float(res.key_cut), (int32_t)res.nk,
                   token_logprob<TIn>(a, r, row, res.token, res.zk));
+    general_top(topo, s, src, r, zc, res.nk, res.zk, a, row, true);
 }
 
 template <typename TIn>
@@ -321,6 +323,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
             t.kind = 0;
             if (status != kRowOk) {
                 if (lane == 0) write_row(a, row, -1, status, __uint_as_float(0x7FC00000u), 0);
+                write_top_single(a, row, -1, (int)lane, 32);
                 if (a.out_probs) t.kind = kTaskZero;
             } else if (p.T <= 0.f) {
                 // greedy: the lowest listed index holding the maximum (the list holds every token
@@ -331,6 +334,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
                         if (key_to_float(slot.lkey[e]) == zmax) mi = min(mi, slot.lidx[e]);
                     mi = __reduce_min_sync(0xFFFFFFFFu, mi);
                     if (lane == 0) write_row(a, row, (int32_t)mi, kRowOk, zmax, 1, 0.f);
+                    write_top_single(a, row, (int32_t)mi, (int)lane, 32);
                 } else {
                     t.kind = kTaskGreedy;  // a pass over the row (also writes the one-hot row)
                 }
@@ -369,6 +373,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
                     if (lane == 0)
                         write_row(a, row, wr.token, kRowOk, key_to_float(wr.key_cut), (int32_t)wr.nk,
                                   token_logprob<TIn>(a, r, row, wr.token, wr.zk));
+                    __syncwarp();  // the sorted survivors are visible to every lane
+                    write_top(a, r, row, (n <= 32) ? st.rbuf : st.rsorted, wr.nk, wr.zk, (int)lane, 32);
                     if (a.out_probs) {
                         t.kind = kTaskProbs;
                         t.key_cut = wr.key_cut;

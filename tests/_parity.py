@@ -14,15 +14,18 @@ PROB_TOL = 1e-5  # absolute, on renormalised probabilities
 LOGPROB_TOL = 1e-5
 
 
-def run_gpu(w, want_probs=True, logits=None, kernel="auto", want_logprob=None):
-    """The library on the GPU.  The log-probability output is requested for the auto kernel (unless
-    want_logprob says otherwise), so the explicit kernels keep covering the path without it."""
+def run_gpu(w, want_probs=True, logits=None, kernel="auto", want_logprob=None, top=None):
+    """The library on the GPU.  The log-probability outputs (the sampled token's, and the top 8
+    tokens') are requested for the auto kernel (unless want_logprob / top say otherwise), so the
+    explicit kernels keep covering the path without them."""
     d = w.to("cuda")
     lg = d.logits if logits is None else logits
     if want_logprob is None:
         want_logprob = kernel == "auto"
+    if top is None:
+        top = 8 if kernel == "auto" else 0
     r = tps.sample(lg, d.temperature, d.top_k, d.top_p, d.min_p, d.seed, d.step, want_probs=want_probs,
-                   diagnostics=True, want_logprob=want_logprob, kernel=kernel)
+                   diagnostics=True, want_logprob=want_logprob, top_logprobs=top, kernel=kernel)
     torch.cuda.synchronize()
     return {k: v.cpu() for k, v in r.items()}
 
@@ -34,6 +37,50 @@ def run_oracle(w, rows=None, want_probs=True):
                          sel(w.top_p).numpy(), sel(w.min_p).numpy(),
                          sel(w.seed).numpy().astype(np.uint64), w.step,
                          row_ids=None if rows is None else np.asarray(rows), want_probs=want_probs)
+
+
+def expected_top(w, o, rows, j, n):
+    """The oracle's n most probable kept tokens of row rows[j] (probability descending, index
+    ascending) and their ln P.  The kept set is every finite logit at or above the cutoff (ties
+    included); a greedy row keeps its token alone."""
+    row = int(rows[j])
+    if float(w.temperature[row]) <= 0.0:
+        return [int(o["token"][j])], [0.0]
+    z = w.logits[row].double().numpy()
+    kept = np.nonzero(np.isfinite(z) & (z >= o["cutoff"][j]))[0]
+    assert len(kept) == int(o["kept"][j]), "the kept set read off the cutoff disagrees with the oracle's count"
+    order = kept[np.lexsort((kept, -z[kept]))][:n]
+    return order.tolist(), np.log(o["probs"][j, order]).tolist()
+
+
+def compare_top(w, g, o, rows, okrow, setband):
+    """Top-n tokens and log-probabilities against the oracle, on rows whose kept set is exact."""
+    fails = []
+    ti = g["top_idx"].numpy()[rows]
+    tl = g["top_logprob"].numpy()[rows].astype(np.float64)
+    n = ti.shape[1]
+    worst = 0.0
+    for j in np.nonzero(okrow & ~setband)[0]:
+        idx, lp = expected_top(w, o, rows, j, n)
+        want = np.full(n, -1, dtype=np.int64)
+        want[:len(idx)] = idx
+        if not np.array_equal(ti[j], want):
+            fails.append(f"top tokens differ at row {rows[j]}: gpu {ti[j].tolist()} oracle {want.tolist()}")
+            break
+        ref = np.asarray(lp)
+        err = np.abs(tl[j, :len(idx)] - ref)
+        bad = err > LOGPROB_TOL + 1e-6 * np.abs(ref)
+        if bad.any():
+            fails.append(f"top log-probability differs by {err.max():.3e} at row {rows[j]}")
+            break
+        if len(idx) < n and not (tl[j, len(idx):] == -np.inf).all():
+            fails.append(f"empty top slots of row {rows[j]} are not -inf")
+            break
+        worst = max(worst, float(err.max()) if len(err) else 0.0)
+    failed = ~okrow
+    if failed.any() and not ((ti[failed] == -1).all() and np.isnan(tl[failed]).all()):
+        fails.append("failed rows have top tokens")
+    return fails
 
 
 def compare(w, g, o, rows=None, check_probs=True):
@@ -78,6 +125,8 @@ def compare(w, g, o, rows=None, check_probs=True):
                 fails.append(f"logprob differs by {err[i]:.3e} at a row with ln P = {ref[i]:.6f}")
         if (~okrow).any() and not np.isnan(lp[~okrow]).all():
             fails.append("failed rows have a non-NaN logprob")
+    if "top_idx" in g and "probs" in o:
+        fails += compare_top(w, g, o, rows, okrow, setband)
     maxdp = 0.0
     if check_probs and "probs" in g and "probs" in o:
         pg = g["probs"].numpy()[rows].astype(np.float64)

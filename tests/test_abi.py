@@ -80,6 +80,21 @@ def test_sample_full_checks_the_logprob_pointer():
     lib = tps.load()
     v = lambda p: None if p is None else ctypes.c_void_p(p)
     # a misaligned out_logprob is rejected before anything is launched
-    rc = lib.tps_sample_full(v(FAKE), 0, 4, 100, 100, v(FAKE), v(FAKE), v(FAKE), v(FAKE), v(FAKE), 0, v(FAKE), None,
-                             None, None, None, v(FAKE + 2), 0, None)
-    assert rc == 4
+    def call(lp=None, n_top=0, ti=None, tl=None):
+        return lib.tps_sample_full(v(FAKE), 0, 4, 100, 100, v(FAKE), v(FAKE), v(FAKE), v(FAKE), v(FAKE), 0, v(FAKE),
+                                   None, None, None, None, v(lp), n_top, v(ti), v(tl), 0, None)
+    assert call(lp=FAKE + 2) == 4
+
+
+def test_sample_full_checks_the_top_token_arguments():
+    lib = tps.load()
+    v = lambda p: None if p is None else ctypes.c_void_p(p)
+    def call(n_top, ti, tl):
+        return lib.tps_sample_full(v(FAKE), 0, 4, 100, 100, v(FAKE), v(FAKE), v(FAKE), v(FAKE), v(FAKE), 0, v(FAKE),
+                                   None, None, None, None, None, n_top, v(ti), v(tl), 0, None)
+    assert call(-1, FAKE, FAKE) == 1              # negative count
+    assert call(tps.MAX_TOP + 1, FAKE, FAKE) == 1  # above TPS_MAX_TOP
+    assert call(3, None, FAKE) == 1               # missing index output
+    assert call(3, FAKE, None) == 1               # missing log-probability output
+    assert call(3, FAKE + 2, FAKE) == 4           # misaligned index output
+    assert call(3, FAKE, FAKE + 1) == 4           # misaligned log-probability output

@@ -207,6 +207,54 @@ def test_empty_batch(kernel):
     assert out.shape == (0,)
 
 
+_ORACLE = {}
+
+
+def _top_check(w, kernel, top=tps.MAX_TOP):
+    key = (w.name, w.B, w.V)
+    if w.name == "edge" or key not in _ORACLE:
+        _ORACLE[key] = _parity.run_oracle(w)
+    o = _ORACLE[key]
+    g = _parity.run_gpu(w, kernel=kernel, want_logprob=True, top=top)
+    rows = np.arange(w.B)
+    okrow = o["status"] == 0
+    setband = (o["flags"] & (_parity.TOPP_BAND | _parity.MINP_BAND)) != 0
+    fails = _parity.compare_top(w, g, o, rows, okrow, setband)
+    assert not fails, f"[{kernel}] " + "\n".join(fails)
+    return g, o
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("name", ["small", "mixed", "ties_masked"])
+def test_top_logprobs(kernel, name):
+    """The 32 most probable kept tokens of each row with their ln P (the most the ABI reports):
+    list-resolved rows, general-path rows (more than 256 survivors) and rows with ties."""
+    _top_check(workloads.make(name, device="cpu"), kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_top_logprobs_big_tie_classes(kernel, dtype):
+    """Tie classes larger than a candidate list where the top tokens end: equal logits over the
+    whole row, and a few distinct leaders followed by one value shared by most of the row; the
+    lowest indices of the tie come first."""
+    V = 128256
+    rng = np.random.default_rng(11)
+    flat = np.zeros(V)
+    lead = rng.normal(0, 1, V) - 6.0
+    lead[rng.choice(V, 100000, replace=False)] = -1.0
+    lead[[5, 900, 77777, 128000]] = [3.0, 2.5, 2.5, 1.0]
+    few = flat.copy()
+    few[:3] = 1.0
+    z = np.stack([flat, flat, lead, lead, lead, few])
+    T = [1.0, 0.5, 1.0, 0.8, 1.0, 1.0]
+    k = [0, 40, 0, 0, 50, 0]
+    p = [0.9, 1.0, 0.95, 1.0, 0.9, 0.999]
+    w = _w(z, T, k, p, 0.0, dtype=dtype)
+    _top_check(w, kernel)
+    _top_check(w, kernel, top=5)
+
+
 @pytest.mark.gpu
 def test_kernels_per_call_follows_the_split_rule():
     f32 = torch.float32
