@@ -56,6 +56,9 @@ class Oracle:
         lib.tpso_philox4x32_10.restype = None
         lib.tpso_philox4x32_10.argtypes = [P, P, P]
         lib.tpso_max_threads.restype = ctypes.c_int
+        I64 = ctypes.c_int64
+        lib.tpso_penalties.restype = ctypes.c_int
+        lib.tpso_penalties.argtypes = [P, ctypes.c_int, I64, I64, I64, P, I64, I64, P, P, P, P, P]
         self.lib = lib
         self.path = lib_path
 
@@ -101,6 +104,32 @@ class Oracle:
             out["probs"] = probs
         return out
 
+    def penalties(self, z, history, hist_len=None, repetition=None, frequency=None, presence=None,
+                  bf16=False):
+        """Repetition, frequency and presence penalties on raw logits (float32 arithmetic).
+
+        ``z``: [B, V] logits as float32 values (bfloat16 logits widened exactly, with ``bf16`` set
+        so results are rounded back to bfloat16); ``history``: [B, H] int32 token ids (entries
+        outside [0, V) ignored); ``hist_len``: [B] or None (every row uses H); the three penalty
+        vectors: [B] float32 or None (off).  Returns (penalised logits as float32, row status).
+        """
+        z = np.array(z, dtype=np.float32, order="C", copy=True)
+        B, V = z.shape
+        h = np.ascontiguousarray(np.asarray(history, dtype=np.int32).reshape(B, -1))
+        H = h.shape[1]
+
+        def vec(x, dt):
+            return None if x is None else np.ascontiguousarray(np.broadcast_to(np.asarray(x, dtype=dt), (B,)))
+
+        L, R, F, Pr = vec(hist_len, np.int32), vec(repetition, np.float32), vec(frequency, np.float32), \
+            vec(presence, np.float32)
+        st = np.empty(B, np.int32)
+        rc = self.lib.tpso_penalties(_ptr(z), int(bool(bf16)), B, V, V, _ptr(h), H, H, _ptr(L), _ptr(R), _ptr(F),
+                                     _ptr(Pr), _ptr(st))
+        if rc != 0:
+            raise MemoryError("oracle scratch allocation failed")
+        return z, st
+
     def uniform(self, seed: int, row: int, step: int, token: int) -> float:
         """The race's uniform u in (0, 1) for (seed, row, step, token)."""
         m = (1 << 64) - 1
@@ -132,6 +161,10 @@ def sample(*args, **kwargs):
 
 def uniform(seed: int, row: int, step: int, token: int) -> float:
     return default().uniform(seed, row, step, token)
+
+
+def penalties(*args, **kwargs):
+    return default().penalties(*args, **kwargs)
 
 
 def philox4x32_10(counter, key):

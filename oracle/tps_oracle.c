@@ -333,3 +333,73 @@ int tpso_max_threads(void)
     return 1;
 #endif
 }
+
+/* ---------------------------------------------------------------------------------------------
+ * Penalties on the raw logits, ahead of the chain above.  [NS] "Where top-p sits in the sampler
+ * chain" puts repetition, frequency and presence penalties first, on the logits; [ORD] "What
+ * interviewers probe next" says they act before temperature, on raw logits, so that they change
+ * the greedy choice too.  The pages give no formulas; this takes the common ones:
+ *   c_t  = number of entries of the row's history equal to t (entries outside [0, V) and past the
+ *          row's history length are ignored; the length is clamped to [0, H]);
+ *   for every t with c_t > 0:
+ *     y   = z_t / r   if z_t > 0,   z_t * r   otherwise          (repetition, r > 0; 1 = off)
+ *     z'_t = y - (f * c_t + rho)                                  (frequency f, presence rho)
+ *   every other logit is unchanged.
+ * Precision: the pages fix none.  The penalised logit is the sampler's input, so it is defined in
+ * float32, one correctly rounded operation at a time in the order written, and rounded to
+ * bfloat16 (nearest, ties to even) for bfloat16 logits; this oracle performs exactly those float
+ * operations (the build disables contraction).  A row with r <= 0 or a non-finite r, f or rho is
+ * left unchanged and reported as a bad parameter.
+ * --------------------------------------------------------------------------------------------- */
+
+/* Round a float32 to the nearest bfloat16 (ties to even), returned as the float it represents. */
+static float round_bf16(float x)
+{
+    if (isnan(x)) return x;
+    uint32_t u;
+    memcpy(&u, &x, 4);
+    const uint32_t keep = u >> 16, rest = u & 0xFFFFu;
+    uint32_t r = keep;
+    if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) r = keep + 1u;  /* carries into the exponent */
+    r <<= 16;
+    float y;
+    memcpy(&y, &r, 4);
+    return y;
+}
+
+int tpso_penalties(float* z, int is_bf16, int64_t B, int64_t V, int64_t ld, const int32_t* hist, int64_t H,
+                   int64_t ldh, const int32_t* hist_len, const float* rep, const float* freq, const float* pres,
+                   int32_t* status)
+{
+    int32_t* cnt = (int32_t*)calloc((size_t)(V > 0 ? V : 1), sizeof(int32_t));
+    if (!cnt) return 1;
+    for (int64_t b = 0; b < B; ++b) {
+        const float r = rep ? rep[b] : 1.0f;
+        const float f = freq ? freq[b] : 0.0f;
+        const float rho = pres ? pres[b] : 0.0f;
+        if (!(isfinite(r) && r > 0.0f && isfinite(f) && isfinite(rho))) {
+            if (status) status[b] = TPSO_ROW_BAD_PARAM;
+            continue;
+        }
+        if (status) status[b] = TPSO_ROW_OK;
+        int64_t n = hist_len ? (int64_t)hist_len[b] : H;
+        if (n < 0) n = 0;
+        if (n > H) n = H;
+        memset(cnt, 0, (size_t)V * sizeof(int32_t));
+        for (int64_t j = 0; j < n; ++j) {
+            const int32_t t = hist[b * ldh + j];
+            if (t >= 0 && (int64_t)t < V) ++cnt[t];
+        }
+        float* row = z + b * ld;
+        for (int64_t t = 0; t < V; ++t) {
+            if (cnt[t] == 0) continue;
+            const float x = row[t];
+            const float y = (x > 0.0f) ? x / r : x * r;
+            const float s = f * (float)cnt[t] + rho;
+            const float out = y - s;
+            row[t] = is_bf16 ? round_bf16(out) : out;
+        }
+    }
+    free(cnt);
+    return 0;
+}

@@ -376,7 +376,87 @@ def check_philox_vs_triton(o):
     return fails
 
 
+def check_penalties(o):
+    """Repetition / frequency / presence penalties (float32 arithmetic), pinned by hand-worked
+    values, identities and invariants of the definition: the pages name the three penalties and
+    their place (on raw logits, before temperature) but print no formula or example."""
+    fails = []
+    f32 = np.float32
+
+    # A hand-worked row (every intermediate is exact in float32):
+    #   t0: c=1, 2/2 = 1,    1 - (0.5*1 + 0.25) = 0.25
+    #   t1: c=2, -1*2 = -2, -2 - (0.5*2 + 0.25) = -3.25
+    #   t2, t3: not in the history, unchanged;  t4: c=3, 3/2 = 1.5, 1.5 - (1.5 + 0.25) = -0.25
+    z = np.array([[2.0, -1.0, 0.5, 0.0, 3.0]], f32)
+    out, st = o.penalties(z, [[0, 1, 1, 4, 4, 4]], repetition=[2.0], frequency=[0.5], presence=[0.25])
+    want = np.array([[0.25, -3.25, 0.5, 0.0, -0.25]], f32)
+    if not np.array_equal(out, want) or st[0] != 0:
+        fails.append(f"worked row: {out.tolist()} status {st.tolist()}, want {want.tolist()}")
+
+    # Repetition alone: positive logits are divided, negative ones multiplied, zero stays zero.
+    out, _ = o.penalties(np.array([[4.0, -4.0, 0.0, 1.5]], f32), [[0, 1, 2]], repetition=[2.0])
+    if not np.array_equal(out, np.array([[2.0, -8.0, 0.0, 1.5]], f32)):
+        fails.append(f"repetition sign rule: {out.tolist()}")
+
+    # Frequency and presence on integer logits: z - f*c - rho, exactly.
+    rng = np.random.default_rng(17)
+    zi = rng.integers(-20, 20, size=(3, 50)).astype(f32)
+    hist = rng.integers(0, 50, size=(3, 40)).astype(np.int32)
+    out, _ = o.penalties(zi, hist, frequency=[0.5, 0.25, 2.0], presence=[1.0, 0.0, 0.5])
+    for b, (fq, pr) in enumerate(((0.5, 1.0), (0.25, 0.0), (2.0, 0.5))):
+        c = np.bincount(hist[b], minlength=50)
+        exp_row = np.where(c > 0, zi[b] - fq * c - pr, zi[b]).astype(f32)
+        if not np.array_equal(out[b], exp_row):
+            fails.append(f"frequency/presence closed form, row {b}")
+
+    # Penalties off: the row is unchanged, bit for bit (NaN, infinities and -0.0 included).
+    zr = rng.normal(0, 3, size=(2, 300)).astype(f32)
+    zr[0, :5] = [np.nan, np.inf, -np.inf, -0.0, 0.0]
+    hr = rng.integers(0, 300, size=(2, 100)).astype(np.int32)
+    out, _ = o.penalties(zr, hr, repetition=[1.0, 1.0], frequency=[0.0, 0.0], presence=[0.0, 0.0])
+    if not np.array_equal(out.view(np.uint32), zr.view(np.uint32)):
+        fails.append("penalties off changed the logits")
+
+    # The history is a multiset: order does not matter; padding (< 0), ids >= V and entries past the
+    # row's length are ignored.
+    args = dict(repetition=[1.3, 0.7], frequency=[0.3, 0.1], presence=[0.2, 0.4])
+    a, _ = o.penalties(zr, hr, **args)
+    b_, _ = o.penalties(zr, hr[:, ::-1].copy(), **args)
+    padded = np.concatenate([hr, np.full((2, 7), -1, np.int32), np.full((2, 3), 300, np.int32),
+                             rng.integers(0, 300, size=(2, 9)).astype(np.int32)], axis=1)
+    c_, _ = o.penalties(zr, padded, hist_len=[100 + 7 + 3, 100 + 10], **args)
+    if not (np.array_equal(a, b_, equal_nan=True) and np.array_equal(a, c_, equal_nan=True)):
+        fails.append("history order, padding or length changed the result")
+    if not np.array_equal(a[:, 5:] != zr[:, 5:], np.stack([np.isin(np.arange(5, 300), hr[i]) for i in range(2)])):
+        fails.append("a token outside the history was changed, or one inside was not")
+
+    # One token repeated H times: z/r - (f*H + rho).
+    out, _ = o.penalties(np.array([[3.0, 1.0]], f32), np.zeros((1, 64), np.int32), repetition=[1.5],
+                         frequency=[0.125], presence=[1.0])
+    if out[0, 0] != f32(2.0) - f32(0.125 * 64 + 1.0) or out[0, 1] != f32(1.0):
+        fails.append(f"repeated token: {out.tolist()}")
+
+    # Bad parameters leave the row unchanged and report it (status 3); the other rows still run.
+    zb = np.tile(np.array([[1.0, -2.0, 3.0]], f32), (6, 1))
+    hb = np.zeros((6, 2), np.int32)
+    out, st = o.penalties(zb, hb, repetition=[0.0, -1.0, np.nan, 1.0, 1.0, 2.0],
+                          frequency=[0.0, 0.0, 0.0, np.inf, 0.0, 0.0], presence=[0.0, 0.0, 0.0, 0.0, np.nan, 0.0])
+    if st.tolist() != [3, 3, 3, 3, 3, 0] or not np.array_equal(out[:5], zb[:5]) or out[5, 0] != f32(0.5):
+        fails.append(f"bad parameters: status {st.tolist()}")
+
+    # bfloat16 logits: the float32 result rounded to nearest bfloat16, ties to even.  Near 1 the
+    # bfloat16 grid is 1 + k/128: 1 + 0.5/128 ties to 1 (k even), 1 + 1.5/128 ties to 1 + 2/128, and
+    # 1 + 0.5/128 + 2^-23 rounds up to 1 + 1/128.
+    fz = np.array([0.99609375, 0.98828125, f32(0.99609375) - f32(2.0 ** -23)], f32)
+    out, _ = o.penalties(np.full((3, 1), 2.0, f32), np.zeros((3, 1), np.int32), frequency=fz, bf16=True)
+    want = np.array([1.0, 1.015625, 1.0078125], f32)
+    if not np.array_equal(out[:, 0], want):
+        fails.append(f"bfloat16 rounding: {out[:, 0].tolist()}, want {want.tolist()}")
+    return fails
+
+
 ALL_CHECKS = {
+    "penalties": check_penalties,
     "worked_examples": check_worked_examples,
     "sample_frequencies": check_sample_frequencies,
     "bruteforce": check_bruteforce,

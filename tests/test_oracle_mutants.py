@@ -37,6 +37,12 @@ MUTANTS = [
     ("uniform even grid", "return ((double)(2u * (w >> 9) + 1u)) * 0x1p-24;",
      "return ((double)(w >> 8) + 0.5) * 0x1p-24;"),
     ("inf not rejected", "if (isnan(v) || v == INFINITY) {", "if (isnan(v)) {"),
+    ("penalty divides negative logits", "const float y = (x > 0.0f) ? x / r : x * r;", "const float y = x / r;"),
+    ("presence per occurrence", "const float s = f * (float)cnt[t] + rho;", "const float s = (f + rho) * (float)cnt[t];"),
+    ("frequency ignores the count", "const float s = f * (float)cnt[t] + rho;", "const float s = f + rho;"),
+    ("history length ignored", "if (n > H) n = H;", "n = H;"),
+    ("bfloat16 ties away from zero", "if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) r = keep + 1u;",
+     "if (rest >= 0x8000u) r = keep + 1u;"),
 ]
 
 
@@ -55,7 +61,7 @@ def test_pins_catch_planted_mistake(mutant_dir, name, old, new):
         f.write(text.replace(old, new, 1))
     lib = oracle.build(force=True, src=src, out=os.path.join(mutant_dir, f"lib{tag}.so"))
     o = oracle.Oracle(lib)
-    checks = [_pins.check_worked_examples, _pins.check_closed_forms, _pins.check_uniform_mapping,
+    checks = [_pins.check_worked_examples, _pins.check_closed_forms, _pins.check_penalties, _pins.check_uniform_mapping,
               lambda x: _pins.check_bruteforce(x, n_batches=120), _pins.check_sample_frequencies]
     if _pins.triton_philox_available():
         checks.append(_pins.check_philox_vs_triton)
