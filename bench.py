@@ -56,6 +56,9 @@ def parse():
     ap.add_argument("--no-latency", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--kernel", default="auto", choices=["auto", "cluster", "stream"])
+    ap.add_argument("--penalties", type=int, default=0, metavar="H",
+                    help="run the penalty kernel (histories of up to H tokens per row) ahead of the sampler "
+                         "in every step")
     ap.add_argument("--sweep", action="store_true",
                     help="time the sweep grid (B x V x dtype, sweep workload) and print one JSON table instead")
     return ap.parse_args()
@@ -227,12 +230,40 @@ def run_reference(args):
     return 0
 
 
+def penalty_kernel_stats(pen, penalise, stream, B, V, es, calls=50):
+    """The penalty kernel timed alone (CUDA events around `calls` back-to-back launches) against its
+    algorithmic bytes: each row's history entries (4 B), a read and a write of each distinct token's
+    logit, and the row's four parameters."""
+    n = pen.hist_len.long().cpu()
+    h = pen.history.cpu()
+    distinct = 0
+    for b in range(B):
+        row = h[b, : int(n[b])]
+        distinct += int(torch.unique(row[(row >= 0) & (row < V)]).numel())
+    alg = int(4 * n.sum().item() + 2 * es * distinct + 16 * B)
+    penalise()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(calls):
+        penalise()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / calls
+    return {"history": int(pen.history.shape[1]), "kernel_us": round(us, 2), "algorithmic_bytes": alg,
+            "distinct_tokens_per_row": round(distinct / B, 1), "gbs": round(alg / (us * 1e-6) / 1e9, 1),
+            "note": "in place on the step's logits; L2-warm when timed alone (the history and the touched "
+                    "lines fit L2)"}
+
+
 def workload_config(args):
     return {"workload": f"{args.workload}_b{args.B}_v{args.V}_{args.dtype}", "B": args.B, "V": args.V,
             "logits_dtype": args.dtype, "params": "T=0.7 top_k=50 top_p=0.9 min_p=0.05" if args.workload == "decode"
             else args.workload, "parallelism": "rows sharded over ranks (replicas, no collective)",
             "l2": "inputs larger than L2 (no flush): %.0f MB of logits per step per GPU" % (
-                args.B * args.V * (4 if args.dtype == "f32" else 2) / 1e6)}
+                args.B * args.V * (4 if args.dtype == "f32" else 2) / 1e6),
+            **({"penalties": f"repetition/frequency/presence, histories of up to {args.penalties} tokens"}
+               if args.penalties else {})}
 
 
 def run_sweep(args):
@@ -304,8 +335,18 @@ def main():
     stream = torch.cuda.current_stream(dev)
     tok = torch.empty(B, dtype=torch.int32, device=dev)
     out = {"token": tok}
+    pen = None
+    if args.penalties:
+        from nucleus_token_sampler_gb300 import workloads
+        pen = workloads.penalty_inputs(B, V, args.penalties, device=dev, seed=rank)
+
+    def penalise():
+        tps.apply_penalties(w.logits, pen.history, pen.hist_len, repetition=pen.repetition,
+                            frequency=pen.frequency, presence=pen.presence)
 
     def step(i):
+        if pen is not None:
+            penalise()  # in place, as an engine does on each step's fresh logits
         tps.sample(w.logits, w.temperature, w.top_k, w.top_p, w.min_p, w.seed, i, out=out, kernel=args.kernel)
 
     for i in range(args.warmup):
@@ -345,7 +386,7 @@ def main():
     kern_ms = statistics.mean(per)
     achieved = alg_bytes / (kern_ms / 1e3) / 1e9
     peak, peak_kind = measured_peaks()
-    tag = f"{args.workload}_b{B}_v{V}_{args.dtype}"
+    tag = f"{args.workload}_b{B}_v{V}_{args.dtype}" + (f"_pen{args.penalties}" if pen is not None else "")
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
             "frac_of_8000": round(achieved / 8000.0, 4), "traffic": committed_traffic(tag),
@@ -356,11 +397,13 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32" if args.dtype == "f32" else "bf16", "data": "synthetic",
             "config": workload_config(args), "roofline": roof,
-            "gpu_launches": args.steps * tps.kernels_per_call(w.logits.dtype, B, V, args.kernel),
+            "gpu_launches": args.steps * (tps.kernels_per_call(w.logits.dtype, B, V, args.kernel) + (pen is not None)),
             "hbm_gbs": round(achieved, 1), "us_per_step": round(1e3 * ms_per_step, 2),
             "wall_s_timed": round(t_wall, 3), "cluster_size": tps.cluster_size(w.logits.dtype, B, V)}
     if clk:
         line["clocks"] = clk
+    if pen is not None:
+        line["penalties"] = penalty_kernel_stats(pen, penalise, stream, B, V, es)
 
     if rank == 0 and not args.no_latency:
         line["latency_b1"] = latency_b1(args, dev)

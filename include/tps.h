@@ -154,6 +154,38 @@ int tps_sample_full(const void* logits, int dtype, int64_t B, int64_t V, int64_t
                     int32_t* out_kept, float* out_logprob, int32_t n_top, int32_t* out_top_idx,
                     float* out_top_logprob, int kernel, void* stream);
 
+/* Longest per-row history tps_apply_penalties takes. */
+#define TPS_MAX_HISTORY 8192
+
+/*
+ * tps_apply_penalties -- repetition, frequency and presence penalties on raw logits, IN PLACE, the
+ * stage that runs ahead of the sampler ("Top-p (Nucleus) Sampling, in depth", "Where top-p sits in
+ * the sampler chain"; "What do temperature, top-k and top-p each do ...", "What interviewers probe
+ * next": on raw logits, before temperature).  For every token t occurring c_t > 0 times in the row's
+ * history:
+ *     y = z_t / r  if z_t > 0,  z_t * r  otherwise;      z_t <- y - (f * c_t + rho)
+ * computed in float32, one correctly rounded operation at a time in that order, and rounded to
+ * nearest-even bfloat16 for bfloat16 logits.  Logits of tokens not in the history are not touched.
+ *
+ *   logits      [B, ld] float32 or bfloat16 (dtype as in tps_sample), modified in place.
+ *   history     [B, ldh] int32 token ids, ldh >= H; ids outside [0, V) are ignored (use -1 to pad).
+ *               May be NULL when H == 0.
+ *   H           0 .. TPS_MAX_HISTORY entries per row; larger is TPS_ERR_ARG.
+ *   hist_len    [B] int32 or NULL: row b uses history entries [0, hist_len[b]) (clamped to [0, H]);
+ *               NULL means H for every row.
+ *   repetition  [B] float or NULL (1: off); must be finite and > 0.
+ *   frequency   [B] float or NULL (0: off); must be finite.
+ *   presence    [B] float or NULL (0: off); must be finite.
+ *   out_status  [B] int32 or NULL: TPS_ROW_OK, or TPS_ROW_BAD_PARAM for a row whose penalty values
+ *               are invalid (that row is left unchanged).
+ * All pointers are caller-owned device memory; the call allocates nothing and is stream-ordered on
+ * `stream`.  With no penalty array and no out_status it returns TPS_OK and enqueues nothing.
+ * Returns TPS_ERR_ARG / _DTYPE / _ALIGN / _UNSUPPORTED_V (V > INT32_MAX) / _CUDA as tps_sample does.
+ */
+int tps_apply_penalties(void* logits, int dtype, int64_t B, int64_t V, int64_t ld, const int32_t* history,
+                        int64_t H, int64_t ldh, const int32_t* hist_len, const float* repetition,
+                        const float* frequency, const float* presence, int32_t* out_status, void* stream);
+
 /* Kernels one tps_sample_kernel call with these arguments launches (1 or 2; 0 for arguments the call
  * would reject).  Host-only query. */
 int tps_kernels_per_call(int dtype, int64_t B, int64_t V, int kernel);

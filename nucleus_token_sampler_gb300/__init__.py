@@ -14,7 +14,7 @@ import threading
 
 import torch
 
-__all__ = ["build", "load", "sample", "TPS_F32", "TPS_BF16", "ROW_STATUS", "library_path", "max_vocab",
+__all__ = ["build", "load", "sample", "apply_penalties", "TPS_F32", "TPS_BF16", "ROW_STATUS", "library_path", "max_vocab",
            "cluster_size", "kernels_per_call", "version"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -23,8 +23,9 @@ _LIB = os.path.join(_HERE, "libtps.so")
 _INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
 # The ABI and launch code, and one translation unit per (kernel, element type): compiled in parallel.
 _SOURCES = ["tps_api.cu", "tps_k_cluster_f32.cu", "tps_k_cluster_bf16.cu", "tps_k_stream_f32.cu",
-            "tps_k_stream_bf16.cu"]
-_HEADERS = ["tps_device.cuh", "tps_common.cuh", "tps_cluster.cuh", "tps_stream.cuh", "tps_kernels.h"]
+            "tps_k_stream_bf16.cu", "tps_k_penalty.cu"]
+_HEADERS = ["tps_device.cuh", "tps_common.cuh", "tps_cluster.cuh", "tps_stream.cuh", "tps_penalty.cuh",
+            "tps_kernels.h"]
 _NVCC = ["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
          "-Xcompiler", "-fPIC"]
 
@@ -87,6 +88,8 @@ def load():
             lib.tps_sample_ex.argtypes = [P, I32, I64, I64, I64, P, P, P, P, P, U64, P, P, P, P, P, P]
             lib.tps_sample_kernel.restype = I32
             lib.tps_sample_kernel.argtypes = [P, I32, I64, I64, I64, P, P, P, P, P, U64, P, P, P, P, P, I32, P]
+            lib.tps_apply_penalties.restype = I32
+            lib.tps_apply_penalties.argtypes = [P, I32, I64, I64, I64, P, I64, I64, P, P, P, P, P, P]
             lib.tps_sample_full.restype = I32
             lib.tps_sample_full.argtypes = [P, I32, I64, I64, I64, P, P, P, P, P, U64, P, P, P, P, P, P, I32, P, P,
                                             I32, P]
@@ -155,6 +158,46 @@ def _param(x, B, dtype, device):
 
 KERNELS = {"auto": 0, "cluster": 1, "stream": 2}
 MAX_TOP = 32  # TPS_MAX_TOP
+MAX_HISTORY = 8192  # TPS_MAX_HISTORY
+
+
+def apply_penalties(logits: torch.Tensor, history: torch.Tensor, hist_len=None, *, repetition=None,
+                    frequency=None, presence=None, status: bool = False, stream=None):
+    """Apply repetition, frequency and presence penalties to ``logits`` IN PLACE (the stage ahead of
+    ``sample``).  For each token t that occurs c > 0 times in the row's history: z/r if z > 0 else
+    z*r, then minus (frequency*c + presence), in float32 (bfloat16 logits rounded back).
+
+    ``history``: [B, H] int32 CUDA tensor of token ids (ids outside [0, V) are ignored, so -1 pads);
+    ``hist_len``: optional [B] int32 (entries past it are ignored).  ``repetition``, ``frequency``,
+    ``presence``: [B] tensors or scalars, or None (off).  Returns ``logits``, or ``(logits, status)``
+    when ``status`` is set (3 marks a row with invalid penalty values, which is left unchanged).
+    """
+    if not logits.is_cuda:
+        raise ValueError("logits must be a CUDA tensor (there is no CPU path)")
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be [B, V] with unit stride along V")
+    B, V = logits.shape
+    ld = logits.stride(0) if B > 1 else V
+    dev = logits.device
+    code = _dtype_code(logits.dtype)
+    if history.dim() != 2 or history.shape[0] != B or history.dtype != torch.int32:
+        raise ValueError("history must be an int32 [B, H] tensor")
+    if history.device != dev:
+        raise ValueError("history must be on the logits' device")
+    h = history if history.stride(1) == 1 else history.contiguous()
+    H = h.shape[1]
+    ldh = h.stride(0) if B > 1 else H
+    L = None if hist_len is None else _param(hist_len, B, torch.int32, dev)
+    R = None if repetition is None else _param(repetition, B, torch.float32, dev)
+    F = None if frequency is None else _param(frequency, B, torch.float32, dev)
+    Pr = None if presence is None else _param(presence, B, torch.float32, dev)
+    st = torch.empty(B, dtype=torch.int32, device=dev) if status else None
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        rc = load().tps_apply_penalties(_ptr(logits), code, B, V, ld, _ptr(h), H, ldh, _ptr(L), _ptr(R), _ptr(F),
+                                        _ptr(Pr), _ptr(st), ctypes.c_void_p(s.cuda_stream))
+    _check(rc)
+    return (logits, st) if status else logits
 
 
 def sample(logits: torch.Tensor, temperature, top_k, top_p, min_p, seed, step: int = 0, *,

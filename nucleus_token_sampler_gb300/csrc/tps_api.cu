@@ -20,6 +20,7 @@
 #include "../../include/tps.h"
 #include "tps_cluster.cuh"
 #include "tps_kernels.h"
+#include "tps_penalty.cuh"
 #include "tps_stream.cuh"
 
 namespace {
@@ -160,6 +161,9 @@ bool wide_cluster_ok(DeviceInfo& d, int dt, int C, size_t smem)
 constexpr size_t kSmemPerBlockMax = 232448;  // 227 KB opt-in shared memory per CTA on sm_100/sm_103
 static_assert((size_t)kStreamStages * kStreamChunk + sizeof(tps::Shared) + sizeof(tps::StreamState) <= kSmemPerBlockMax,
               "the streaming kernel's ring and state must fit one CTA's shared memory");
+
+static_assert(tps::kMaxHistory == TPS_MAX_HISTORY && 2 * tps::penalty_slots(TPS_MAX_HISTORY) * sizeof(uint32_t) <= kSmemPerBlockMax,
+              "the penalty kernel's hash table for the longest history fits one CTA's shared memory");
 
 size_t stream_smem_bytes() { return (size_t)kStreamStages * kStreamChunk + sizeof(tps::Shared) + sizeof(tps::StreamState); }
 
@@ -409,6 +413,42 @@ int tps_sample_full(const void* logits, int dtype, int64_t B, int64_t V, int64_t
                                : launch_stream<__nv_bfloat16>(*d, &d->sattrs_bf16, a, true, st);
         if (e != cudaSuccess) return fail_cuda(e);
     }
+    return TPS_OK;
+}
+
+int tps_apply_penalties(void* logits, int dtype, int64_t B, int64_t V, int64_t ld, const int32_t* history, int64_t H,
+                        int64_t ldh, const int32_t* hist_len, const float* repetition, const float* frequency,
+                        const float* presence, int32_t* out_status, void* stream)
+{
+    if (B < 0 || V < 1 || ld < V || H < 0 || H > TPS_MAX_HISTORY || ldh < H) return TPS_ERR_ARG;
+    const int es = elem_bytes(dtype);
+    if (!es) return TPS_ERR_DTYPE;
+    if (B == 0) return TPS_OK;
+    if (!logits || (H > 0 && !history)) return TPS_ERR_ARG;
+    if (!aligned(logits, es) || (history && !aligned(history, 4)) || (hist_len && !aligned(hist_len, 4)) ||
+        (repetition && !aligned(repetition, 4)) || (frequency && !aligned(frequency, 4)) ||
+        (presence && !aligned(presence, 4)) || (out_status && !aligned(out_status, 4)))
+        return TPS_ERR_ALIGN;
+    if (V > INT32_MAX) return TPS_ERR_UNSUPPORTED_V;
+    if (!repetition && !frequency && !presence && !out_status) return TPS_OK;  // nothing to change or report
+
+    DeviceInfo* d = nullptr;
+    if (!device_info(&d)) return fail_cuda(cudaGetLastError());
+    tps::PenaltyArgs a;
+    a.logits = logits;
+    a.B = B;
+    a.V = V;
+    a.ld = ld;
+    a.hist = history;
+    a.H = H;
+    a.ldh = ldh;
+    a.hist_len = hist_len;
+    a.rep = repetition;
+    a.freq = frequency;
+    a.pres = presence;
+    a.out_status = out_status;
+    const cudaError_t e = tps::launch_penalties(a, dtype == TPS_BF16, d->sms, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e);
     return TPS_OK;
 }
 

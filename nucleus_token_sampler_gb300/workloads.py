@@ -199,3 +199,37 @@ def tiny_grid(seed: int, n_batches: int = 300, rows: int = 4, max_v: int = 39):
         out.append(Workload(f"tiny{bi}", z, T.float(), k, p.float(), m.float(), seeds, step=bi))
     return out
 
+
+
+@dataclasses.dataclass
+class PenaltyInputs:
+    history: torch.Tensor     # [B, H] int32 token ids (-1 pads; a few ids >= V)
+    hist_len: torch.Tensor    # [B] int32
+    repetition: torch.Tensor  # [B] float32
+    frequency: torch.Tensor   # [B] float32
+    presence: torch.Tensor    # [B] float32
+
+
+def penalty_inputs(B: int, V: int, H: int, device="cpu", seed: int = 0, bad_rows: int = 0) -> PenaltyInputs:
+    """Token histories shaped like a decode batch's generated text: 70% of the entries come from a
+    per-row pool of 32 ids (so tokens repeat), the rest uniformly from the vocabulary; 5% of the
+    entries are -1 padding and 1% are ids >= V.  Lengths are uniform in [H/2, H].  Penalty values:
+    repetition in [1, 1.5], frequency and presence in [0, 1].  The last `bad_rows` rows get an
+    invalid penalty value (repetition 0 or -1, or a NaN/inf frequency or presence)."""
+    g = _gen(device, seed + 7919)
+    pool = torch.randint(0, V, (B, 32), generator=g, device=device)
+    pick = torch.randint(0, 32, (B, H), generator=g, device=device)
+    from_pool = torch.gather(pool, 1, pick)
+    uniform = torch.randint(0, V, (B, H), generator=g, device=device)
+    r = torch.rand((B, H), generator=g, device=device)
+    hist = torch.where(r < 0.7, from_pool, uniform)
+    hist = torch.where(r > 0.95, torch.full_like(hist, -1), hist)
+    hist = torch.where((r > 0.94) & (r <= 0.95), hist + V, hist)
+    lens = torch.randint(H // 2, H + 1, (B,), generator=g, device=device)
+    rep = 1.0 + 0.5 * torch.rand(B, generator=g, device=device)
+    freq = torch.rand(B, generator=g, device=device)
+    pres = torch.rand(B, generator=g, device=device)
+    bad = [(0.0, 0.0, 0.0), (-1.0, 0.0, 0.0), (1.2, float("nan"), 0.0), (1.2, 0.0, float("inf"))]
+    for i in range(min(bad_rows, B)):
+        rep[B - 1 - i], freq[B - 1 - i], pres[B - 1 - i] = bad[i % len(bad)]
+    return PenaltyInputs(hist.to(torch.int32), lens.to(torch.int32), rep.float(), freq.float(), pres.float())

@@ -98,3 +98,25 @@ def test_sample_full_checks_the_top_token_arguments():
     assert call(3, FAKE, None) == 1               # missing log-probability output
     assert call(3, FAKE + 2, FAKE) == 4           # misaligned index output
     assert call(3, FAKE, FAKE + 1) == 4           # misaligned log-probability output
+
+
+def test_apply_penalties_checks_its_arguments():
+    lib = tps.load()
+    v = lambda p: None if p is None else ctypes.c_void_p(p)
+
+    def call(B=4, V=100, ld=100, hist=FAKE, H=8, ldh=8, lens=None, rep=FAKE, freq=None, pres=None, st=None,
+             logits=FAKE, dtype=0):
+        return lib.tps_apply_penalties(v(logits), dtype, B, V, ld, v(hist), H, ldh, v(lens), v(rep), v(freq), v(pres),
+                                       v(st), None)
+    assert call(H=tps.MAX_HISTORY + 1, ldh=tps.MAX_HISTORY + 1) == 1  # history too long
+    assert call(H=-1) == 1                                            # negative length
+    assert call(ldh=7) == 1                                           # row stride below H
+    assert call(ld=99) == 1                                           # logits stride below V
+    assert call(logits=None) == 1                                     # no logits
+    assert call(hist=None) == 1                                       # no history with H > 0
+    assert call(dtype=5) == 2                                         # unknown dtype
+    assert call(logits=FAKE + 2) == 4                                 # misaligned float32 logits
+    assert call(hist=FAKE + 1) == 4                                   # misaligned history
+    assert call(rep=FAKE + 2) == 4                                    # misaligned penalty array
+    assert call(B=0) == 0                                             # empty batch: nothing to do
+    assert call(rep=None) == 0                                        # no penalty and no status: nothing to do
