@@ -11,9 +11,10 @@ cudaError_t launch_penalties(const PenaltyArgs& a, bool bf16, int sms, cudaStrea
         const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    // Tables of a few KB let several CTAs share an SM; rows are independent.
-    const int per_sm = smem <= 8192 ? 8 : (smem <= 32768 ? 4 : 1);
-    const int64_t grid = a.B < (int64_t)sms * per_sm ? a.B : (int64_t)sms * per_sm;
+    // One CTA per row, up to 64 per SM (grid-stride beyond): the block scheduler hands rows to SMs
+    // as earlier ones finish (four 512-thread CTAs fit an SM when their tables do).
+    const int64_t cap = (int64_t)sms * 64;
+    const int64_t grid = a.B < cap ? a.B : cap;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(kPenaltyThreads, 1, 1);

@@ -8,20 +8,22 @@
 // in float32, one correctly rounded operation at a time (no contraction), rounded to nearest-even
 // bfloat16 for bfloat16 logits.  Every other logit is left as it is.
 //
-// One CTA per row (grid-stride over rows).  The row's valid history ids (those in [0, V)) are
-// counted in a shared-memory hash table of at least twice the history length (open addressing,
-// linear probing; a compare-and-swap claims a slot for an id, an integer add counts it), then every
-// occupied slot rewrites its token with the count.  Each token is written by one thread with its
-// exact count whatever the slot layout, so the result is deterministic; three barriers per row.
-// Memory traffic per row: the history (4 B per entry) plus a read and a write of each distinct
-// token's logit.
+// One CTA of 512 threads per row (up to 64 CTAs per SM, grid-stride beyond).  The row's valid
+// history ids (those in [0, V)) are counted in a shared-memory hash table of at least twice the
+// history length (open addressing, linear probing; the lanes of a warp holding the same id are
+// grouped with a match, and the group's leader claims the slot with a compare-and-swap and adds
+// the group's size); then every occupied slot rewrites its token with the count.  Each token is
+// written by one thread with its exact count whatever the slot layout, so the result is
+// deterministic; three barriers per row.  History entries and the logits a thread rewrites are
+// loaded four at a time, so their latencies overlap.  Memory traffic per row: the history (4 B per
+// entry) plus a read and a write of each distinct token's logit.
 #pragma once
 
 #include "tps_common.cuh"
 
 namespace tps {
 
-constexpr int kPenaltyThreads = 256;
+constexpr int kPenaltyThreads = 512;
 constexpr int kMaxHistory = 8192;  // history entries per row (a 128 KB hash table)
 
 struct PenaltyArgs {
@@ -41,6 +43,23 @@ __device__ __forceinline__ float pen_load(const __nv_bfloat16* p) { return __bfl
 __device__ __forceinline__ void pen_store(float* p, float v) { *p = v; }
 __device__ __forceinline__ void pen_store(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
+constexpr int kBatch = 4;  // history entries / table slots a thread handles per round
+
+// Count `k` occurrences of id t in the table (open addressing, linear probing).  At most n <= S/2
+// distinct ids are inserted, so a slot is always found within S probes.
+__device__ __forceinline__ void count_id(uint32_t* keys, uint32_t* cnt, uint32_t t, uint32_t k, int S, int sh)
+{
+    uint32_t s = (t * 0x9E3779B1u) >> sh;
+    for (int probe = 0; probe < S; ++probe) {
+        const uint32_t prev = atomicCAS(&keys[s], 0xFFFFFFFFu, t);
+        if (prev == 0xFFFFFFFFu || prev == t) {
+            atomicAdd(&cnt[s], k);
+            return;
+        }
+        s = (s + 1u) & (uint32_t)(S - 1);
+    }
+}
+
 // Hash-table slots for a history of n entries: a power of two >= max(2 n, 64).
 __host__ __device__ constexpr int penalty_slots(int64_t n)
 {
@@ -50,7 +69,7 @@ __host__ __device__ constexpr int penalty_slots(int64_t n)
 }
 
 template <typename TIn>
-__global__ void __launch_bounds__(kPenaltyThreads) penalty_rows_kernel(const PenaltyArgs a)
+__global__ void __launch_bounds__(kPenaltyThreads, 4) penalty_rows_kernel(const PenaltyArgs a)
 {
     extern __shared__ uint32_t sm[];  // keys[S], counts[S] with S = penalty_slots(H)
     constexpr uint32_t kNone = 0xFFFFFFFFu;
@@ -77,30 +96,45 @@ __global__ void __launch_bounds__(kPenaltyThreads) penalty_rows_kernel(const Pen
         }
         __syncthreads();
         const int32_t* h = a.hist + row * a.ldh;
-        for (int j = tid; j < n; j += kPenaltyThreads) {
-            const int32_t v = h[j];
-            if (v < 0 || (int64_t)v >= a.V) continue;
-            const uint32_t t = (uint32_t)v;
-            uint32_t s = (t * 0x9E3779B1u) >> sh;
-            for (int probe = 0; probe < S; ++probe) {  // at most n <= S/2 ids: a slot is always found
-                const uint32_t prev = atomicCAS(&keys[s], kNone, t);
-                if (prev == kNone || prev == t) {
-                    atomicAdd(&cnt[s], 1u);
-                    break;
-                }
-                s = (s + 1u) & (uint32_t)(S - 1);
+        const int lane = tid & 31;
+        // kBatch history entries per thread are loaded before any is counted, so their latencies
+        // overlap; whole warps run each batch together (the match needs every lane).
+        for (int base = 0; base < n; base += kBatch * kPenaltyThreads) {
+            int32_t v[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int j = base + u * kPenaltyThreads + tid;
+                v[u] = (j < n) ? h[j] : -1;
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                if (base + u * kPenaltyThreads >= n) break;  // uniform across the CTA
+                const bool valid = v[u] >= 0 && (int64_t)v[u] < a.V;
+                const uint32_t t = valid ? (uint32_t)v[u] : kNone;
+                const uint32_t peers = __match_any_sync(0xFFFFFFFFu, t);
+                if (valid && lane == __ffs(peers) - 1) count_id(keys, cnt, t, (uint32_t)__popc(peers), S, sh);
             }
         }
         __syncthreads();
+        // Every occupied slot rewrites its token: a thread's slots are read first, then written.
         TIn* zrow = static_cast<TIn*>(a.logits) + row * a.ld;
-        for (int j = tid; j < S; j += kPenaltyThreads) {
-            const uint32_t t = keys[j];
-            if (t == kNone) continue;
-            const float c = (float)cnt[j];
-            const float x = pen_load(zrow + t);
-            const float y = (x > 0.f) ? __fdiv_rn(x, r) : __fmul_rn(x, r);
-            const float s = __fadd_rn(__fmul_rn(f, c), rho);
-            pen_store(zrow + t, __fsub_rn(y, s));
+        for (int base = 0; base < S; base += kBatch * kPenaltyThreads) {
+            uint32_t t[kBatch];
+            float x[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int j = base + u * kPenaltyThreads + tid;
+                t[u] = (j < S) ? keys[j] : kNone;
+                x[u] = (t[u] != kNone) ? pen_load(zrow + t[u]) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                if (t[u] == kNone) continue;
+                const float c = (float)cnt[base + u * kPenaltyThreads + tid];
+                const float y = (x[u] > 0.f) ? __fdiv_rn(x[u], r) : __fmul_rn(x[u], r);
+                const float s = __fadd_rn(__fmul_rn(f, c), rho);
+                pen_store(zrow + t[u], __fsub_rn(y, s));
+            }
         }
         __syncthreads();  // the next row reuses the table
     }
