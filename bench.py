@@ -41,7 +41,7 @@ KERNEL_SOURCES = ["nucleus_token_sampler_gb300/csrc/tps_stream.cuh",
                   "nucleus_token_sampler_gb300/csrc/tps_api.cu"]
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
@@ -61,7 +61,7 @@ def parse():
                          "in every step")
     ap.add_argument("--sweep", action="store_true",
                     help="time the sweep grid (B x V x dtype, sweep workload) and print one JSON table instead")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def dist_env():
@@ -69,6 +69,21 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    if world == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rows_per_s(rows_per_rank: int, world: int, steps: int, total_ms: float) -> float:
+    """Whole-job throughput: every rank samples its own rows (the batch is sharded by rows, no
+    collective on the data path), timed by the slowest rank."""
+    return rows_per_rank * world * steps / (total_ms / 1e3)
 
 
 def kernel_source_hash() -> str:
@@ -384,13 +399,9 @@ def main():
     clk = clocks.stop() if clocks else None
     per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
     total_ms = ev[0].elapsed_time(ev[-1])
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
-    rows_total = B * world
-    value = rows_total * args.steps / (total_ms / 1e3)
+    value = job_rows_per_s(B, world, args.steps, total_ms)
 
     # roofline for the one kernel of the step (each step is exactly one launch)
     alg_bytes = B * (V * es + ROW_PARAM_BYTES)
