@@ -76,6 +76,35 @@ def test_sweep_large_rows_sampled(V):
     check(w, rows=np.arange(0, 64, 4), max_band_frac=0.6)
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_sweep_largest_config_sampled_rows(dtype):
+    """The sweep's largest shape, B=4096 x V=256,000 (4.2 GB of fp32 logits), in the launch
+    configuration the benchmark times; 24 rows checked against the oracle (probabilities are
+    checked at smaller sizes)."""
+    w = workloads.make("sweep", device="cpu", B=4096, V=256000, dtype=dtype)
+    rows = np.unique(np.concatenate([np.arange(8), np.arange(4096 - 8, 4096),
+                                     np.random.default_rng(1).choice(4096, 8, replace=False)]))
+    g, _, _ = check(w, rows=rows, want_probs=False, max_band_frac=0.6)
+    assert (g["status"].numpy() == 0).all()
+
+
+def test_largest_vocabulary():
+    """V = tps_max_vocab() (2^20 - 1 tokens): too wide for a 16-CTA cluster, so every kernel choice
+    that accepts it runs the streaming kernel; rows with and without min-p, greedy and masked."""
+    V = tps.max_vocab(torch.float32)
+    rng = np.random.default_rng(23)
+    z = rng.normal(0, 2.0, size=(4, V))
+    z[1, rng.choice(V, 20, replace=False)] += 9.0
+    z[3, : V // 2] = -np.inf
+    # top-p off over the whole vocabulary; min-p + top-k + top-p on a peaked row; greedy; top-k 1000
+    # on a half-masked row (no top-p, so no row sits on a top-p boundary)
+    w = _w(z, [0.9, 0.7, 0.0, 1.3], [0, 50, 0, 1000], [1.0, 0.9, 0.9, 1.0], [0.0, 0.05, 0.0, 0.0])
+    g, _, rep = check(w, kernels=["stream", "auto"])
+    assert rep["band_rows"] == 0 and g["kept"].tolist() == [V, g["kept"][1].item(), 1, 1000]
+    with pytest.raises(RuntimeError):
+        _parity.run_gpu(w, kernel="cluster")
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_tiny_vocabularies_grid(kernel):
     fails = []
