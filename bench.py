@@ -56,6 +56,9 @@ def parse(argv=None):
     ap.add_argument("--no-latency", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--kernel", default="auto", choices=["auto", "cluster", "stream"])
+    ap.add_argument("--logprobs", type=int, default=-1, metavar="N",
+                    help="also return the sampled token's processed log-probability and the top N (0..32) "
+                         "in every step")
     ap.add_argument("--penalties", type=int, default=0, metavar="H",
                     help="run the penalty kernel (histories of up to H tokens per row) ahead of the sampler "
                          "in every step")
@@ -289,7 +292,9 @@ def workload_config(args):
             "l2": "inputs larger than L2 (no flush): %.0f MB of logits per step per GPU" % (
                 args.B * args.V * (4 if args.dtype == "f32" else 2) / 1e6),
             **({"penalties": f"repetition/frequency/presence, histories of up to {args.penalties} tokens"}
-               if args.penalties else {})}
+               if args.penalties else {}),
+            **({"logprobs": f"sampled token's processed log-probability and the top {args.logprobs}"}
+               if args.logprobs >= 0 else {})}
 
 
 def run_sweep(args):
@@ -361,6 +366,13 @@ def main():
     stream = torch.cuda.current_stream(dev)
     tok = torch.empty(B, dtype=torch.int32, device=dev)
     out = {"token": tok}
+    lp_kw = {}
+    if args.logprobs >= 0:
+        n = args.logprobs
+        out.update(logprob=torch.empty(B, dtype=torch.float32, device=dev),
+                   top_idx=torch.empty((B, n), dtype=torch.int32, device=dev),
+                   top_logprob=torch.empty((B, n), dtype=torch.float32, device=dev))
+        lp_kw = {"want_logprob": True, "top_logprobs": n}
     pen = None
     if args.penalties:
         from nucleus_token_sampler_gb300 import workloads
@@ -373,7 +385,8 @@ def main():
     def step(i):
         if pen is not None:
             penalise()  # in place, as an engine does on each step's fresh logits
-        tps.sample(w.logits, w.temperature, w.top_k, w.top_p, w.min_p, w.seed, i, out=out, kernel=args.kernel)
+        tps.sample(w.logits, w.temperature, w.top_k, w.top_p, w.min_p, w.seed, i, out=out, kernel=args.kernel,
+                   **lp_kw)
 
     for i in range(args.warmup):
         step(i)
@@ -408,7 +421,8 @@ def main():
     kern_ms = statistics.mean(per)
     achieved = alg_bytes / (kern_ms / 1e3) / 1e9
     peak, peak_kind = measured_peaks()
-    tag = f"{args.workload}_b{B}_v{V}_{args.dtype}" + (f"_pen{args.penalties}" if pen is not None else "")
+    tag = f"{args.workload}_b{B}_v{V}_{args.dtype}" + (f"_pen{args.penalties}" if pen is not None else "") + (
+        f"_lp{args.logprobs}" if args.logprobs >= 0 else "")
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
             "frac_of_8000": round(achieved / 8000.0, 4), "traffic": committed_traffic(tag),
