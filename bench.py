@@ -513,47 +513,69 @@ def latency_b1(args, dev, calls=300):
     return out
 
 
-def e2e(args, w, dev, world, steps=None):
+def e2e(args, w, dev, world, steps=None, nstreams=4):
     """Same metric through the public call with host buffers: per step, pinned host logits and
-    parameters are copied to the device, the batch is sampled and the tokens are read back."""
+    parameters are copied to the device, the batch is sampled and the tokens are read back.  The
+    logits copy is split by rows over `nstreams` copy streams (several DMA engines), and the device
+    inputs are double-buffered so that one step's copy overlaps the previous step's sampling; every
+    step still copies all of its inputs inside the timed region."""
     import nucleus_token_sampler_gb300 as tps
     steps = steps or max(3, min(args.steps, 20))
     B, V = w.B, w.V
-    host = {k: getattr(w, k).cpu().pin_memory() for k in ("logits", "temperature", "top_k", "top_p", "min_p",
-                                                          "seed")}
-    dbuf = {k: torch.empty_like(getattr(w, k)) for k in host}
+    keys = ("logits", "temperature", "top_k", "top_p", "min_p", "seed")
+    host = {k: getattr(w, k).cpu().pin_memory() for k in keys}
+    bufs = [{k: torch.empty_like(getattr(w, k)) for k in keys} for _ in range(2)]
     tok_h = torch.empty(B, dtype=torch.int32).pin_memory()
     out = {"token": torch.empty(B, dtype=torch.int32, device=dev)}
     s = torch.cuda.current_stream(dev)
+    copiers = [torch.cuda.Stream(dev) for _ in range(nstreams)]
+    bounds = [B * c // nstreams for c in range(nstreams + 1)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = tok_h.numel() * 4
+    freed = [None, None]  # per buffer: an event after the last sampling that read it
 
-    def one(i):
-        for k in host:
-            dbuf[k].copy_(host[k], non_blocking=True)
-        tps.sample(dbuf["logits"], dbuf["temperature"], dbuf["top_k"], dbuf["top_p"], dbuf["min_p"], dbuf["seed"],
-                   i, out=out)
+    def one(i, gate):
+        db = bufs[i % 2]
+        ready = []
+        for c, st in enumerate(copiers):
+            st.wait_event(gate)
+            if freed[i % 2] is not None:
+                st.wait_event(freed[i % 2])
+            with torch.cuda.stream(st):
+                r0, r1 = bounds[c], bounds[c + 1]
+                db["logits"][r0:r1].copy_(host["logits"][r0:r1], non_blocking=True)
+                if c == 0:
+                    for k in keys[1:]:
+                        db[k].copy_(host[k], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(st)
+            ready.append(ev)
+        for ev in ready:
+            s.wait_event(ev)
+        tps.sample(db["logits"], db["temperature"], db["top_k"], db["top_p"], db["min_p"], db["seed"], i, out=out)
         tok_h.copy_(out["token"], non_blocking=True)
+        freed[i % 2] = torch.cuda.Event()
+        freed[i % 2].record(s)
 
+    start = torch.cuda.Event(enable_timing=True)
+    start.record(s)
     for i in range(3):
-        one(i)
+        one(i, start)
     torch.cuda.synchronize()
+    freed[0] = freed[1] = None
     if world > 1:
         torch.distributed.barrier()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(s)
     for i in range(steps):
-        one(i)
+        one(i, a)  # no copy starts before the timed region does
     b.record(s)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(a.elapsed_time(b), world, dev)
     return {"value": B * world * steps / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps}
+            "d2h_bytes_per_step": d2h, "steps": steps, "copy_streams": nstreams,
+            "h2d_gbs": round(h2d * steps / (ms / 1e3) / 1e9, 1)}
 
 
 if __name__ == "__main__":
