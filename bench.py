@@ -210,8 +210,36 @@ def cpu_baseline(w_cpu, rows_target_s=10.0, max_rows=512):
         spent += time.perf_counter() - t0
         done += len(rows)
         n = min(2 * n, max_rows)
+    # one core, on the first rows of the same workload
+    n1 = min(16, B)
+    rows = np.arange(n1)
+    t0 = time.perf_counter()
+    o.sample(w_cpu.logits[rows].double().numpy(), w_cpu.temperature[rows].numpy(), w_cpu.top_k[rows].numpy(),
+             w_cpu.top_p[rows].numpy(), w_cpu.min_p[rows].numpy(), w_cpu.seed[rows].numpy().astype(np.uint64),
+             w_cpu.step, row_ids=rows, nthreads=1)
+    one_core = n1 / (time.perf_counter() - t0)
     return {"value": done / spent, "unit": "rows/s", "cores": cores, "kind": "oracle",
-            "sample": f"{done} of {B} rows of the same workload, float64 oracle, OpenMP over rows ({spent:.1f} s)"}
+            "sample": f"{done} of {B} rows of the same workload, float64 oracle, OpenMP over rows ({spent:.1f} s)",
+            "one_core_rows_per_s": round(one_core, 1), "cpu": cpu_model()}
+
+
+def cpu_model() -> str:
+    """The host CPU as the OS describes it (model name, or the Arm implementer/part codes)."""
+    import platform
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        return platform.processor() or platform.machine()
+    for key in ("model name", "Model"):
+        for line in info:
+            if line.split(":")[0].strip() == key:
+                return line.split(":", 1)[1].strip()
+    parts = {}
+    for line in info:
+        k = line.split(":")[0].strip()
+        if k in ("CPU implementer", "CPU part") and k not in parts:
+            parts[k] = line.split(":", 1)[1].strip()
+    return f"{platform.machine()} " + " ".join(f"{k.split()[-1]} {v}" for k, v in parts.items())
 
 
 def run_reference(args):
