@@ -112,3 +112,21 @@ def test_penalties_then_sample_moves_the_greedy_choice():
     o = _parity.run_oracle(w2)
     _, fails = _parity.compare(w2, g, o)
     assert not fails, fails
+
+
+def test_penalties_history_stride_and_grid_stride():
+    """A history view whose row stride exceeds H, and more rows than the launch's CTAs (the kernel
+    caps the grid at 64 CTAs per SM and strides over the rest)."""
+    g = torch.Generator().manual_seed(13)
+    B, V = 12000, 1000
+    z = torch.randn((B, V), generator=g)
+    full = torch.randint(-1, V, (B, 48), generator=g, dtype=torch.int32)
+    hist = full[:, :20]  # stride 48 > H = 20
+    rep = 1.0 + torch.rand(B, generator=g)
+    freq = torch.rand(B, generator=g)
+    want, st_o = _oracle(z, hist.contiguous(), None, rep, freq, None)
+    zz = z.cuda()
+    _, st = tps.apply_penalties(zz, full.cuda()[:, :20], repetition=rep.cuda(), frequency=freq.cuda(), status=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(st.cpu().numpy(), st_o)
+    assert _same_bits(zz.cpu().numpy(), want)
