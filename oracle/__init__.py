@@ -51,6 +51,10 @@ class Oracle:
         lib.tpso_sample.restype = ctypes.c_int
         lib.tpso_sample.argtypes = [P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P, P, P, P, P,
                                     P, ctypes.c_uint64, P, P, P, P, P, P, P, ctypes.c_int]
+        lib.tpso_sample_rejection.restype = ctypes.c_int
+        lib.tpso_sample_rejection.argtypes = lib.tpso_sample.argtypes + [P]
+        lib.tpso_uniform_round.restype = ctypes.c_double
+        lib.tpso_uniform_round.argtypes = [ctypes.c_uint64] * 4 + [ctypes.c_uint32]
         lib.tpso_uniform.restype = ctypes.c_double
         lib.tpso_uniform.argtypes = [ctypes.c_uint64] * 4
         lib.tpso_philox4x32_10.restype = None
@@ -63,12 +67,15 @@ class Oracle:
         self.path = lib_path
 
     def sample(self, z, temperature, top_k, top_p, min_p, seed, step=0, *, row_ids=None,
-               want_probs=False, nthreads=0):
+               want_probs=False, nthreads=0, draw="race"):
         """Run the oracle on a [B, V] array of logits (widened exactly to float64).
 
         ``temperature``, ``top_p`` and ``min_p`` are rounded to float32 first (the values the GPU
         receives) and then widened, so both sides see the same numbers.  Returns a dict of numpy
         arrays: token, status, cutoff, kept, flags, z_s, z_k, n_s (+ probs when asked).
+
+        ``draw="rejection"`` draws each row by sort-free rejection rounds instead of one race over
+        the kept set (same kept set and distribution, other uniforms) and adds ``rounds``.
         """
         z = np.ascontiguousarray(np.asarray(z, dtype=np.float64))
         if z.ndim != 2:
@@ -93,10 +100,16 @@ class Oracle:
         }
         aux = np.empty((B, 3), np.float64)
         probs = np.empty((B, V), np.float64) if want_probs else None
-        rc = self.lib.tpso_sample(_ptr(z), B, V, V, _ptr(T), _ptr(K), _ptr(P), _ptr(M), _ptr(S),
-                                  _ptr(R), int(step) & ((1 << 64) - 1), _ptr(out["token"]),
-                                  _ptr(probs), _ptr(out["status"]), _ptr(out["cutoff"]),
-                                  _ptr(out["kept"]), _ptr(out["flags"]), _ptr(aux), int(nthreads))
+        args = (_ptr(z), B, V, V, _ptr(T), _ptr(K), _ptr(P), _ptr(M), _ptr(S), _ptr(R),
+                int(step) & ((1 << 64) - 1), _ptr(out["token"]), _ptr(probs), _ptr(out["status"]),
+                _ptr(out["cutoff"]), _ptr(out["kept"]), _ptr(out["flags"]), _ptr(aux), int(nthreads))
+        if draw == "race":
+            rc = self.lib.tpso_sample(*args)
+        elif draw == "rejection":
+            out["rounds"] = np.zeros(B, np.int32)
+            rc = self.lib.tpso_sample_rejection(*args, _ptr(out["rounds"]))
+        else:
+            raise ValueError("draw must be 'race' or 'rejection'")
         if rc != 0:
             raise MemoryError("oracle scratch allocation failed")
         out["z_s"], out["z_k"], out["n_s"] = aux[:, 0].copy(), aux[:, 1].copy(), aux[:, 2].copy()
@@ -134,6 +147,11 @@ class Oracle:
         """The race's uniform u in (0, 1) for (seed, row, step, token)."""
         m = (1 << 64) - 1
         return self.lib.tpso_uniform(seed & m, row & m, step & m, token & m)
+
+    def uniform_round(self, seed: int, row: int, step: int, token: int, rnd: int) -> float:
+        """The rejection draw's uniform for (seed, row, step, token) in round `rnd`."""
+        m = (1 << 64) - 1
+        return self.lib.tpso_uniform_round(seed & m, row & m, step & m, token & m, rnd)
 
     def philox4x32_10(self, counter, key):
         """One Philox4x32-10 block: counter = 4 x uint32, key = 2 x uint32 -> 4 x uint32."""

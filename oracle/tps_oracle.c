@@ -100,6 +100,20 @@ double tpso_uniform(uint64_t seed, uint64_t row, uint64_t step, uint64_t token)
     return ((double)(2u * (w >> 9) + 1u)) * 0x1p-24;
 }
 
+/* The uniform of token `token` in round `round` of the rejection draw: the same generator and
+ * mapping, with round + 1 in bits 18..31 of the counter's first word (token / 4 < 2^18 for
+ * V <= 2^20), so no round's uniforms coincide with the select path's (which has 0 there). */
+double tpso_uniform_round(uint64_t seed, uint64_t row, uint64_t step, uint64_t token, uint32_t round)
+{
+    uint32_t ctr[4] = {(uint32_t)(token / 4u) | ((round + 1u) << 18), (uint32_t)row, (uint32_t)step,
+                       (uint32_t)(step >> 32)};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t x[4];
+    tpso_philox4x32_10(ctr, key, x);
+    uint32_t w = x[token % 4u];
+    return ((double)(2u * (w >> 9) + 1u)) * 0x1p-24;
+}
+
 /* Race key of a kept token: ln P_i - ln E_i up to the row constant ln Z. */
 static double race_key(double zmax, double zi, double T, double u)
 {
@@ -130,8 +144,9 @@ typedef struct {
 /* One row, straight from the definition.  `pairs` and `e` are scratch of length V. */
 static void sample_row(const double* z, int64_t V, double T, int32_t k, double p, double m,
                        uint64_t seed, uint64_t row_id, uint64_t step, double* probs,
-                       zi_pair* pairs, double* e, row_out* r)
+                       zi_pair* pairs, double* e, row_out* r, int draw, int32_t* rounds)
 {
+    if (rounds) *rounds = 0;
     memset(r, 0, sizeof(*r));
     r->token = -1;
     r->cutoff = NAN;
@@ -246,6 +261,45 @@ static void sample_row(const double* z, int64_t V, double T, int32_t k, double p
     if (probs)
         for (int64_t t = 0; t < nk; ++t) probs[pairs[t].i] = e[pairs[t].i] / zk;
 
+    r->kept = (int32_t)nk;
+    r->cutoff = pairs[nk - 1].z;
+    r->z_s = zs;
+    r->z_k = zk;
+    r->n_s = (double)ns;
+
+    if (draw == 1) {
+        /* Sort-free top-p by rejection ([NS] "Sort-free top-p by rejection sampling"): each round
+         * races among the survivors above the pivot (all of S at first), in proportion to e_i; the
+         * winner t is accepted when the mass of strictly more probable survivors is below p * Z_S
+         * -- the same test that defines the kept set, so the class of the maximum always passes --
+         * and otherwise t's logit becomes the pivot, dropping t's class and everything below. */
+        double zpiv = -INFINITY;
+        for (uint32_t round = 0; round < (1u << 16); ++round) {
+            double best = -INFINITY;
+            int64_t arg = -1;
+            for (int64_t t = 0; t < ns; ++t) {
+                if (!(pairs[t].z > zpiv)) continue;
+                int64_t i = pairs[t].i;
+                double key = race_key(zmax, z[i], T, tpso_uniform_round(seed, row_id, step, (uint64_t)i, round));
+                if (key > best || (key == best && i < arg)) {
+                    best = key;
+                    arg = i;
+                }
+            }
+            double above = 0.0;
+            for (int64_t t = 0; t < ns; ++t)
+                if (pairs[t].z > z[arg]) above += e[pairs[t].i];
+            if (rounds) *rounds = (int32_t)(round + 1);
+            if (z[arg] == zmax || p >= 1.0 || above < p * zs) {
+                r->token = (int32_t)arg;
+                return;
+            }
+            zpiv = z[arg];
+        }
+        r->token = -1; /* unreachable: every rejection removes at least one class */
+        return;
+    }
+
     /* Exponential race over the kept set ([ORD] "A strong answer": argmax p / Exp(1)). */
     double best = -INFINITY, second = -INFINITY;
     int64_t arg = -1;
@@ -264,11 +318,6 @@ static void sample_row(const double* z, int64_t V, double T, int32_t k, double p
     if (nk > 1 && best - second <= RACE_BAND * fmax(1.0, fabs(best))) r->flags |= TPSO_FLAG_RACE_BAND;
 
     r->token = (int32_t)arg;
-    r->kept = (int32_t)nk;
-    r->cutoff = pairs[nk - 1].z;
-    r->z_s = zs;
-    r->z_k = zk;
-    r->n_s = (double)ns;
 }
 
 /*
@@ -278,11 +327,11 @@ static void sample_row(const double* z, int64_t V, double T, int32_t k, double p
  * out_probs ([B, V], nullable) and out_aux ([B, 3] = Z_S, Z_K, |S|, nullable).
  * nthreads <= 0 uses the OpenMP default.  Returns 0, or -1 when scratch cannot be allocated.
  */
-int tpso_sample(const double* z, int64_t B, int64_t V, int64_t ld, const double* T, const int32_t* k,
-                const double* p, const double* m, const uint64_t* seed, const int64_t* row_ids,
-                uint64_t step, int32_t* out_token, double* out_probs, int32_t* out_status,
-                double* out_cutoff, int32_t* out_kept, int32_t* out_flags, double* out_aux,
-                int nthreads)
+static int sample_batch(const double* z, int64_t B, int64_t V, int64_t ld, const double* T, const int32_t* k,
+                        const double* p, const double* m, const uint64_t* seed, const int64_t* row_ids,
+                        uint64_t step, int32_t* out_token, double* out_probs, int32_t* out_status,
+                        double* out_cutoff, int32_t* out_kept, int32_t* out_flags, double* out_aux,
+                        int nthreads, int draw, int32_t* out_rounds)
 {
     if (B <= 0) return 0;
     int failed = 0;
@@ -306,7 +355,8 @@ int tpso_sample(const double* z, int64_t B, int64_t V, int64_t ld, const double*
                 row_out r;
                 uint64_t rid = row_ids ? (uint64_t)row_ids[b] : (uint64_t)b;
                 sample_row(z + b * ld, V, T[b], k[b], p[b], m[b], seed[b], rid, step,
-                           out_probs ? out_probs + b * V : NULL, pairs, e, &r);
+                           out_probs ? out_probs + b * V : NULL, pairs, e, &r, draw,
+                           out_rounds ? out_rounds + b : NULL);
                 out_token[b] = r.token;
                 if (out_status) out_status[b] = r.status;
                 if (out_cutoff) out_cutoff[b] = r.cutoff;
@@ -323,6 +373,28 @@ int tpso_sample(const double* z, int64_t B, int64_t V, int64_t ld, const double*
         free(e);
     }
     return failed ? -1 : 0;
+}
+
+int tpso_sample(const double* z, int64_t B, int64_t V, int64_t ld, const double* T, const int32_t* k,
+                const double* p, const double* m, const uint64_t* seed, const int64_t* row_ids,
+                uint64_t step, int32_t* out_token, double* out_probs, int32_t* out_status,
+                double* out_cutoff, int32_t* out_kept, int32_t* out_flags, double* out_aux,
+                int nthreads)
+{
+    return sample_batch(z, B, V, ld, T, k, p, m, seed, row_ids, step, out_token, out_probs, out_status, out_cutoff,
+                        out_kept, out_flags, out_aux, nthreads, 0, NULL);
+}
+
+/* The same rows drawn by rejection rounds instead of one race over the kept set (same kept set,
+ * same distribution, different uniforms); out_rounds[b] = rounds row b took. */
+int tpso_sample_rejection(const double* z, int64_t B, int64_t V, int64_t ld, const double* T, const int32_t* k,
+                          const double* p, const double* m, const uint64_t* seed, const int64_t* row_ids,
+                          uint64_t step, int32_t* out_token, double* out_probs, int32_t* out_status,
+                          double* out_cutoff, int32_t* out_kept, int32_t* out_flags, double* out_aux,
+                          int nthreads, int32_t* out_rounds)
+{
+    return sample_batch(z, B, V, ld, T, k, p, m, seed, row_ids, step, out_token, out_probs, out_status, out_cutoff,
+                        out_kept, out_flags, out_aux, nthreads, 1, out_rounds);
 }
 
 int tpso_max_threads(void)

@@ -455,7 +455,68 @@ def check_penalties(o):
     return fails
 
 
+def _expected_rounds(e_sorted_classes, n_kept_classes):
+    """Mean rounds of the rejection draw, by recursion over the classes (descending): with the
+    top j classes eligible, one round draws class c with probability m_c / M_j; a kept class ends
+    the draw, any other leaves its upper classes (1..c-1) eligible."""
+    m = np.asarray(e_sorted_classes, np.float64)
+    E = np.ones(len(m) + 1)
+    for j in range(n_kept_classes + 1, len(m) + 1):
+        M = m[:j].sum()
+        E[j] = 1.0 + sum(m[c - 1] / M * E[c - 1] for c in range(n_kept_classes + 1, j + 1))
+    return E[len(m)]
+
+
+def check_rejection(o):
+    """The sort-free rejection draw: the page's printed run (frequencies and mean rounds), the exact
+    distribution and expected rounds, and membership of every draw in the kept set."""
+    fails = []
+    for c in _golden()["rejection_frequencies"]:
+        z = np.asarray(c["logits"], np.float64)
+        n = int(c["draws"])
+        seeds = np.arange(n, dtype=np.uint64) * np.uint64(0x9E3779B97F4A7C15) + np.uint64(999)
+        r = o.sample(np.tile(z, (n, 1)), np.float32(c["temperature"]), 0, np.float32(c["top_p"]), 0.0, seeds,
+                     step=3, draw="rejection")
+        exact = _run1(o, z, c["temperature"], c["top_p"])["probs"][0]
+        freq = np.bincount(r["token"], minlength=len(z)) / n
+        sig = np.sqrt(exact * (1 - exact) / n)
+        if np.any(np.abs(freq - exact) > 5 * sig + 1e-12):
+            fails.append(f"{c['id']}: frequencies {np.round(freq, 4)} vs exact {np.round(exact, 4)}")
+        want = np.asarray(c["frequencies"])
+        k = len(want)
+        if np.any(np.abs(freq[:k] - want) > 5 * np.sqrt(2) * sig[:k] + 6e-4):
+            fails.append(f"{c['id']}: frequencies {np.round(freq[:k], 4)} vs printed {want}")
+        # expected rounds: distinct logits here, so every token is its own class
+        e = np.exp(-(z.max() - np.sort(z)[::-1]) / np.float64(np.float32(c["temperature"])))
+        Er = _expected_rounds(e, int((exact > 0).sum()))
+        mr, sr = r["rounds"].mean(), r["rounds"].std() / np.sqrt(n)
+        if abs(mr - Er) > 5 * sr + 1e-12:
+            fails.append(f"{c['id']}: mean rounds {mr:.4f} vs expected {Er:.4f}")
+        if abs(mr - c["mean_rounds"]) > 5 * np.sqrt(2) * sr + 0.005:
+            fails.append(f"{c['id']}: mean rounds {mr:.4f} vs printed {c['mean_rounds']}")
+    # every draw lies in the kept set; greedy rows match the race; no top-p means one round
+    for w in _tiny_batches(n_batches=150):
+        args = (w.logits.double().numpy(), w.temperature.numpy(), w.top_k.numpy(), w.top_p.numpy(),
+                w.min_p.numpy(), w.seed.numpy().astype(np.uint64), w.step)
+        a, b = o.sample(*args), o.sample(*args, draw="rejection")
+        zz = w.logits.double().numpy()
+        for i in range(w.B):
+            if a["status"][i] != 0:
+                if b["token"][i] != -1:
+                    fails.append(f"{w.name} row {i}: failed row drew a token")
+                continue
+            t = b["token"][i]
+            if not (t >= 0 and np.isfinite(zz[i, t]) and zz[i, t] >= a["cutoff"][i]):
+                fails.append(f"{w.name} row {i}: rejection draw {t} outside the kept set")
+            if w.temperature[i] <= 0 and t != a["token"][i]:
+                fails.append(f"{w.name} row {i}: greedy row differs")
+            if w.temperature[i] > 0 and w.top_p[i] >= 1 and b["rounds"][i] != 1:
+                fails.append(f"{w.name} row {i}: {b['rounds'][i]} rounds with top-p off")
+    return fails
+
+
 ALL_CHECKS = {
+    "rejection": check_rejection,
     "penalties": check_penalties,
     "worked_examples": check_worked_examples,
     "sample_frequencies": check_sample_frequencies,

@@ -41,6 +41,9 @@ MUTANTS = [
     ("presence per occurrence", "const float s = f * (float)cnt[t] + rho;", "const float s = (f + rho) * (float)cnt[t];"),
     ("frequency ignores the count", "const float s = f * (float)cnt[t] + rho;", "const float s = f + rho;"),
     ("history length ignored", "if (n > H) n = H;", "n = H;"),
+    ("rejection counts the winner's class as above", "if (pairs[t].z > z[arg]) above += e[pairs[t].i];",
+     "if (pairs[t].z >= z[arg]) above += e[pairs[t].i];"),
+    ("rejection never raises the pivot", "            zpiv = z[arg];\n", "            (void)zpiv;\n"),
     ("bfloat16 ties away from zero", "if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) r = keep + 1u;",
      "if (rest >= 0x8000u) r = keep + 1u;"),
 ]
@@ -61,7 +64,8 @@ def test_pins_catch_planted_mistake(mutant_dir, name, old, new):
         f.write(text.replace(old, new, 1))
     lib = oracle.build(force=True, src=src, out=os.path.join(mutant_dir, f"lib{tag}.so"))
     o = oracle.Oracle(lib)
-    checks = [_pins.check_worked_examples, _pins.check_closed_forms, _pins.check_penalties, _pins.check_uniform_mapping,
+    checks = [_pins.check_worked_examples, _pins.check_closed_forms, _pins.check_penalties, _pins.check_rejection,
+              _pins.check_uniform_mapping,
               lambda x: _pins.check_bruteforce(x, n_batches=120), _pins.check_sample_frequencies]
     if _pins.triton_philox_available():
         checks.append(_pins.check_philox_vs_triton)
