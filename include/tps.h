@@ -8,6 +8,8 @@
  * p_i(T) equation, the engine order and the exponential-race draw) and "Implement batched top-p
  * sampling with temperature" ('How to approach it': keep token i iff the mass of strictly more
  * probable tokens is below p; 'A strong answer': the greedy branch and per-request p).
+ * An optional stage ahead of that chain, tps_apply_penalties, applies repetition, frequency and
+ * presence penalties to the raw logits in place.
  *
  * Rules, per row (T = temperature[b], k = top_k[b], p = top_p[b], m = min_p[b]):
  *   - T <= 0: greedy; the token is the lowest index holding the largest logit.
@@ -26,7 +28,8 @@
  * Calling convention (all entry points):
  *   - every pointer argument is a DEVICE pointer owned by the caller, except where marked; the
  *     library allocates no memory per call, never synchronises the host, keeps no state between
- *     calls and may be called from several host threads at once;
+ *     calls beyond a per-device cache of queried limits, and may be called from several host
+ *     threads at once;
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream); all work is enqueued on it;
  *   - the return value is a tps_status; errors in the arguments are reported before anything is
  *     enqueued; problems in a row's data are reported per row in out_status and never abort the
