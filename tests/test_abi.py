@@ -17,6 +17,41 @@ def declared_symbols():
     return sorted(set(re.findall(r"\b(tps_[a-z0-9_]+)\s*\(", text)))
 
 
+def declarations():
+    """name -> (return type, [parameter types]) for every function the header declares."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for ret, name, params in re.findall(r"([A-Za-z_][\w \*]*?)\s*\b(tps_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", text):
+        ps = [q.strip() for q in params.split(",") if q.strip() and q.strip() != "void"]
+        types = [re.sub(r"\s*\b\w+$", "", q) if not q.endswith("*") else q for q in ps]
+        out[name] = (ret.strip(), types)
+    return out
+
+
+_CTYPE = {"int": ctypes.c_int, "int32_t": ctypes.c_int, "int64_t": ctypes.c_int64, "uint64_t": ctypes.c_uint64,
+          "const char*": ctypes.c_char_p}
+
+
+def _ctype_of(decl: str):
+    d = decl.replace(" *", "*").strip()
+    return ctypes.c_void_p if d.endswith("*") and d != "const char*" else _CTYPE[d]
+
+
+def test_binding_signatures_match_the_header():
+    """Every entry point's ctypes signature in the binding has the header's parameter count and
+    types, and its return type (a mismatch would pass wrong values silently)."""
+    lib = tps.load()
+    decls = declarations()
+    assert set(decls) == set(declared_symbols())
+    for name, (ret, params) in decls.items():
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, f"{name}: no argtypes in the binding"
+        assert len(fn.argtypes) == len(params), f"{name}: {len(fn.argtypes)} argtypes, header has {len(params)}"
+        for i, (have, want) in enumerate(zip(fn.argtypes, params)):
+            assert have == _ctype_of(want), f"{name} parameter {i}: binding {have}, header {want!r}"
+        assert fn.restype == _ctype_of(ret), f"{name}: return {fn.restype}, header {ret!r}"
+
+
 def test_header_declares_entry_points():
     syms = declared_symbols()
     for s in ("tps_sample", "tps_sample_ex", "tps_max_vocab", "tps_cluster_size", "tps_status_string",
