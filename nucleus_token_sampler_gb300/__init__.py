@@ -156,6 +156,22 @@ def _param(x, B, dtype, device):
     return x.contiguous()
 
 
+def _out(res, name, shape, dtype, device):
+    """The caller's output tensor `name` from `res` after checking it, or a new one.  The kernels
+    write through raw pointers, so a buffer of the wrong shape, dtype or device, or a strided view,
+    would be written out of bounds or misread: it is rejected here."""
+    t = res.get(name)
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"out[{name!r}] must be a tensor")
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype or t.device != device or not t.is_contiguous():
+        raise ValueError(f"out[{name!r}] must be a contiguous {dtype} tensor of shape {tuple(shape)} on {device}, "
+                         f"got {t.dtype} {tuple(t.shape)} on {t.device}"
+                         + ("" if t.is_contiguous() else " (not contiguous)"))
+    return t
+
+
 KERNELS = {"auto": 0, "cluster": 1, "stream": 2}
 MAX_TOP = 32  # TPS_MAX_TOP
 MAX_HISTORY = 8192  # TPS_MAX_HISTORY
@@ -184,16 +200,19 @@ def apply_penalties(logits: torch.Tensor, history: torch.Tensor, hist_len=None, 
         raise ValueError("history must be an int32 [B, H] tensor")
     if history.device != dev:
         raise ValueError("history must be on the logits' device")
-    h = history if history.stride(1) == 1 else history.contiguous()
-    H = h.shape[1]
-    ldh = h.stride(0) if B > 1 else H
-    L = None if hist_len is None else _param(hist_len, B, torch.int32, dev)
-    R = None if repetition is None else _param(repetition, B, torch.float32, dev)
-    F = None if frequency is None else _param(frequency, B, torch.float32, dev)
-    Pr = None if presence is None else _param(presence, B, torch.float32, dev)
-    st = torch.empty(B, dtype=torch.int32, device=dev) if status else None
     s = stream if stream is not None else torch.cuda.current_stream(dev)
-    with torch.cuda.device(dev):
+    # Every temporary (converted parameters, a contiguous copy of the history) is made on the stream
+    # the kernel runs on, so it is written before the kernel reads it and its memory is not handed to
+    # other work until the kernel is done with it.
+    with torch.cuda.device(dev), torch.cuda.stream(s):
+        h = history if history.stride(1) == 1 else history.contiguous()
+        H = h.shape[1]
+        ldh = h.stride(0) if B > 1 else H
+        L = None if hist_len is None else _param(hist_len, B, torch.int32, dev)
+        R = None if repetition is None else _param(repetition, B, torch.float32, dev)
+        F = None if frequency is None else _param(frequency, B, torch.float32, dev)
+        Pr = None if presence is None else _param(presence, B, torch.float32, dev)
+        st = torch.empty(B, dtype=torch.int32, device=dev) if status else None
         rc = load().tps_apply_penalties(_ptr(logits), code, B, V, ld, _ptr(h), H, ldh, _ptr(L), _ptr(R), _ptr(F),
                                         _ptr(Pr), _ptr(st), ctypes.c_void_p(s.cuda_stream))
     _check(rc)
@@ -225,41 +244,33 @@ def sample(logits: torch.Tensor, temperature, top_k, top_p, min_p, seed, step: i
     ld = logits.stride(0) if B > 1 else V
     dev = logits.device
     code = _dtype_code(logits.dtype)
-    T = _param(temperature, B, torch.float32, dev)
-    K = _param(top_k, B, torch.int32, dev)
-    P = _param(top_p, B, torch.float32, dev)
-    M = _param(min_p, B, torch.float32, dev)
-    S = _param(seed, B, torch.int64, dev)
-    res = out if out is not None else {}
-    tok = res.get("token")
-    if tok is None:
-        tok = torch.empty(B, dtype=torch.int32, device=dev)
-    probs = res.get("probs") if want_probs else None
-    if want_probs and probs is None:
-        probs = torch.empty((B, V), dtype=torch.float32, device=dev)
-    st = cut = kept = None
-    if diagnostics:
-        st = res.get("status", None)
-        st = st if st is not None else torch.empty(B, dtype=torch.int32, device=dev)
-        cut = res.get("cutoff", None)
-        cut = cut if cut is not None else torch.empty(B, dtype=torch.float32, device=dev)
-        kept = res.get("kept", None)
-        kept = kept if kept is not None else torch.empty(B, dtype=torch.int32, device=dev)
-    lp = None
-    if want_logprob:
-        lp = res.get("logprob", None)
-        lp = lp if lp is not None else torch.empty(B, dtype=torch.float32, device=dev)
     n_top = int(top_logprobs)
     if not 0 <= n_top <= MAX_TOP:
         raise ValueError(f"top_logprobs must lie in [0, {MAX_TOP}]")
-    ti = tl = None
-    if n_top:
-        ti = res.get("top_idx", None)
-        ti = ti if ti is not None else torch.empty((B, n_top), dtype=torch.int32, device=dev)
-        tl = res.get("top_logprob", None)
-        tl = tl if tl is not None else torch.empty((B, n_top), dtype=torch.float32, device=dev)
+    if kernel not in KERNELS:
+        raise ValueError(f"kernel must be one of {sorted(KERNELS)}")
+    res = out if out is not None else {}
     s = stream if stream is not None else torch.cuda.current_stream(dev)
-    with torch.cuda.device(dev):
+    # Parameters converted here and outputs allocated here are made on the stream the kernel runs on
+    # (see apply_penalties).
+    with torch.cuda.device(dev), torch.cuda.stream(s):
+        T = _param(temperature, B, torch.float32, dev)
+        K = _param(top_k, B, torch.int32, dev)
+        P = _param(top_p, B, torch.float32, dev)
+        M = _param(min_p, B, torch.float32, dev)
+        S = _param(seed, B, torch.int64, dev)
+        tok = _out(res, "token", (B,), torch.int32, dev)
+        probs = _out(res, "probs", (B, V), torch.float32, dev) if want_probs else None
+        st = cut = kept = None
+        if diagnostics:
+            st = _out(res, "status", (B,), torch.int32, dev)
+            cut = _out(res, "cutoff", (B,), torch.float32, dev)
+            kept = _out(res, "kept", (B,), torch.int32, dev)
+        lp = _out(res, "logprob", (B,), torch.float32, dev) if want_logprob else None
+        ti = tl = None
+        if n_top:
+            ti = _out(res, "top_idx", (B, n_top), torch.int32, dev)
+            tl = _out(res, "top_logprob", (B, n_top), torch.float32, dev)
         rc = load().tps_sample_full(_ptr(logits), code, B, V, ld, _ptr(T), _ptr(K), _ptr(P), _ptr(M), _ptr(S),
                                     int(step) & ((1 << 64) - 1), _ptr(tok), _ptr(probs), _ptr(st), _ptr(cut),
                                     _ptr(kept), _ptr(lp), n_top, _ptr(ti), _ptr(tl), KERNELS[kernel],

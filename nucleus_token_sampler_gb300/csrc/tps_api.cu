@@ -48,12 +48,16 @@ constexpr int kStreamStages = 3;
 constexpr uint32_t kStreamChunk = 64u * 1024u;
 constexpr int64_t kStreamMinRows = 32;  // batches at least this large use the streaming kernel
 
+// Per-device limits, filled once under g_mu and published through `ready` (release/acquire), so a
+// thread that sees ready == true also sees sms and smem_optin.  The attribute flags only record that
+// cudaFuncSetAttribute has succeeded once; setting an attribute twice is harmless, so they need no
+// lock, only atomic access.
 struct DeviceInfo {
-    bool ready = false;
+    std::atomic<bool> ready{false};
     int sms = 0;
     int smem_optin = 0;
-    bool attrs_f32 = false, attrs_bf16 = false;
-    bool sattrs_f32 = false, sattrs_bf16 = false;
+    std::atomic<bool> attrs_f32{false}, attrs_bf16{false};
+    std::atomic<bool> sattrs_f32{false}, sattrs_bf16{false};
     // Largest dynamic shared memory per CTA seen to co-schedule a cluster of 9..16 CTAs, per dtype
     // (0 = not known yet).
     std::atomic<long> wide_ok[2][kMaxCluster + 1];
@@ -70,13 +74,16 @@ bool device_info(DeviceInfo** out)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
     DeviceInfo& d = g_dev[dev];
-    if (!d.ready) {
+    if (!d.ready.load(std::memory_order_acquire)) {
         std::lock_guard<std::mutex> lk(g_mu);
-        if (!d.ready) {
-            if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
-            if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        if (!d.ready.load(std::memory_order_relaxed)) {
+            int sms = 0, optin = 0;
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+            if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
                 return false;
-            d.ready = true;
+            d.sms = sms;
+            d.smem_optin = optin;
+            d.ready.store(true, std::memory_order_release);
         }
     }
     *out = &d;
@@ -171,15 +178,15 @@ size_t stream_smem_bytes() { return (size_t)kStreamStages * kStreamChunk + sizeo
 // in the stream (the cluster kernel of a split batch), so its CTAs may start on SMs that kernel has
 // already released.
 template <typename TIn>
-cudaError_t launch_stream(const DeviceInfo& d, bool* attrs_done, const tps::Args& a, bool dependent,
+cudaError_t launch_stream(const DeviceInfo& d, std::atomic<bool>* attrs_done, const tps::Args& a, bool dependent,
                           cudaStream_t stream)
 {
     auto k = stream_kernel<TIn>();
     const size_t smem = stream_smem_bytes();
-    if (!*attrs_done) {
+    if (!attrs_done->load(std::memory_order_acquire)) {
         const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        *attrs_done = true;
+        attrs_done->store(true, std::memory_order_release);
     }
     const int64_t grid = a.B < (int64_t)d.sms ? a.B : (int64_t)d.sms;
     cudaLaunchConfig_t cfg = {};
@@ -386,19 +393,19 @@ int tps_sample_full(const void* logits, int dtype, int64_t B, int64_t V, int64_t
         return true;
     };
     if (dtype == TPS_F32) {
-        if (!d->attrs_f32) {
+        if (!d->attrs_f32.load(std::memory_order_acquire)) {
             e = prepare_kernel<float>(*d);
             if (e != cudaSuccess) return fail_cuda(e);
-            d->attrs_f32 = true;
+            d->attrs_f32.store(true, std::memory_order_release);
         }
         if (Cl > 8 && !wide_cluster_ok<float>(*d, 0, Cl, sm) && !use_portable()) return TPS_ERR_UNSUPPORTED_V;
         const int64_t ncl = split ? std::min<int64_t>(B, resident_clusters<float>(*d, 0, Cl, sm)) : B;
         e = launch<float>(a, Cl, sm, ncl, st);
     } else {
-        if (!d->attrs_bf16) {
+        if (!d->attrs_bf16.load(std::memory_order_acquire)) {
             e = prepare_kernel<__nv_bfloat16>(*d);
             if (e != cudaSuccess) return fail_cuda(e);
-            d->attrs_bf16 = true;
+            d->attrs_bf16.store(true, std::memory_order_release);
         }
         if (Cl > 8 && !wide_cluster_ok<__nv_bfloat16>(*d, 1, Cl, sm) && !use_portable())
             return TPS_ERR_UNSUPPORTED_V;

@@ -430,6 +430,15 @@ __device__ __forceinline__ uint32_t bin_pos16(float d32, int b)
     return __float_as_uint(__fmaf_rn(d32 - (float)b, 65536.f, 0x1p23f)) - 0x4B000000u;
 }
 
+// Whether a scaled distance d32 falls in the fine bins [b_lo, b_end).  The last bin has no upper
+// bound: it holds every d32 >= kFineBins - 1, including +inf (a temperature small enough to overflow
+// (zmax - z) / T), so ranges are always tested through fine_bin, never against a float bound.
+__device__ __forceinline__ bool in_bins(float d32, int b_lo, int b_end)
+{
+    const int b = fine_bin(d32);
+    return b >= b_lo && b < b_end;
+}
+
 // Cluster-wide sum of the CTAs' fine histograms hc into hr (a copy for a cluster of one CTA; nothing
 // to do when hr is hc itself).
 // Starts with a topology barrier: every CTA's histogram and published values are then complete,
@@ -786,11 +795,11 @@ __device__ __forceinline__ double race_key64(const RowCtx& r, float z, float u) 
 // kept tokens have d <= dcut.
 __device__ __forceinline__ float race_tol(float dcut) { return 1e-5f + 1e-6f * dcut; }
 
-// Refine the cut among the survivors (min-p, key >= key_lo) whose scaled distance d32 lies in
-// [flo, fhi), given the (count, mass) of the survivors above that range.  Exact: ends with a sorted
+// Refine the cut among the survivors (min-p, key >= key_lo) whose scaled distance d32 lies in the
+// fine bins [b_lo, b_end), given the (count, mass) of the survivors above that range.  Exact: ends with a sorted
 // candidate list or with a single logit value.  Starts with a topology barrier.
 template <typename Topo, typename Src>
-__device__ Sel refine_range(Topo& topo, Shared& s, const Src& sl, const RowCtx& r, float zc, float flo, float fhi,
+__device__ Sel refine_range(Topo& topo, Shared& s, const Src& sl, const RowCtx& r, float zc, int b_lo, int b_end,
                             uint32_t key_lo, const Crit& cr, uint64_t C0, uint64_t A0)
 {
     const uint32_t C = topo.C;
@@ -808,10 +817,7 @@ __device__ Sel refine_range(Topo& topo, Shared& s, const Src& sl, const RowCtx& 
             const uint32_t key = fkey(z);
             if (key < key_lo || key < lo || key > hi) return;
             const float d = dist(r, z);
-            if (by_range) {
-                const float d32 = d * kFineScale;
-                if (!(d32 >= flo && d32 < fhi)) return;
-            }
+            if (by_range && !in_bins(d * kFineScale, b_lo, b_end)) return;
             if (!minp_ok(r, z, d)) return;
             ++lcnt;
             lmin = min(lmin, key);
@@ -1643,11 +1649,10 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
             topo.sync();  // the other CTAs are done with this CTA's published values
             if (tid == 0) s.ncand = 0;
             cta_sync();
-            const float fend = (bk >= kFineBins - 1) ? INFINITY : (float)(bk + 1);
             src.for_each(s, [&](float z, int32_t i) {
                 if (!(z > zc)) return;
                 const float d = dist(r, z);
-                if (!(d * kFineScale < fend) || !minp_ok(r, z, d)) return;
+                if (fine_bin(d * kFineScale) > bk || !minp_ok(r, z, d)) return;
                 const uint32_t slot = atomicAdd(&s.ncand, 1u);
                 s.ckey[slot] = fkey(z);
                 s.cidx[slot] = (uint32_t)i;
@@ -1664,8 +1669,7 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
         ck2.by_mass = false;
         ck2.tcnt = (uint64_t)K;
         ck2.tmass = 0.0;
-        const float fhi = (bk >= kFineBins - 1) ? INFINITY : (float)(bk + 1);
-        const Sel sk = refine_range(topo, s, src, r, zc, (float)bk, fhi, 0u, ck2, ck, 0);
+        const Sel sk = refine_range(topo, s, src, r, zc, bk, bk + 1, 0u, ck2, ck, 0);
         key_k = sk.key;
         NS = sk.cnt;
         part = (uint32_t)(sk.cnt - ck);
@@ -1680,7 +1684,7 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
             c1.by_mass = false;
             c1.tcnt = 1;
             c1.tmass = 0.0;
-            const Sel s1 = refine_range(topo, s, src, r, zc, 0.f, 1.f, key_k, c1, 0, 0);
+            const Sel s1 = refine_range(topo, s, src, r, zc, 0, 1, key_k, c1, 0, 0);
             res.key_cut = s1.key;
             res.nk = s1.cnt;
             res.zk = s1.mass;
@@ -1749,8 +1753,10 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
             w.list = false;
             race.init();
         }
+        // window bins [b_lo, b_end); a window reaching the last bin has no upper bound (d = +inf included)
         const float flo = (float)w.b_lo;
-        const float fend = (w.b_end >= kFineBins) ? INFINITY : (float)w.b_end;
+        const bool open_end = w.b_end >= kFineBins;
+        const float fend = open_end ? INFINITY : (float)w.b_end;
         const bool list = w.list;
         const int b_lo = w.b_lo, sh = w.sh;
         topo.sync();  // nobody still reads this CTA's window sums, lists or published values
@@ -1775,7 +1781,7 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
             zlo += f.lo;
             const float d32 = d * kFineScale;
             if (list) {
-                if (d32 < fend) {
+                if (open_end || d32 < fend) {
                     const uint32_t slot = atomicAdd(&s.ncand, 1u);
                     s.ckey[slot] = key;
                     s.cidx[slot] = (uint32_t)i;
@@ -1788,7 +1794,7 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
                 ++ca;
                 return !(16.64f - d < race.t2.k2);
             }
-            if (d32 < fend) {
+            if (open_end || d32 < fend) {
                 const int g = (fine_bin(d32) - b_lo) >> sh;
                 atomicAdd((unsigned long long*)&s.wmass[g], (unsigned long long)(((uint64_t)f.hi << 22) + f.lo));
                 atomicAdd(&s.wcnt[g], 1u);
@@ -1907,8 +1913,7 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
     cp.by_mass = true;
     cp.tcnt = 1;
     cp.tmass = tmass;
-    const Sel sp = refine_range(topo, s, src, r, zc, (float)g_lo, (g_end >= kFineBins) ? INFINITY : (float)g_end,
-                                key_k, cp, C0, A0);
+    const Sel sp = refine_range(topo, s, src, r, zc, g_lo, g_end, key_k, cp, C0, A0);
     res.key_cut = max(sp.key, key_k);
     res.nk = sp.cnt;
     res.zk = sp.mass;
@@ -2032,12 +2037,10 @@ __device__ __noinline__ void general_top(Topo& topo, Shared& s, const Src& src, 
         ck.by_mass = false;
         ck.tcnt = Kt;
         ck.tmass = 0.0;
-        const float fhi = (bn >= kFineBins - 1) ? INFINITY : (float)(bn + 1);
-        const Sel sk = refine_range(topo, s, src, r, zc, (float)bn, fhi, 0u, ck, cn, 0);
+        const Sel sk = refine_range(topo, s, src, r, zc, bn, bn + 1, 0u, ck, cn, 0);
         key_lo = sk.key;
         if (sk.cnt > (uint64_t)kCand) key_lo = sk.key + 1u;  // the tie class at sk.key is resolved below
     }
-    const float fend = (bn >= kFineBins - 1) ? INFINITY : (float)(bn + 1);
     topo.sync();  // nobody still reads this CTA's lists or published values
     if (threadIdx.x == 0) s.ncand = 0;
     cta_sync();
@@ -2046,7 +2049,7 @@ __device__ __noinline__ void general_top(Topo& topo, Shared& s, const Src& src, 
         const uint32_t key = fkey(z);
         if (key < key_lo) return;
         const float d = dist(r, z);
-        if (!(d * kFineScale < fend) || !minp_ok(r, z, d)) return;
+        if (fine_bin(d * kFineScale) > bn || !minp_ok(r, z, d)) return;
         const uint32_t slot = atomicAdd(&s.ncand, 1u);
         if (slot < (uint32_t)kCand) {
             s.ckey[slot] = key;

@@ -155,3 +155,27 @@ def test_apply_penalties_checks_its_arguments():
     assert call(rep=FAKE + 2) == 4                                    # misaligned penalty array
     assert call(B=0) == 0                                             # empty batch: nothing to do
     assert call(rep=None) == 0                                        # no penalty and no status: nothing to do
+
+
+def test_caller_output_buffers_are_checked():
+    """Output tensors a caller passes in `out` reach the kernels as raw pointers, so the binding
+    rejects any whose shape, dtype, device or layout differs from what the call writes."""
+    import torch
+    dev = torch.device("cpu")
+    ok = torch.empty(8, dtype=torch.int32)
+    assert tps._out({"token": ok}, "token", (8,), torch.int32, dev) is ok
+    assert tps._out({}, "token", (8,), torch.int32, dev).shape == (8,)
+    bad = {
+        "shape": torch.empty(7, dtype=torch.int32),
+        "dtype": torch.empty(8, dtype=torch.int64),
+        "strided": torch.empty(16, dtype=torch.int32)[::2],
+        "2-d": torch.empty((8, 1), dtype=torch.int32),
+    }
+    for why, t in bad.items():
+        with pytest.raises(ValueError):
+            tps._out({"token": t}, "token", (8,), torch.int32, dev)
+    with pytest.raises(ValueError):  # another device
+        tps._out({"token": ok}, "token", (8,), torch.int32, torch.device("meta"))
+    top = torch.empty((8, 4), dtype=torch.int32)  # a buffer kept from a call with fewer top tokens
+    with pytest.raises(ValueError):
+        tps._out({"top_idx": top}, "top_idx", (8, 8), torch.int32, dev)
