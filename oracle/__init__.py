@@ -24,6 +24,8 @@ _default = None
 
 ROW_OK, ROW_NAN, ROW_ALL_MASKED, ROW_BAD_PARAM = 0, 1, 2, 3
 FLAG_TOPP_BAND, FLAG_MINP_BAND, FLAG_RACE_BAND = 1, 2, 4
+FLAG_ACCEPT_BAND = 8                                  # speculative acceptance: u Q(x) within rounding of P(x)
+FLAG_DRAFT_TOPP_BAND, FLAG_DRAFT_MINP_BAND = 16, 32   # the draft row's own band flags
 
 
 def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
@@ -57,6 +59,11 @@ class Oracle:
         lib.tpso_uniform_round.argtypes = [ctypes.c_uint64] * 4 + [ctypes.c_uint32]
         lib.tpso_uniform.restype = ctypes.c_double
         lib.tpso_uniform.argtypes = [ctypes.c_uint64] * 4
+        lib.tpso_uniform_spec.restype = ctypes.c_double
+        lib.tpso_uniform_spec.argtypes = [ctypes.c_uint64] * 4
+        lib.tpso_spec_accept.restype = ctypes.c_int
+        lib.tpso_spec_accept.argtypes = [P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P, P, P, P, P, P, P, P,
+                                         P, P, P, ctypes.c_uint64, P, P, P, P, P, P, ctypes.c_int]
         lib.tpso_philox4x32_10.restype = None
         lib.tpso_philox4x32_10.argtypes = [P, P, P]
         lib.tpso_max_threads.restype = ctypes.c_int
@@ -116,6 +123,50 @@ class Oracle:
         if want_probs:
             out["probs"] = probs
         return out
+
+    def spec_accept(self, zt, zd, target, draft, draft_token, seed, step=0, *, row_ids=None, nthreads=0):
+        """Speculative acceptance of one draft token per row.
+
+        ``zt``, ``zd``: [B, V] target and draft logits (widened exactly to float64); ``target`` and
+        ``draft``: (temperature, top_k, top_p, min_p), each a scalar or [B] (T, p and min_p rounded to
+        float32 first, as the GPU receives them); ``draft_token``: [B] the token the draft sampled.
+        Returns token, accepted, status, flags, p_x (P of the draft token) and q_x (Q of it)."""
+        zt = np.ascontiguousarray(np.asarray(zt, dtype=np.float64))
+        zd = np.ascontiguousarray(np.asarray(zd, dtype=np.float64))
+        if zt.ndim != 2 or zt.shape != zd.shape:
+            raise ValueError("zt and zd must both be [B, V]")
+        B, V = zt.shape
+
+        def vec(x, dt):
+            return np.ascontiguousarray(np.broadcast_to(np.asarray(x), (B,)).astype(dt))
+
+        def params(t):
+            T, k, p, m = t
+            return (vec(np.asarray(T, dtype=np.float32), np.float64), vec(k, np.int32),
+                    vec(np.asarray(p, dtype=np.float32), np.float64), vec(np.asarray(m, dtype=np.float32), np.float64))
+
+        Tt, kt, pt, mt = params(target)
+        Td, kd, pd, md = params(draft)
+        X = vec(draft_token, np.int32)
+        S = vec(np.asarray(seed).astype(np.uint64), np.uint64)
+        R = None if row_ids is None else vec(row_ids, np.int64)
+        out = {k: np.empty(B, np.int32) for k in ("token", "accepted", "status", "flags")}
+        out["p_x"] = np.empty(B, np.float64)
+        out["q_x"] = np.empty(B, np.float64)
+        rc = self.lib.tpso_spec_accept(_ptr(zt), _ptr(zd), B, V, V, _ptr(Tt), _ptr(kt), _ptr(pt), _ptr(mt), _ptr(Td),
+                                       _ptr(kd), _ptr(pd), _ptr(md), _ptr(X), _ptr(S), _ptr(R),
+                                       int(step) & ((1 << 64) - 1), _ptr(out["token"]), _ptr(out["accepted"]),
+                                       _ptr(out["status"]), _ptr(out["flags"]), _ptr(out["p_x"]), _ptr(out["q_x"]),
+                                       int(nthreads))
+        if rc != 0:
+            raise MemoryError("oracle scratch allocation failed")
+        return out
+
+    def uniform_spec(self, seed: int, row: int, step: int, token: int) -> float:
+        """The speculative acceptance's uniform for (seed, row, step, token); token 2^20 - 1 is the
+        acceptance test's own."""
+        m = (1 << 64) - 1
+        return self.lib.tpso_uniform_spec(seed & m, row & m, step & m, token & m)
 
     def penalties(self, z, history, hist_len=None, repetition=None, frequency=None, presence=None,
                   bf16=False):
@@ -183,6 +234,10 @@ def uniform(seed: int, row: int, step: int, token: int) -> float:
 
 def penalties(*args, **kwargs):
     return default().penalties(*args, **kwargs)
+
+
+def spec_accept(*args, **kwargs):
+    return default().spec_accept(*args, **kwargs)
 
 
 def philox4x32_10(counter, key):

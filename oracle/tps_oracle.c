@@ -114,6 +114,21 @@ double tpso_uniform_round(uint64_t seed, uint64_t row, uint64_t step, uint64_t t
     return ((double)(2u * (w >> 9) + 1u)) * 0x1p-24;
 }
 
+/* The uniforms of speculative acceptance: the same generator and mapping with bit 31 of the counter's
+ * row word set.  Row indices stay below 2^31, so neither the race nor any rejection round uses these
+ * counters.  Token TPSO_SPEC_ACCEPT_SLOT (2^20 - 1, above every token index) gives the acceptance
+ * test's uniform; a token index gives that token's uniform in the residual race. */
+#define TPSO_SPEC_ACCEPT_SLOT 0xFFFFFu
+double tpso_uniform_spec(uint64_t seed, uint64_t row, uint64_t step, uint64_t token)
+{
+    uint32_t ctr[4] = {(uint32_t)(token / 4u), (uint32_t)row | 0x80000000u, (uint32_t)step, (uint32_t)(step >> 32)};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t x[4];
+    tpso_philox4x32_10(ctr, key, x);
+    uint32_t w = x[token % 4u];
+    return ((double)(2u * (w >> 9) + 1u)) * 0x1p-24;
+}
+
 /* Race key of a kept token: ln P_i - ln E_i up to the row constant ln Z. */
 static double race_key(double zmax, double zi, double T, double u)
 {
@@ -404,6 +419,110 @@ int tpso_max_threads(void)
 #else
     return 1;
 #endif
+}
+
+/* ---------------------------------------------------------------------------------------------
+ * Speculative acceptance on truncated distributions ([NS] "Logprobs, speculative decoding and
+ * reproducibility": accept a draft token x with probability min(1, P(x)/Q(x)); on rejection draw
+ * from the normalised positive part of P - Q; P is the target's truncated and renormalised
+ * distribution, Q the distribution the draft actually sampled from, truncation included).
+ *   P = the renormalised kept distribution of the target row under its (T, k, p, m) -- exactly the
+ *       probability row the chain above produces (one-hot for a greedy target);
+ *   Q = the same for the draft row under the draft's (T, k, p, m);
+ *   accepted iff u * Q(x) < P(x), with u the acceptance uniform (an odd multiple of 2^-24 in (0, 1),
+ *       so this holds with probability min(1, P(x)/Q(x)) up to the 2^-23 grid);
+ *   otherwise the token is argmax over i with r_i = P_i - Q_i > 0 of ln r_i - ln(-ln u_i) (an
+ *       exponential race over the residual; lowest index on equal keys).
+ * A row fails (token -1, not accepted) when the target or the draft row fails, or when x is not a
+ * token the draft distribution can produce (outside [0, V), or Q(x) = 0): TPSO_ROW_BAD_PARAM.
+ * Flags: the target's top-p / min-p band flags in bits 0-1, the draft's in bits 4-5; bit 3 when
+ * u Q(x) and P(x) lie within SPEC_BAND (relative) of each other; bit 2 when the two best residual
+ * race keys lie within the error the residuals' rounding allows.
+ * --------------------------------------------------------------------------------------------- */
+#define TPSO_FLAG_ACCEPT_BAND 8
+static const double SPEC_BAND = 1e-5;
+
+int tpso_spec_accept(const double* zt, const double* zd, int64_t B, int64_t V, int64_t ld, const double* Tt,
+                     const int32_t* kt, const double* pt, const double* mt, const double* Td, const int32_t* kd,
+                     const double* pd, const double* md, const int32_t* draft, const uint64_t* seed,
+                     const int64_t* row_ids, uint64_t step, int32_t* out_token, int32_t* out_accepted,
+                     int32_t* out_status, int32_t* out_flags, double* out_px, double* out_qx, int nthreads)
+{
+    if (B <= 0) return 0;
+    int failed = 0;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel
+#endif
+    {
+        zi_pair* pairs = (zi_pair*)malloc(sizeof(zi_pair) * (size_t)V);
+        double* e = (double*)malloc(sizeof(double) * (size_t)V);
+        double* P = (double*)malloc(sizeof(double) * (size_t)V);
+        double* Q = (double*)malloc(sizeof(double) * (size_t)V);
+        if (!pairs || !e || !P || !Q) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+            for (int64_t b = 0; b < B; ++b) {
+                uint64_t rid = row_ids ? (uint64_t)row_ids[b] : (uint64_t)b;
+                row_out rt, rd;
+                sample_row(zt + b * ld, V, Tt[b], kt[b], pt[b], mt[b], seed[b], rid, step, P, pairs, e, &rt, 0, NULL);
+                sample_row(zd + b * ld, V, Td[b], kd[b], pd[b], md[b], seed[b], rid, step, Q, pairs, e, &rd, 0, NULL);
+                int32_t x = draft[b];
+                int32_t status = rt.status != TPSO_ROW_OK ? rt.status : rd.status;
+                if (status == TPSO_ROW_OK && (x < 0 || (int64_t)x >= V || !(Q[x] > 0.0))) status = TPSO_ROW_BAD_PARAM;
+                int32_t flags = (rt.flags & 3) | ((rd.flags & 3) << 4);
+                int32_t token = -1, accepted = 0;
+                double px = NAN, qx = NAN;
+                if (status == TPSO_ROW_OK) {
+                    px = P[x];
+                    qx = Q[x];
+                    double u = tpso_uniform_spec(seed[b], rid, step, TPSO_SPEC_ACCEPT_SLOT);
+                    double lhs = u * qx;
+                    if (fabs(lhs - px) <= SPEC_BAND * fmax(lhs, px)) flags |= TPSO_FLAG_ACCEPT_BAND;
+                    if (lhs < px) {
+                        accepted = 1;
+                        token = x;
+                    } else {
+                        double best = -INFINITY, second = -INFINITY, tol_best = 0.0, tol_second = 0.0;
+                        for (int64_t i = 0; i < V; ++i) {
+                            double r = P[i] - Q[i];
+                            if (!(r > 0.0)) continue;
+                            double key = log(r) - log(-log(tpso_uniform_spec(seed[b], rid, step, (uint64_t)i)));
+                            double tol = SPEC_BAND * (P[i] + Q[i]) / r;
+                            if (key > best) {
+                                second = best;
+                                tol_second = tol_best;
+                                best = key;
+                                tol_best = tol;
+                                token = (int32_t)i;
+                            } else if (key > second) {
+                                second = key;
+                                tol_second = tol;
+                            }
+                        }
+                        if (second > -INFINITY && best - second <= tol_best + tol_second + 1e-12) flags |= TPSO_FLAG_RACE_BAND;
+                    }
+                }
+                out_token[b] = token;
+                if (out_accepted) out_accepted[b] = accepted;
+                if (out_status) out_status[b] = status;
+                if (out_flags) out_flags[b] = flags;
+                if (out_px) out_px[b] = px;
+                if (out_qx) out_qx[b] = qx;
+            }
+        }
+        free(pairs);
+        free(e);
+        free(P);
+        free(Q);
+    }
+    return failed ? -1 : 0;
 }
 
 /* ---------------------------------------------------------------------------------------------

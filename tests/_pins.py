@@ -515,7 +515,163 @@ def check_rejection(o):
     return fails
 
 
+def _philox_word(o, seed, c0, row_word, step, token):
+    blk = o.philox4x32_10([c0 & 0xFFFFFFFF, row_word & 0xFFFFFFFF, step & 0xFFFFFFFF, (step >> 32) & 0xFFFFFFFF],
+                          [seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF])
+    return (2 * (int(blk[token % 4]) >> 9) + 1) * 2.0 ** -24
+
+
+def check_counter_layouts(o):
+    """Where each draw takes its uniforms from (the generator itself is pinned against Triton's
+    Philox): the race at counter (i/4, row, step); rejection round r at ((i/4) | (r+1) << 18, row,
+    step), so round 0 never reuses the race's counters; speculative acceptance at (i/4, row | 2^31,
+    step), with token 2^20 - 1 (word 3 of block 2^18 - 1, above every token index) the acceptance
+    test's own uniform."""
+    fails = []
+    rng = np.random.default_rng(17)
+    for _ in range(200):
+        seed = int(rng.integers(0, 2**63))
+        row, step, tok = int(rng.integers(0, 2**27)), int(rng.integers(0, 2**63)), int(rng.integers(0, 2**20 - 1))
+        u_race = o.uniform(seed, row, step, tok)
+        if u_race != _philox_word(o, seed, tok // 4, row, step, tok):
+            fails.append(f"race uniform of token {tok} not at counter (i/4, row, step)")
+        for r in (0, 1, 5):
+            u = o.uniform_round(seed, row, step, tok, r)
+            if u != _philox_word(o, seed, (tok // 4) | ((r + 1) << 18), row, step, tok):
+                fails.append(f"rejection round {r} uniform of token {tok} not at counter ((i/4) | (r+1) << 18, ...)")
+        if o.uniform_round(seed, row, step, tok, 0) == u_race:
+            fails.append("rejection round 0 reuses the race's uniform")
+        u_spec = o.uniform_spec(seed, row, step, tok)
+        if u_spec != _philox_word(o, seed, tok // 4, row | 0x80000000, step, tok):
+            fails.append(f"speculative uniform of token {tok} not at counter (i/4, row | 2^31, step)")
+        if u_spec == u_race:
+            fails.append("speculative uniform reuses the race's")
+        if o.uniform_spec(seed, row, step, 2**20 - 1) != _philox_word(o, seed, 2**18 - 1, row | 0x80000000, step, 3):
+            fails.append("the acceptance uniform is not word 3 of block 2^18 - 1")
+        if len(fails) > 5:
+            break
+    return fails
+
+
+def _softmax_trunc(z, T, k=0, p=1.0, m=0.0):
+    """The renormalised kept distribution written out for small, tie-free rows: min-p, top-k, then
+    top-p on the survivors (keep a token iff the mass of more probable survivors is below p)."""
+    z = np.asarray(z, np.float64)
+    T = float(np.float32(T))
+    p = float(np.float32(p))
+    e = np.exp((z - z.max()) / T)
+    keep = np.ones(len(z), bool)
+    if m > 0:
+        keep &= e >= min(float(np.float32(m)), 1.0)
+    if 0 < k < len(z):
+        keep &= z >= np.sort(z)[::-1][k - 1]
+    if p < 1:
+        order = np.argsort(-z)
+        Zs = e[keep].sum()
+        above = 0.0
+        for i in order:
+            if not keep[i]:
+                continue
+            if above >= p * Zs and z[i] < z.max():
+                keep[i] = False
+            above += e[i]
+    P = np.where(keep, e, 0.0)
+    return P / P.sum()
+
+
+def check_spec_accept(o):
+    """Speculative acceptance ("Top-p (Nucleus) Sampling, in depth", 'Logprobs, speculative decoding
+    and reproducibility'): the draft token is accepted with probability min(1, P(x)/Q(x)) and a
+    rejection draws from the normalised (P - Q)+, which makes the output distributed exactly as P for
+    any draft distribution Q; P and Q are the truncated, renormalised distributions."""
+    fails = []
+    rng = np.random.default_rng(23)
+    # --- statistics on small rows, P and Q written out independently of the oracle
+    cases = [
+        # (target logits, target (T, k, p, m), draft logits, draft (T, k, p, m))
+        (np.log([0.5, 0.3, 0.2]), (1.0, 0, 0.6, 0.0), np.zeros(3), (1.0, 0, 1.0, 0.0)),
+        ([2.0, 1.0, 0.0, -1.0, 0.5], (0.7, 0, 1.0, 0.0), [0.0, 1.0, 2.0, 0.5, -0.3], (1.3, 3, 1.0, 0.0)),
+        ([0.3, 1.7, -0.4, 0.9], (1.1, 0, 0.95, 0.1), [1.2, 0.1, 0.8, -2.0], (0.6, 0, 0.9, 0.0)),
+    ]
+    n = 200_000
+    for ci, (zt, pt, zd, pd) in enumerate(cases):
+        zt, zd = np.asarray(zt, np.float64), np.asarray(zd, np.float64)
+        P, Q = _softmax_trunc(zt, *pt), _softmax_trunc(zd, *pd)
+        x = rng.choice(len(zd), size=n, p=Q)
+        seeds = np.arange(n, dtype=np.uint64) * np.uint64(0x9E3779B97F4A7C15) + np.uint64(31 + ci)
+        r = o.spec_accept(np.tile(zt, (n, 1)), np.tile(zd, (n, 1)), pt, pd, x, seeds, step=5)
+        if (r["status"] != 0).any():
+            fails.append(f"case {ci}: failed rows")
+            continue
+        acc = r["accepted"].mean()
+        a_exact = np.minimum(P, Q).sum()
+        if abs(acc - a_exact) > 5 * np.sqrt(a_exact * (1 - a_exact) / n) + 1e-9:
+            fails.append(f"case {ci}: acceptance rate {acc:.5f} vs sum min(P, Q) = {a_exact:.5f}")
+        freq = np.bincount(r["token"], minlength=len(zt)) / n
+        sig = np.sqrt(P * (1 - P) / n)
+        if np.any(np.abs(freq - P) > 5 * sig + 1e-9):
+            fails.append(f"case {ci}: output frequencies {np.round(freq, 4)} vs P {np.round(P, 4)}")
+        rej = r["accepted"] == 0
+        resid = np.maximum(P - Q, 0)
+        if rej.sum() > 1000 and resid.sum() > 0:
+            R = resid / resid.sum()
+            fr = np.bincount(r["token"][rej], minlength=len(zt)) / rej.sum()
+            if np.any(np.abs(fr - R) > 5 * np.sqrt(R * (1 - R) / rej.sum()) + 1e-9):
+                fails.append(f"case {ci}: rejected draws {np.round(fr, 4)} vs normalised (P-Q)+ {np.round(R, 4)}")
+        if np.any((r["accepted"] == 1) & (r["token"] != x)):
+            fails.append(f"case {ci}: an accepted row does not return the draft token")
+        if np.any(np.abs(r["p_x"] - P[x]) > 1e-12) or np.any(np.abs(r["q_x"] - Q[x]) > 1e-12):
+            fails.append(f"case {ci}: P(x) or Q(x) differs from the written-out distributions")
+    # --- special cases
+    V = 40
+    zt = rng.normal(0, 2, size=(64, V))
+    zt[:, 5] = zt[:, 7] = zt.max(axis=1) + 0.5  # tied maxima
+    T = rng.choice([0.5, 1.0, 2.0], 64)
+    k = rng.choice([0, 3, 10], 64)
+    p = rng.uniform(0.2, 1.0, 64)
+    m = rng.choice([0.0, 0.05], 64)
+    seeds = np.arange(64, dtype=np.uint64) + np.uint64(100)
+    own = o.sample(zt, T, k, p, m, seeds, 9)["token"]
+    # P == Q: every draft token the draft can produce is accepted
+    r = o.spec_accept(zt, zt, (T, k, p, m), (T, k, p, m), own, seeds, step=9)
+    if not (r["accepted"] == 1).all() or not (r["token"] == own).all():
+        fails.append("identical target and draft: not every draft token accepted")
+    # greedy target: always its lowest-index maximum
+    r = o.spec_accept(zt, zt, (0.0, 0, 1.0, 0.0), (T, k, p, m), own, seeds, step=9)
+    if not (r["token"] == 5).all():
+        fails.append("greedy target: not always its lowest-index maximum")
+    # disjoint supports: never accepted, the output lies in the target's support
+    za, zb = zt.copy(), zt.copy()
+    za[:, 20:] = -np.inf
+    zb[:, :20] = -np.inf
+    xb = o.sample(zb, 1.0, 0, 1.0, 0.0, seeds, 9)["token"]
+    r = o.spec_accept(za, zb, (1.0, 0, 1.0, 0.0), (1.0, 0, 1.0, 0.0), xb, seeds, step=9)
+    if (r["accepted"] != 0).any() or (r["token"] >= 20).any() or (r["token"] < 0).any():
+        fails.append("disjoint supports: a draft token accepted, or the output outside the target's support")
+    # truncation is respected: a draft token outside the target's nucleus is never accepted
+    z3 = np.tile(np.log([0.5, 0.3, 0.2]), (64, 1))
+    r = o.spec_accept(z3, np.zeros((64, 3)), (1.0, 0, 0.6, 0.0), (1.0, 0, 1.0, 0.0), np.full(64, 2), seeds, step=9)
+    if (r["accepted"] != 0).any() or (r["token"] == 2).any():
+        fails.append("a draft token outside the target's nucleus was accepted")
+    # failures: a draft token the draft cannot produce, out of range, a failed target or draft row
+    zbad = zt[:4].copy()
+    zbad[2, 3] = np.nan
+    zd = zt[:4].copy()
+    zd[3] = -np.inf
+    x = np.array([-1, V, 0, 0])
+    r = o.spec_accept(zbad, zd, (1.0, 0, 1.0, 0.0), (1.0, 0, 1.0, 0.0), x, seeds[:4], step=9)
+    if r["status"].tolist() != [3, 3, 1, 2] or (r["token"] != -1).any() or (r["accepted"] != 0).any():
+        fails.append(f"failed rows: status {r['status'].tolist()} tokens {r['token'].tolist()}")
+    zq = np.log(np.array([[0.7, 0.2, 0.1]]))
+    r = o.spec_accept(zq, zq, (1.0, 0, 1.0, 0.0), (1.0, 1, 1.0, 0.0), [2], seeds[:1], step=9)
+    if r["status"][0] != 3:
+        fails.append("a draft token outside the draft's own kept set is not rejected as invalid")
+    return fails
+
+
 ALL_CHECKS = {
+    "counter_layouts": check_counter_layouts,
+    "spec_accept": check_spec_accept,
     "rejection": check_rejection,
     "penalties": check_penalties,
     "worked_examples": check_worked_examples,

@@ -44,6 +44,12 @@ MUTANTS = [
     ("rejection counts the winner's class as above", "if (pairs[t].z > z[arg]) above += e[pairs[t].i];",
      "if (pairs[t].z >= z[arg]) above += e[pairs[t].i];"),
     ("rejection never raises the pivot", "            zpiv = z[arg];\n", "            (void)zpiv;\n"),
+    ("rejection round 0 on the race's counters", "((round + 1u) << 18)", "(round << 18)"),
+    ("spec ignores the draft probability", "if (lhs < px) {", "if (u < px) {"),
+    ("spec residual is the target probability", "double r = P[i] - Q[i];", "double r = P[i];"),
+    ("spec takes the raw target distribution", "sample_row(zt + b * ld, V, Tt[b], kt[b], pt[b], mt[b],",
+     "sample_row(zt + b * ld, V, Tt[b], 0, 1.0, 0.0,"),
+    ("spec uniforms on the race's counters", "(uint32_t)row | 0x80000000u", "(uint32_t)row"),
     ("bfloat16 ties away from zero", "if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) r = keep + 1u;",
      "if (rest >= 0x8000u) r = keep + 1u;"),
 ]
@@ -65,7 +71,7 @@ def test_pins_catch_planted_mistake(mutant_dir, name, old, new):
     lib = oracle.build(force=True, src=src, out=os.path.join(mutant_dir, f"lib{tag}.so"))
     o = oracle.Oracle(lib)
     checks = [_pins.check_worked_examples, _pins.check_closed_forms, _pins.check_penalties, _pins.check_rejection,
-              _pins.check_uniform_mapping,
+              _pins.check_uniform_mapping, _pins.check_counter_layouts, _pins.check_spec_accept,
               lambda x: _pins.check_bruteforce(x, n_batches=120), _pins.check_sample_frequencies]
     if _pins.triton_philox_available():
         checks.append(_pins.check_philox_vs_triton)
