@@ -189,6 +189,41 @@ int tps_apply_penalties(void* logits, int dtype, int64_t B, int64_t V, int64_t l
                         int64_t H, int64_t ldh, const int32_t* hist_len, const float* repetition,
                         const float* frequency, const float* presence, int32_t* out_status, void* stream);
 
+/*
+ * tps_spec_accept -- speculative acceptance of one draft token per row on truncated distributions
+ * ("Top-p (Nucleus) Sampling, in depth", 'Logprobs, speculative decoding and reproducibility': accept
+ * a draft token x with probability min(1, P(x)/Q(x)); on rejection draw from the normalised positive
+ * part of P - Q, which reproduces P exactly; P is the target's truncated and renormalised
+ * distribution, Q the one the draft actually sampled from, truncation included).
+ *
+ *   P, Q    the renormalised kept distributions tps_sample draws from, for the target row under
+ *           (target_temperature, target_top_k, target_top_p, target_min_p) and for the draft row
+ *           under the draft's four parameters (one-hot for a greedy row).
+ *   The row accepts x iff u Q(x) < P(x) (u: the acceptance uniform); otherwise its token is the
+ *   argmax over i with r_i = P(i) - Q(i) > 0 of ln r_i - ln(-ln u_i), lowest index on equal keys.
+ *   Uniforms: u = (2 (w >> 9) + 1) 2^-24 with w = word (i mod 4) of Philox4x32-10, key = seed[b] and
+ *   counter (i / 4, b | 2^31, step low word, step high word); i = 2^20 - 1 gives the acceptance
+ *   uniform.  (Bit 31 of the row word keeps these apart from the sampling draw's counters.)
+ *
+ *   target_logits, draft_logits  [B, ld] of the same dtype (TPS_F32 / TPS_BF16), V <= ld.
+ *   draft_token  [B] int32: the token the draft model drew for the row.
+ *   seed         [B] uint64;  step: 64-bit counter word, as in tps_sample.
+ *   out_token    [B] int32: x if accepted, else the residual draw; -1 for a failed row.
+ *   out_accepted [B] int32 or NULL: 1 if x was accepted, else 0 (0 for a failed row).
+ *   out_status   [B] int32 or NULL: a tps_row_status -- the target row's failure first, then the
+ *                draft row's; TPS_ROW_BAD_PARAM also when x is outside [0, V) or Q(x) = 0 (the draft
+ *                could not have drawn it).
+ * A sequence of k draft tokens is k rows; the caller keeps the tokens up to the first rejection.
+ * All pointers are caller-owned device memory; the call allocates nothing and is stream-ordered on
+ * `stream`.  Returns TPS_ERR_ARG / _DTYPE / _ALIGN / _UNSUPPORTED_V / _CUDA as tps_sample does.
+ */
+int tps_spec_accept(const void* target_logits, const void* draft_logits, int dtype, int64_t B, int64_t V, int64_t ld,
+                    const float* target_temperature, const int32_t* target_top_k, const float* target_top_p,
+                    const float* target_min_p, const float* draft_temperature, const int32_t* draft_top_k,
+                    const float* draft_top_p, const float* draft_min_p, const int32_t* draft_token,
+                    const uint64_t* seed, uint64_t step, int32_t* out_token, int32_t* out_accepted,
+                    int32_t* out_status, void* stream);
+
 /* Kernels one tps_sample_kernel call with these arguments launches (1 or 2; 0 for arguments the call
  * would reject).  Host-only query. */
 int tps_kernels_per_call(int dtype, int64_t B, int64_t V, int kernel);

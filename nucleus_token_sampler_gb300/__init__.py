@@ -14,7 +14,7 @@ import threading
 
 import torch
 
-__all__ = ["build", "load", "sample", "apply_penalties", "TPS_F32", "TPS_BF16", "ROW_STATUS", "library_path", "max_vocab",
+__all__ = ["build", "load", "sample", "apply_penalties", "spec_accept", "TPS_F32", "TPS_BF16", "ROW_STATUS", "library_path", "max_vocab",
            "cluster_size", "kernels_per_call", "version"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -23,9 +23,9 @@ _LIB = os.path.join(_HERE, "libtps.so")
 _INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
 # The ABI and launch code, and one translation unit per (kernel, element type): compiled in parallel.
 _SOURCES = ["tps_api.cu", "tps_k_cluster_f32.cu", "tps_k_cluster_bf16.cu", "tps_k_stream_f32.cu",
-            "tps_k_stream_bf16.cu", "tps_k_penalty.cu"]
+            "tps_k_stream_bf16.cu", "tps_k_penalty.cu", "tps_k_spec.cu"]
 _HEADERS = ["tps_device.cuh", "tps_common.cuh", "tps_cluster.cuh", "tps_stream.cuh", "tps_penalty.cuh",
-            "tps_kernels.h"]
+            "tps_spec.cuh", "tps_kernels.h"]
 _NVCC = ["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
          "-Xcompiler", "-fPIC"]
 
@@ -93,6 +93,8 @@ def load():
             lib.tps_sample_full.restype = I32
             lib.tps_sample_full.argtypes = [P, I32, I64, I64, I64, P, P, P, P, P, U64, P, P, P, P, P, P, I32, P, P,
                                             I32, P]
+            lib.tps_spec_accept.restype = I32
+            lib.tps_spec_accept.argtypes = [P, P, I32, I64, I64, I64, P, P, P, P, P, P, P, P, P, P, U64, P, P, P, P]
             lib.tps_max_vocab.restype = I64
             lib.tps_max_vocab.argtypes = [I32]
             lib.tps_cluster_size.restype = I32
@@ -288,3 +290,46 @@ def sample(logits: torch.Tensor, temperature, top_k, top_p, min_p, seed, step: i
     if want_probs:
         r["probs"] = probs
     return r
+
+
+def spec_accept(target_logits: torch.Tensor, draft_logits: torch.Tensor, target, draft, draft_token, seed,
+                step: int = 0, *, diagnostics: bool = False, stream=None):
+    """Speculative acceptance of one draft token per row: accept the draft's token x with
+    probability min(1, P(x)/Q(x)), else draw from the normalised (P - Q)+, where P and Q are the
+    renormalised kept distributions ``sample`` draws from for the target row under ``target`` and the
+    draft row under ``draft`` (each a (temperature, top_k, top_p, min_p) tuple of [B] tensors or
+    scalars).  ``target_logits`` and ``draft_logits``: [B, V] CUDA tensors of the same dtype and
+    shape.  Returns the [B] int32 tokens, or a dict with ``token``, ``accepted`` and ``status`` when
+    ``diagnostics`` is set."""
+    for t in (target_logits, draft_logits):
+        if not t.is_cuda or t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError("logits must be [B, V] CUDA tensors with unit stride along V")
+    if target_logits.shape != draft_logits.shape or target_logits.dtype != draft_logits.dtype:
+        raise ValueError("target and draft logits must have the same shape and dtype")
+    if target_logits.device != draft_logits.device:
+        raise ValueError("target and draft logits must be on one device")
+    B, V = target_logits.shape
+    if B > 1 and target_logits.stride(0) != draft_logits.stride(0):
+        raise ValueError("target and draft logits must share a row stride")
+    ld = target_logits.stride(0) if B > 1 else V
+    dev = target_logits.device
+    code = _dtype_code(target_logits.dtype)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev), torch.cuda.stream(s):
+        tT, tK, tP, tM = (_param(v, B, dt, dev) for v, dt in zip(target, (torch.float32, torch.int32, torch.float32,
+                                                                         torch.float32)))
+        dT, dK, dP, dM = (_param(v, B, dt, dev) for v, dt in zip(draft, (torch.float32, torch.int32, torch.float32,
+                                                                        torch.float32)))
+        X = _param(draft_token, B, torch.int32, dev)
+        S = _param(seed, B, torch.int64, dev)
+        tok = torch.empty(B, dtype=torch.int32, device=dev)
+        acc = torch.empty(B, dtype=torch.int32, device=dev) if diagnostics else None
+        st = torch.empty(B, dtype=torch.int32, device=dev) if diagnostics else None
+        rc = load().tps_spec_accept(_ptr(target_logits), _ptr(draft_logits), code, B, V, ld, _ptr(tT), _ptr(tK), _ptr(tP),
+                                    _ptr(tM), _ptr(dT), _ptr(dK), _ptr(dP), _ptr(dM), _ptr(X), _ptr(S),
+                                    int(step) & ((1 << 64) - 1), _ptr(tok), _ptr(acc), _ptr(st),
+                                    ctypes.c_void_p(s.cuda_stream))
+    _check(rc)
+    if not diagnostics:
+        return tok
+    return {"token": tok, "accepted": acc, "status": st}

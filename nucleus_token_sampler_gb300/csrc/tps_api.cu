@@ -1,14 +1,15 @@
 // tps_api.cu -- the C ABI declared in include/tps.h: argument checks, kernel and launch-shape
-// choice, and the launch.  No allocation, no host synchronisation, no state kept between calls
-// beyond a per-device cache of queried limits.
+// choice, and the launches.  No host synchronisation, no state kept between calls beyond a
+// per-device cache of queried limits.
 //
 // Two kernels sample the rows.  The cluster kernel (a thread-block cluster per row, the row held in
 // the cluster's shared memory) spreads each row over up to 16 SMs; it samples small batches.  The
 // streaming kernel (one persistent CTA per SM, rows streamed through a ring of bulk-copied chunks)
-// reads each row once at HBM speed and resolves rows with min-p (and greedy rows) on the fly.  A
-// large batch is split: the cluster kernel takes the rows without min-p, whose general path makes
-// several passes over the row, and the streaming kernel, launched behind it as its programmatic
-// dependent, takes the rest.
+// reads each row once at HBM speed and resolves rows with min-p (and greedy rows) on the fly; its
+// CTAs claim work dynamically through a small global scratch, which the call draws from the
+// device's stream-ordered memory pool and which a one-CTA kernel clears just before.  A large batch
+// is split: the streaming kernel lists the rows without min-p (whose general path makes several
+// passes over the row) in the scratch, and the cluster kernel, launched behind it, samples them.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -21,6 +22,7 @@
 #include "tps_cluster.cuh"
 #include "tps_kernels.h"
 #include "tps_penalty.cuh"
+#include "tps_spec.cuh"
 #include "tps_stream.cuh"
 
 namespace {
@@ -47,6 +49,7 @@ constexpr int kMaxCluster = 16;
 constexpr int kStreamStages = 3;
 constexpr uint32_t kStreamChunk = 64u * 1024u;
 constexpr int64_t kStreamMinRows = 32;  // batches at least this large use the streaming kernel
+constexpr int64_t kSegBytes = 256 * 1024;  // target size of a segment of a split row
 
 // Per-device limits, filled once under g_mu and published through `ready` (release/acquire), so a
 // thread that sees ready == true also sees sms and smem_optin.  The attribute flags only record that
@@ -99,11 +102,44 @@ uint32_t slice_cap_bytes(int64_t V, int es, int C)
     return (uint32_t)(((per * 16) + 127) / 128 * 128);
 }
 
-// Slice, shared state, the cluster-wide fine histogram, the list of a pass's rows and the exchange inbox.
+// Slice, shared state, the cluster-wide fine histogram, a spare row list and the exchange inbox.
 size_t smem_bytes(uint32_t slice_cap)
 {
     return (size_t)slice_cap + sizeof(tps::Shared) + 2 * (size_t)tps::kFineBins * sizeof(uint32_t) +
            (size_t)tps::kThreads * sizeof(int32_t) + sizeof(tps::Inbox);
+}
+
+// The streaming kernel's work for B rows: rows [0, b_whole) are claimed whole; the last nsplit rows
+// (two per SM, so the last claims of the call are short) are claimed as nseg segments of about
+// kSegBytes each; rows of at most kSegBytes are never split.
+struct StreamPlan {
+    int64_t b_whole, nsplit;
+    int nseg;
+    int64_t claims;
+    int grid;
+    tps::ScratchLayout layout;
+};
+StreamPlan stream_plan(const DeviceInfo& d, int64_t B, int64_t V, int es)
+{
+    StreamPlan p;
+    const int64_t row_bytes = V * es;
+    int64_t nseg = (row_bytes + kSegBytes - 1) / kSegBytes;
+    p.nseg = (int)std::max<int64_t>(1, std::min<int64_t>(nseg, tps::kMaxSegments));
+    p.nsplit = p.nseg > 1 ? std::min<int64_t>(B, 2 * (int64_t)d.sms) : 0;
+    p.b_whole = B - p.nsplit;
+    p.claims = p.b_whole + p.nsplit * p.nseg;
+    p.grid = (int)std::min<int64_t>(d.sms, p.claims);
+    p.layout = tps::ScratchLayout::of(B, p.nsplit, p.nseg);
+    return p;
+}
+
+// Zero the part of a streaming call's scratch that must start at zero (counters), then let the
+// streaming kernel, launched behind this one as its programmatic dependent, start at once: it
+// reads logits and parameters right away and waits for this grid only before its first claim.
+__global__ void clear_scratch_kernel(uint32_t* p, uint32_t nwords)
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    for (uint32_t i = threadIdx.x; i < nwords; i += blockDim.x) p[i] = 0u;
 }
 
 // Choose the cluster size: the smallest C whose slice fits the preferred size, widened for small
@@ -174,12 +210,10 @@ static_assert(tps::kMaxHistory == TPS_MAX_HISTORY && 2 * tps::penalty_slots(TPS_
 
 size_t stream_smem_bytes() { return (size_t)kStreamStages * kStreamChunk + sizeof(tps::Shared) + sizeof(tps::StreamState); }
 
-// The streaming kernel.  `dependent`: launched as a programmatic dependent of the preceding kernel
-// in the stream (the cluster kernel of a split batch), so its CTAs may start on SMs that kernel has
-// already released.
+// The streaming kernel over `grid` CTAs, as the programmatic dependent of the clear kernel
+// launched just before it.
 template <typename TIn>
-cudaError_t launch_stream(const DeviceInfo& d, std::atomic<bool>* attrs_done, const tps::Args& a, bool dependent,
-                          cudaStream_t stream)
+cudaError_t launch_stream(std::atomic<bool>* attrs_done, const tps::Args& a, int grid, cudaStream_t stream)
 {
     auto k = stream_kernel<TIn>();
     const size_t smem = stream_smem_bytes();
@@ -188,7 +222,6 @@ cudaError_t launch_stream(const DeviceInfo& d, std::atomic<bool>* attrs_done, co
         if (e != cudaSuccess) return e;
         attrs_done->store(true, std::memory_order_release);
     }
-    const int64_t grid = a.B < (int64_t)d.sms ? a.B : (int64_t)d.sms;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(tps::kStreamThreads, 1, 1);
@@ -198,26 +231,29 @@ cudaError_t launch_stream(const DeviceInfo& d, std::atomic<bool>* attrs_done, co
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = dependent ? 1 : 0;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, k, a, (int)kStreamStages, (uint32_t)kStreamChunk);
 }
 
-// The cluster kernel over `nclusters` clusters of C CTAs.
+// The cluster kernel over `nclusters` clusters of C CTAs; `dependent`: as the programmatic
+// dependent of the streaming kernel launched just before it (list mode).
 template <typename TIn>
-cudaError_t launch(const tps::Args& a, int C, size_t smem, int64_t nclusters, cudaStream_t stream)
+cudaError_t launch(const tps::Args& a, int C, size_t smem, int64_t nclusters, bool dependent, cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(nclusters * C), 1, 1);
     cfg.blockDim = dim3(tps::kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = dependent ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, cluster_kernel<TIn>(), a);
 }
 
@@ -256,6 +292,156 @@ int fail_cuda(cudaError_t e)
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+
+// One sampling call's arguments (the C ABI's, gathered).
+struct Call {
+    const void* logits;
+    int dtype;
+    int64_t B, V, ld;
+    const float* temperature;
+    const int32_t* top_k;
+    const float* top_p;
+    const float* min_p;
+    const uint64_t* seed;
+    uint64_t step;
+    int32_t* out_token;
+    float* out_probs;
+    int32_t* out_status;
+    float* out_cutoff;
+    int32_t* out_kept;
+    float* out_logprob;
+    int32_t n_top;
+    int32_t* out_top_idx;
+    float* out_top_logprob;
+    int kernel;
+    cudaStream_t stream;
+    uint64_t wait_ns = tps::kWaitLimitNs;
+    int64_t stall_chunk = -1;
+};
+
+// Where a streaming call's scratch comes from.
+enum class ScratchSource { kPool };
+
+int sample_call(const Call& c, ScratchSource src)
+{
+    const int64_t B = c.B, V = c.V;
+    if (c.kernel < TPS_KERNEL_AUTO || c.kernel > TPS_KERNEL_STREAM) return TPS_ERR_ARG;
+    if (B < 0 || V < 1 || c.ld < V || c.n_top < 0 || c.n_top > TPS_MAX_TOP) return TPS_ERR_ARG;
+    if (c.n_top > 0 && (!c.out_top_idx || !c.out_top_logprob)) return TPS_ERR_ARG;
+    const int es = elem_bytes(c.dtype);
+    if (!es) return TPS_ERR_DTYPE;
+    if (B == 0) return TPS_OK;
+    if (!c.logits || !c.temperature || !c.top_k || !c.top_p || !c.min_p || !c.seed || !c.out_token) return TPS_ERR_ARG;
+    if (!aligned(c.logits, es) || !aligned(c.temperature, 4) || !aligned(c.top_k, 4) || !aligned(c.top_p, 4) ||
+        !aligned(c.min_p, 4) || !aligned(c.seed, 8) || !aligned(c.out_token, 4) ||
+        (c.out_probs && !aligned(c.out_probs, 4)) || (c.out_status && !aligned(c.out_status, 4)) ||
+        (c.out_cutoff && !aligned(c.out_cutoff, 4)) || (c.out_kept && !aligned(c.out_kept, 4)) ||
+        (c.out_logprob && !aligned(c.out_logprob, 4)) ||
+        (c.n_top > 0 && (!aligned(c.out_top_idx, 4) || !aligned(c.out_top_logprob, 4))))
+        return TPS_ERR_ALIGN;
+    if (V > kMaxVocabMass || V > INT32_MAX) return TPS_ERR_UNSUPPORTED_V;
+    if (B > (int64_t)INT32_MAX / kMaxCluster) return TPS_ERR_ARG;
+
+    DeviceInfo* d = nullptr;
+    if (!device_info(&d)) return fail_cuda(cudaGetLastError());
+    const int Cfit = choose_cluster(*d, es, B, V);
+    const int kernel = c.kernel;
+    const bool use_stream = kernel == TPS_KERNEL_STREAM || (kernel == TPS_KERNEL_AUTO && B >= kStreamMinRows) ||
+                            (kernel == TPS_KERNEL_AUTO && Cfit == 0);
+    // A large batch is split: the streaming kernel takes the rows with min-p (and greedy and failed
+    // rows) and lists the others, which the cluster kernel, launched behind it, samples.
+    const bool split = kernel == TPS_KERNEL_AUTO && use_stream && Cfit != 0;
+    if (!use_stream && Cfit == 0) return TPS_ERR_UNSUPPORTED_V;
+
+    tps::Args a = {};
+    a.logits = c.logits;
+    a.B = B;
+    a.V = V;
+    a.ld = c.ld;
+    a.temperature = c.temperature;
+    a.top_k = c.top_k;
+    a.top_p = c.top_p;
+    a.min_p = c.min_p;
+    a.seed = c.seed;
+    a.step = c.step;
+    a.out_token = c.out_token;
+    a.out_probs = c.out_probs;
+    a.out_status = c.out_status;
+    a.out_cutoff = c.out_cutoff;
+    a.out_kept = c.out_kept;
+    a.out_logprob = c.out_logprob;
+    a.n_top = c.n_top;
+    a.out_top_idx = c.n_top > 0 ? c.out_top_idx : nullptr;
+    a.out_top_logprob = c.n_top > 0 ? c.out_top_logprob : nullptr;
+    a.wait_ns = c.wait_ns;
+    a.stall_chunk = c.stall_chunk;
+    const cudaStream_t st = c.stream;
+    cudaError_t e;
+
+    // The cluster kernel's shape (for a cluster-only call, or the list mode of a split batch).
+    int Cl = Cfit;
+    uint32_t cap = Cfit ? slice_cap_bytes(V, es, Cfit) : 0u;
+    size_t sm = smem_bytes(cap);
+    if (!use_stream || split) {
+        const int dt = c.dtype == TPS_F32 ? 0 : 1;
+        std::atomic<bool>& done = c.dtype == TPS_F32 ? d->attrs_f32 : d->attrs_bf16;
+        if (!done.load(std::memory_order_acquire)) {
+            e = c.dtype == TPS_F32 ? prepare_kernel<float>(*d) : prepare_kernel<__nv_bfloat16>(*d);
+            if (e != cudaSuccess) return fail_cuda(e);
+            done.store(true, std::memory_order_release);
+        }
+        // a cluster wider than 8 that the GPU cannot co-schedule falls back to 8 CTAs, if they hold the row
+        if (Cl > 8) {
+            const bool wide = c.dtype == TPS_F32 ? wide_cluster_ok<float>(*d, dt, Cl, sm)
+                                                 : wide_cluster_ok<__nv_bfloat16>(*d, dt, Cl, sm);
+            if (!wide) {
+                if (smem_bytes(slice_cap_bytes(V, es, 8)) > (size_t)d->smem_optin) return TPS_ERR_UNSUPPORTED_V;
+                Cl = 8;
+                cap = slice_cap_bytes(V, es, 8);
+                sm = smem_bytes(cap);
+            }
+        }
+    }
+    if (!use_stream) {  // the cluster kernel alone, one cluster per row
+        a.route = tps::kRouteAll;
+        a.slice_cap = cap;
+        e = c.dtype == TPS_F32 ? launch<float>(a, Cl, sm, B, false, st) : launch<__nv_bfloat16>(a, Cl, sm, B, false, st);
+        return e == cudaSuccess ? TPS_OK : fail_cuda(e);
+    }
+
+    // The streaming kernel (and, for a split batch, the cluster kernel behind it) with its scratch.
+    const StreamPlan pl = stream_plan(*d, B, V, es);
+    void* scratch = nullptr;
+    if (src == ScratchSource::kPool) {
+        e = cudaMallocAsync(&scratch, (size_t)pl.layout.total, st);
+        if (e != cudaSuccess) return fail_cuda(e);
+    }
+    a.scratch = scratch;
+    a.b_whole = pl.b_whole;
+    a.nsplit = pl.nsplit;
+    a.nseg = pl.nseg;
+    a.route = split ? tps::kRouteStream : tps::kRouteAll;
+    a.slice_cap = 0;
+    clear_scratch_kernel<<<1, 256, 0, st>>>(static_cast<uint32_t*>(scratch), (uint32_t)(pl.layout.clear_bytes() / 4));
+    e = cudaGetLastError();
+    if (e == cudaSuccess)
+        e = c.dtype == TPS_F32 ? launch_stream<float>(&d->sattrs_f32, a, pl.grid, st)
+                               : launch_stream<__nv_bfloat16>(&d->sattrs_bf16, a, pl.grid, st);
+    if (e == cudaSuccess && split) {
+        a.route = tps::kRouteList;
+        a.slice_cap = cap;
+        const int dt = c.dtype == TPS_F32 ? 0 : 1;
+        const int64_t ncl = std::min<int64_t>(B, c.dtype == TPS_F32 ? resident_clusters<float>(*d, dt, Cl, sm)
+                                                                    : resident_clusters<__nv_bfloat16>(*d, dt, Cl, sm));
+        e = c.dtype == TPS_F32 ? launch<float>(a, Cl, sm, ncl, true, st) : launch<__nv_bfloat16>(a, Cl, sm, ncl, true, st);
+    }
+    if (src == ScratchSource::kPool) {
+        const cudaError_t ef = cudaFreeAsync(scratch, st);
+        if (e == cudaSuccess) e = ef;
+    }
+    return e == cudaSuccess ? TPS_OK : fail_cuda(e);
+}
 
 }  // namespace
 
@@ -302,8 +488,9 @@ int tps_kernels_per_call(int dtype, int64_t B, int64_t V, int kernel)
     if (!device_info(&d)) return 0;
     const int Cfit = choose_cluster(*d, es, B, V);
     if (kernel == TPS_KERNEL_CLUSTER) return Cfit ? 1 : 0;
-    if (kernel == TPS_KERNEL_STREAM) return 1;
-    return (B >= kStreamMinRows && Cfit != 0) ? 2 : 1;  // auto: a large batch is split over both kernels
+    if (kernel == TPS_KERNEL_STREAM) return 2;  // the scratch clear, the streaming kernel
+    if (B < kStreamMinRows && Cfit != 0) return 1;
+    return Cfit != 0 ? 3 : 2;  // auto: a large batch is split (clear, streaming, cluster)
 }
 
 int tps_cluster_size(int dtype, int64_t B, int64_t V)
@@ -322,105 +509,30 @@ int tps_sample_full(const void* logits, int dtype, int64_t B, int64_t V, int64_t
                     int32_t* out_kept, float* out_logprob, int32_t n_top, int32_t* out_top_idx,
                     float* out_top_logprob, int kernel, void* stream)
 {
-    if (kernel < TPS_KERNEL_AUTO || kernel > TPS_KERNEL_STREAM) return TPS_ERR_ARG;
-    if (B < 0 || V < 1 || ld < V || n_top < 0 || n_top > TPS_MAX_TOP) return TPS_ERR_ARG;
-    if (n_top > 0 && (!out_top_idx || !out_top_logprob)) return TPS_ERR_ARG;
-    const int es = elem_bytes(dtype);
-    if (!es) return TPS_ERR_DTYPE;
-    if (B == 0) return TPS_OK;
-    if (!logits || !temperature || !top_k || !top_p || !min_p || !seed || !out_token) return TPS_ERR_ARG;
-    if (!aligned(logits, es) || !aligned(temperature, 4) || !aligned(top_k, 4) || !aligned(top_p, 4) ||
-        !aligned(min_p, 4) || !aligned(seed, 8) || !aligned(out_token, 4) || (out_probs && !aligned(out_probs, 4)) ||
-        (out_status && !aligned(out_status, 4)) || (out_cutoff && !aligned(out_cutoff, 4)) ||
-        (out_kept && !aligned(out_kept, 4)) || (out_logprob && !aligned(out_logprob, 4)) ||
-        (n_top > 0 && (!aligned(out_top_idx, 4) || !aligned(out_top_logprob, 4))))
-        return TPS_ERR_ALIGN;
-    if (V > kMaxVocabMass || V > INT32_MAX) return TPS_ERR_UNSUPPORTED_V;
-    if (B > (int64_t)INT32_MAX / kMaxCluster) return TPS_ERR_ARG;
-
-    DeviceInfo* d = nullptr;
-    if (!device_info(&d)) return fail_cuda(cudaGetLastError());
-    const int Cfit = choose_cluster(*d, es, B, V);
-    const bool use_stream = kernel == TPS_KERNEL_STREAM || (kernel == TPS_KERNEL_AUTO && B >= kStreamMinRows) ||
-                            (kernel == TPS_KERNEL_AUTO && Cfit == 0);
-    // A large batch is split: the streaming kernel takes the rows with min-p (and greedy and failed
-    // rows), the cluster kernel, launched right behind it, the rows that need the general path.
-    const bool split = kernel == TPS_KERNEL_AUTO && use_stream && Cfit != 0;
-    const int C = use_stream ? (split ? Cfit : 1) : Cfit;
-    if (C == 0) return TPS_ERR_UNSUPPORTED_V;
-    const uint32_t cap = (use_stream && !split) ? 0u : slice_cap_bytes(V, es, C);
-    const size_t smem = smem_bytes(cap);
-
-    tps::Args a;
-    a.logits = logits;
-    a.B = B;
-    a.V = V;
-    a.ld = ld;
-    a.temperature = temperature;
-    a.top_k = top_k;
-    a.top_p = top_p;
-    a.min_p = min_p;
-    a.seed = seed;
-    a.step = step;
-    a.out_token = out_token;
-    a.out_probs = out_probs;
-    a.out_status = out_status;
-    a.out_cutoff = out_cutoff;
-    a.out_kept = out_kept;
-    a.out_logprob = out_logprob;
-    a.n_top = n_top;
-    a.out_top_idx = n_top > 0 ? out_top_idx : nullptr;
-    a.out_top_logprob = n_top > 0 ? out_top_logprob : nullptr;
-    a.slice_cap = cap;
-    a.route = split ? tps::kRouteCluster : tps::kRouteAll;
-
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    if (use_stream && !split) {
-        e = (dtype == TPS_F32) ? launch_stream<float>(*d, &d->sattrs_f32, a, false, st)
-                               : launch_stream<__nv_bfloat16>(*d, &d->sattrs_bf16, a, false, st);
-        if (e != cudaSuccess) return fail_cuda(e);
-        return TPS_OK;
-    }
-    int Cl = C;
-    size_t sm = smem;
-    // A cluster wider than 8 that the GPU cannot co-schedule falls back to 8 CTAs, if they hold the row.
-    auto use_portable = [&]() -> bool {
-        if (smem_bytes(slice_cap_bytes(V, es, 8)) > (size_t)d->smem_optin) return false;
-        Cl = 8;
-        a.slice_cap = slice_cap_bytes(V, es, 8);
-        sm = smem_bytes(a.slice_cap);
-        return true;
-    };
-    if (dtype == TPS_F32) {
-        if (!d->attrs_f32.load(std::memory_order_acquire)) {
-            e = prepare_kernel<float>(*d);
-            if (e != cudaSuccess) return fail_cuda(e);
-            d->attrs_f32.store(true, std::memory_order_release);
-        }
-        if (Cl > 8 && !wide_cluster_ok<float>(*d, 0, Cl, sm) && !use_portable()) return TPS_ERR_UNSUPPORTED_V;
-        const int64_t ncl = split ? std::min<int64_t>(B, resident_clusters<float>(*d, 0, Cl, sm)) : B;
-        e = launch<float>(a, Cl, sm, ncl, st);
-    } else {
-        if (!d->attrs_bf16.load(std::memory_order_acquire)) {
-            e = prepare_kernel<__nv_bfloat16>(*d);
-            if (e != cudaSuccess) return fail_cuda(e);
-            d->attrs_bf16.store(true, std::memory_order_release);
-        }
-        if (Cl > 8 && !wide_cluster_ok<__nv_bfloat16>(*d, 1, Cl, sm) && !use_portable())
-            return TPS_ERR_UNSUPPORTED_V;
-        const int64_t ncl = split ? std::min<int64_t>(B, resident_clusters<__nv_bfloat16>(*d, 1, Cl, sm)) : B;
-        e = launch<__nv_bfloat16>(a, Cl, sm, ncl, st);
-    }
-    if (e != cudaSuccess) return fail_cuda(e);
-    if (split) {  // the rest of the batch, behind the cluster kernel
-        a.route = tps::kRouteStream;
-        a.slice_cap = 0;
-        e = (dtype == TPS_F32) ? launch_stream<float>(*d, &d->sattrs_f32, a, true, st)
-                               : launch_stream<__nv_bfloat16>(*d, &d->sattrs_bf16, a, true, st);
-        if (e != cudaSuccess) return fail_cuda(e);
-    }
-    return TPS_OK;
+    Call c;
+    c.logits = logits;
+    c.dtype = dtype;
+    c.B = B;
+    c.V = V;
+    c.ld = ld;
+    c.temperature = temperature;
+    c.top_k = top_k;
+    c.top_p = top_p;
+    c.min_p = min_p;
+    c.seed = seed;
+    c.step = step;
+    c.out_token = out_token;
+    c.out_probs = out_probs;
+    c.out_status = out_status;
+    c.out_cutoff = out_cutoff;
+    c.out_kept = out_kept;
+    c.out_logprob = out_logprob;
+    c.n_top = n_top;
+    c.out_top_idx = out_top_idx;
+    c.out_top_logprob = out_top_logprob;
+    c.kernel = kernel;
+    c.stream = static_cast<cudaStream_t>(stream);
+    return sample_call(c, ScratchSource::kPool);
 }
 
 int tps_apply_penalties(void* logits, int dtype, int64_t B, int64_t V, int64_t ld, const int32_t* history, int64_t H,
@@ -457,6 +569,53 @@ int tps_apply_penalties(void* logits, int dtype, int64_t B, int64_t V, int64_t l
     const cudaError_t e = tps::launch_penalties(a, dtype == TPS_BF16, d->sms, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(e);
     return TPS_OK;
+}
+
+int tps_spec_accept(const void* target_logits, const void* draft_logits, int dtype, int64_t B, int64_t V, int64_t ld,
+                    const float* target_temperature, const int32_t* target_top_k, const float* target_top_p,
+                    const float* target_min_p, const float* draft_temperature, const int32_t* draft_top_k,
+                    const float* draft_top_p, const float* draft_min_p, const int32_t* draft_token,
+                    const uint64_t* seed, uint64_t step, int32_t* out_token, int32_t* out_accepted,
+                    int32_t* out_status, void* stream)
+{
+    if (B < 0 || V < 1 || ld < V) return TPS_ERR_ARG;
+    const int es = elem_bytes(dtype);
+    if (!es) return TPS_ERR_DTYPE;
+    if (B == 0) return TPS_OK;
+    if (!target_logits || !draft_logits || !target_temperature || !target_top_k || !target_top_p || !target_min_p ||
+        !draft_temperature || !draft_top_k || !draft_top_p || !draft_min_p || !draft_token || !seed || !out_token)
+        return TPS_ERR_ARG;
+    if (!aligned(target_logits, es) || !aligned(draft_logits, es) || !aligned(target_temperature, 4) ||
+        !aligned(target_top_k, 4) || !aligned(target_top_p, 4) || !aligned(target_min_p, 4) ||
+        !aligned(draft_temperature, 4) || !aligned(draft_top_k, 4) || !aligned(draft_top_p, 4) ||
+        !aligned(draft_min_p, 4) || !aligned(draft_token, 4) || !aligned(seed, 8) || !aligned(out_token, 4) ||
+        (out_accepted && !aligned(out_accepted, 4)) || (out_status && !aligned(out_status, 4)))
+        return TPS_ERR_ALIGN;
+    if (V > kMaxVocabMass || V > INT32_MAX) return TPS_ERR_UNSUPPORTED_V;
+    DeviceInfo* d = nullptr;
+    if (!device_info(&d)) return fail_cuda(cudaGetLastError());
+    tps::SpecArgs a;
+    a.target = target_logits;
+    a.draft = draft_logits;
+    a.B = B;
+    a.V = V;
+    a.ld = ld;
+    a.tT = target_temperature;
+    a.tK = target_top_k;
+    a.tP = target_top_p;
+    a.tM = target_min_p;
+    a.dT = draft_temperature;
+    a.dK = draft_top_k;
+    a.dP = draft_top_p;
+    a.dM = draft_min_p;
+    a.draft_token = draft_token;
+    a.seed = seed;
+    a.step = step;
+    a.out_token = out_token;
+    a.out_accepted = out_accepted;
+    a.out_status = out_status;
+    const cudaError_t e = tps::launch_spec(a, dtype == TPS_BF16, d->sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TPS_OK : fail_cuda(e);
 }
 
 int tps_sample_kernel(const void* logits, int dtype, int64_t B, int64_t V, int64_t ld, const float* temperature,

@@ -316,46 +316,40 @@ __device__ __forceinline__ void fail_row(const Args& a, int64_t row, int32_t sta
 }
 
 // ---------------------------------------------------------------------------------------------
-// The kernel.  Grid: ncl clusters of C CTAs along x; cluster q samples rows q, q + ncl, ...  With
-// a.route == kRouteAll every row is sampled (ncl = B: one row per cluster); with kRouteCluster
-// only the rows routed_to_cluster() selects, found by one parallel read of the rows' parameters
-// (the grid then holds as many clusters as the GPU keeps resident).
+// The kernel.  Grid: clusters of C CTAs along x.  With a.route == kRouteAll cluster q samples row q
+// (one cluster per row).  With kRouteList the kernel runs behind the streaming kernel of a split
+// batch (as its programmatic dependent): it waits for that kernel to finish, then its clusters
+// claim the rows it listed in the scratch one at a time, so rows of very different cost spread
+// over the clusters by themselves.
 // ---------------------------------------------------------------------------------------------
 template <typename TIn>
 __global__ void __launch_bounds__(kThreads, 2) sample_rows_kernel(const Args a)
 {
     extern __shared__ __align__(128) unsigned char dsmem[];
     ClusterTopo topo;
-    const uint32_t C = topo.C;
     Shared& s = *reinterpret_cast<Shared*>(dsmem + a.slice_cap);
     topo.hr = reinterpret_cast<uint32_t*>(dsmem + a.slice_cap + sizeof(Shared));  // cluster-wide fine counts
     int32_t* rows = reinterpret_cast<int32_t*>(dsmem + a.slice_cap + sizeof(Shared) + 2 * kFineBins * sizeof(uint32_t));
     Inbox* inbox = reinterpret_cast<Inbox*>(reinterpret_cast<unsigned char*>(rows) + kThreads * sizeof(int32_t));
-    const int64_t ncl = (int64_t)(gridDim.x / C), cid = (int64_t)(blockIdx.x / C);
+    const int64_t cid = (int64_t)(blockIdx.x / topo.C);
     const int tid = threadIdx.x;
-    // A kernel launched as this one's programmatic dependent (the streaming kernel of a split batch)
-    // may be scheduled from now on: it samples the other rows and waits for this grid before it exits.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    bool alive = true;
-    if (a.route == kRouteAll && ncl >= a.B) {  // one row per cluster: no list to build
+    if (a.route != kRouteList) {
         if (cid < a.B) (void)cluster_row<TIn>(a, topo, s, inbox, dsmem, cid);
         return;
     }
-    for (int64_t base = cid; base < a.B; base += (int64_t)kThreads * ncl) {
-        // this pass's rows: base + t * ncl for t < kThreads, kept in order
-        const int64_t r = base + (int64_t)tid * ncl;
-        bool mine = r < a.B;
-        if (mine && a.route == kRouteCluster) mine = routed_to_cluster(a.temperature[r], a.top_p[r], a.min_p[r]);
-        uint64_t total;
-        const uint32_t at = (uint32_t)block_exscan_u64(mine ? 1u : 0u, s, &total);
-        if (mine) rows[at] = (int32_t)r;
-        cta_sync();
-        for (uint32_t k = 0; k < (uint32_t)total; ++k) {
-            const int64_t row = rows[k];
-            if (alive) alive = cluster_row<TIn>(a, topo, s, inbox, dsmem, row);
-            else if (topo.rank == 0) fail_row(a, row, kRowTimeout);
-        }
-        cta_sync();  // rows[] is rewritten by the next pass
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the streaming kernel has listed every row
+    const ScratchView sv(a);
+    const uint32_t nlisted = __ldcg(&sv.hdr->ngen);
+    bool alive = true;
+    for (;;) {
+        if (topo.rank == 0 && tid == 0) s.pub_claim = atomicAdd(&sv.hdr->gclaim, 1u);
+        topo.sync();
+        const uint32_t k = *topo.map(&s.pub_claim, 0u);
+        topo.sync();  // every CTA has read the claim before rank 0 takes the next one
+        if (k >= nlisted) break;
+        const int64_t row = __ldcg(&sv.genlist[k]);
+        if (alive) alive = cluster_row<TIn>(a, topo, s, inbox, dsmem, row);
+        else if (topo.rank == 0) fail_row(a, row, kRowTimeout);
     }
 }
 

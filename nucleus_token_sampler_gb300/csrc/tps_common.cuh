@@ -51,11 +51,87 @@ struct Args {
     float* out_top_logprob;  // [B, n_top]: their ln P
     uint32_t slice_cap;  // bytes reserved for the slice at the start of dynamic shared memory
     uint32_t route;      // which rows the kernel samples (RowRoute)
+    // Streaming kernel's work: rows [0, b_whole) are claimed whole; each of the last nsplit rows is
+    // claimed as nseg segments, merged by the CTA that finishes a row's last segment.
+    void* scratch;       // global scratch of the call (ScratchLayout), cleared before the kernel claims
+    int64_t b_whole;
+    int64_t nsplit;
+    int32_t nseg;
+    uint64_t wait_ns;     // limit of the consumers' waits in the streaming kernel (kWaitLimitNs; shorter in a test)
+    int64_t stall_chunk;  // test hook: chunk whose copy CTA 0 of the streaming kernel withholds (-1: none)
 };
 
 // Which rows a kernel samples.  A large batch is split between the two kernels: the streaming
-// kernel takes every row but those routed_to_cluster() selects, which the cluster kernel takes.
-enum RowRoute : uint32_t { kRouteAll = 0, kRouteStream = 1, kRouteCluster = 2 };
+// kernel takes every row but those routed_to_cluster() selects and lists those in the scratch; the
+// cluster kernel, launched behind it, takes the listed rows.
+enum RowRoute : uint32_t { kRouteAll = 0, kRouteStream = 1, kRouteList = 2 };
+
+// ---------------------------------------------------------------------------------------------
+// Global scratch of one streaming call.  Work is claimed dynamically: a claim q < b_whole is row q,
+// whole; a claim q >= b_whole is segment (q - b_whole) % nseg of row b_whole + (q - b_whole) / nseg.
+// A CTA's first claim is its block index; later claims come from `claim`.  Each segment of a split
+// row publishes a partial result (its maximum and the tokens it listed); the CTA whose arrival on
+// the row's counter completes the count merges them.  Everything that must start at zero (the
+// header and the arrival counters) lies in the first clear_bytes() bytes.
+// ---------------------------------------------------------------------------------------------
+struct ScratchHdr {
+    uint32_t claim;   // dynamic claims taken (claim q = gridDim.x + this counter)
+    uint32_t ngen;    // rows listed for the cluster kernel
+    uint32_t gclaim;  // listed rows the cluster kernel has claimed
+    uint32_t pad;
+};
+constexpr int kPartList = 256;  // tokens one segment publishes at most
+constexpr int kMaxSegments = 8;  // segments of a split row, at most (a merge parks 32 entries of each)
+struct PartHdr {
+    float max;       // the segment's maximum (NaN-propagating)
+    uint32_t n;      // tokens published
+    uint32_t flags;  // PartFlag bits
+    uint32_t pad;
+};
+enum PartFlag : uint32_t { kPartOverflow = 1, kPartTimeout = 2, kPartUnlisted = 4 };
+constexpr uint64_t kPartBytes = sizeof(PartHdr) + (uint64_t)kPartList * sizeof(uint64_t);
+
+struct ScratchLayout {
+    uint64_t arrive;   // uint32_t[nsplit]: segments of each split row published so far
+    uint64_t genlist;  // int32_t[B]: rows left to the cluster kernel
+    uint64_t parts;    // nsplit * nseg partials of kPartBytes
+    uint64_t total;
+    __host__ __device__ static ScratchLayout of(int64_t B, int64_t nsplit, int nseg)
+    {
+        ScratchLayout L;
+        L.arrive = sizeof(ScratchHdr);
+        L.genlist = L.arrive + 4ull * (uint64_t)nsplit;
+        L.parts = (L.genlist + 4ull * (uint64_t)B + 15ull) & ~15ull;
+        L.total = L.parts + (uint64_t)nsplit * (uint64_t)nseg * kPartBytes;
+        return L;
+    }
+    __host__ __device__ uint64_t clear_bytes() const { return genlist; }
+};
+
+struct ScratchView {
+    ScratchHdr* hdr;
+    uint32_t* arrive;
+    int32_t* genlist;
+    unsigned char* parts;
+    __device__ __forceinline__ explicit ScratchView(const Args& a)
+    {
+        const ScratchLayout L = ScratchLayout::of(a.B, a.nsplit, a.nseg);
+        unsigned char* base = static_cast<unsigned char*>(a.scratch);
+        hdr = reinterpret_cast<ScratchHdr*>(base);
+        arrive = reinterpret_cast<uint32_t*>(base + L.arrive);
+        genlist = reinterpret_cast<int32_t*>(base + L.genlist);
+        parts = base + L.parts;
+    }
+    __device__ __forceinline__ PartHdr* part_hdr(int64_t split_row, int seg, int nseg) const
+    {
+        return reinterpret_cast<PartHdr*>(parts + ((uint64_t)split_row * (uint64_t)nseg + (uint64_t)seg) * kPartBytes);
+    }
+    __device__ __forceinline__ uint64_t* part_ent(int64_t split_row, int seg, int nseg) const
+    {
+        return reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(part_hdr(split_row, seg, nseg)) +
+                                           sizeof(PartHdr));
+    }
+};
 
 // Rows left to the cluster kernel in a split batch: sampling with min-p off.  They need the general
 // path, which takes several passes over the row: on-chip in the cluster kernel, from global memory
@@ -82,6 +158,7 @@ struct Shared {
     uint32_t pub_ca;  // exact pass: tokens above the top-p window
     uint64_t pub_z;   // exact pass: fixed-point mass of the survivors
     uint64_t pub_a;   // exact pass: fixed-point mass above the top-p window
+    uint32_t pub_claim;  // list mode: the listed row this cluster claimed (rank 0's copy is read)
     // --- ragged elements
     int32_t nx;
     float xz[kMaxExtra];
@@ -358,8 +435,9 @@ using GlobalRow = VecSource<TIn, true>;
 
 // Maximum (NaN-propagating) over nvec 16-byte vectors, listing every element above thr through
 // list(z, i).  Each thread takes 16 elements per step and reduces them with a tree of max
-// operations; only a step whose maximum exceeds thr is looked at element by element, so a pass
-// costs about one instruction per element when little is listed.
+// operations -- three-input float maxima for float32, packed bfloat16x2 maxima for bfloat16 (no
+// unpacking) -- and only a step whose maximum exceeds thr is looked at element by element, so a pass
+// costs well under one instruction per element when little is listed.
 template <typename TIn, bool kGlobal, typename ListF>
 __device__ __forceinline__ float scan_max_list(const uint4* vec, int nvec, int32_t elem0, float thr, ListF&& list)
 {
@@ -381,27 +459,34 @@ __device__ __forceinline__ float scan_max_list(const uint4* vec, int nvec, int32
                 w[u] = neg_inf;
             }
         }
-        float z[U * EPV];
+        float m;
+        if constexpr (EPV == 4) {
+            float z[16];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            float t[EPV];
-            E::unpack(w[u], t);
-#pragma unroll
-            for (int j = 0; j < EPV; ++j) z[u * EPV + j] = t[j];
+            for (int u = 0; u < U; ++u) {
+                z[4 * u] = __uint_as_float(w[u].x);
+                z[4 * u + 1] = __uint_as_float(w[u].y);
+                z[4 * u + 2] = __uint_as_float(w[u].z);
+                z[4 * u + 3] = __uint_as_float(w[u].w);
+            }
+            const float n0 = fmax3_nan(fmax3_nan(z[0], z[1], z[2]), fmax3_nan(z[3], z[4], z[5]), fmax3_nan(z[6], z[7], z[8]));
+            const float n1 = fmax3_nan(fmax3_nan(z[9], z[10], z[11]), fmax3_nan(z[12], z[13], z[14]), z[15]);
+            m = fmax_nan(n0, n1);
+        } else {
+            const uint32_t c = bmax2_nan(bmax2_nan(bmax2_nan(w[0].x, w[0].y), bmax2_nan(w[0].z, w[0].w)),
+                                         bmax2_nan(bmax2_nan(w[1].x, w[1].y), bmax2_nan(w[1].z, w[1].w)));
+            m = fmax_nan(__uint_as_float(c << 16), __uint_as_float(c & 0xFFFF0000u));
         }
-        float m8[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) m8[j] = fmax_nan(z[j], z[j + 8]);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) m8[j] = fmax_nan(m8[j], m8[j + 4]);
-        const float m = fmax_nan(fmax_nan(m8[0], m8[2]), fmax_nan(m8[1], m8[3]));
         cm = fmax_nan(cm, m);
         if (m > thr) {
 #pragma unroll
-            for (int u = 0; u < U; ++u)
+            for (int u = 0; u < U; ++u) {
+                float t[EPV];
+                E::unpack(w[u], t);
 #pragma unroll
                 for (int j = 0; j < EPV; ++j)
-                    if (z[u * EPV + j] > thr) list(z[u * EPV + j], elem0 + (v + u * kThreads) * EPV + j);
+                    if (t[j] > thr) list(t[j], elem0 + (v + u * kThreads) * EPV + j);
+            }
         }
     }
     return cm;
@@ -1041,7 +1126,9 @@ __device__ __forceinline__ WarpResult warp_resolve(uint64_t* buf, const RowCtx& 
 
 // Resolve a row whose survivors are buf[0, n) (32 < n <= 256, distinct, any order) with one warp:
 // rank sort into sorted[], fixed-point mass prefixes in pre[0, n], the top-k and top-p class cuts,
-// then the race.  Lane l owns sorted positions [8 l, 8 l + 8).  Every lane returns the same result.
+// then the race.  For the scan and the cuts lane l owns sorted positions [8 l, 8 l + 8); the masses
+// and the race's Philox draws are spread over all lanes (position l + 32 m), so a list of a few dozen
+// survivors does not leave most lanes idle.  Every lane returns the same result.
 __device__ __forceinline__ WarpResult warp_resolve_big(const uint64_t* buf, uint64_t* sorted, uint64_t* pre, uint32_t n,
                                                        const RowCtx& r, const RaceCtx& rc, bool topk_on, int32_t K,
                                                        float P)
@@ -1060,6 +1147,9 @@ __device__ __forceinline__ WarpResult warp_resolve_big(const uint64_t* buf, uint
         sorted[rank] = v;
     }
     __syncwarp();
+    // masses at strided positions (every lane busy), parked in pre[] for the scan below
+    for (uint32_t pos = lane; pos < n; pos += 32) pre[pos] = qmass_d(dist(r, key_to_float(sb_key(sorted[pos]))));
+    __syncwarp();
     const uint32_t p0 = 8 * lane;
     uint64_t q[8];
     uint32_t kk[8];
@@ -1068,9 +1158,10 @@ __device__ __forceinline__ WarpResult warp_resolve_big(const uint64_t* buf, uint
     for (int m = 0; m < 8; ++m) {
         const uint32_t pos = p0 + m;
         kk[m] = (pos < n) ? sb_key(sorted[pos]) : 0u;
-        q[m] = (pos < n) ? qmass_d(dist(r, key_to_float(kk[m]))) : 0;
+        q[m] = (pos < n) ? pre[pos] : 0;
         loc += q[m];
     }
+    __syncwarp();  // every lane has read its masses before pre[] is overwritten with prefixes
     uint64_t inc = loc;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -1130,17 +1221,18 @@ __device__ __forceinline__ WarpResult warp_resolve_big(const uint64_t* buf, uint
         zk = pre[e];
     }
     const uint32_t key_cut = sb_key(sorted[nk - 1]);
-    // race over positions < nk
+    // race over positions < nk, strided over the lanes (position lane + 32 m) so every lane draws
     float k32[8], uu[8];
     float m32 = -INFINITY;
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
-        const uint32_t pos = p0 + m;
+        const uint32_t pos = lane + 32u * (uint32_t)m;
         k32[m] = -INFINITY;
         uu[m] = 0.f;
         if (pos < nk) {
-            uu[m] = race_u(rc, sb_idx(sorted[pos]));
-            k32[m] = race_key32(dist(r, key_to_float(kk[m])), uu[m]);
+            const uint64_t v = sorted[pos];
+            uu[m] = race_u(rc, sb_idx(v));
+            k32[m] = race_key32(dist(r, key_to_float(sb_key(v))), uu[m]);
             m32 = fmaxf(m32, k32[m]);
         }
     }
@@ -1149,11 +1241,13 @@ __device__ __forceinline__ WarpResult warp_resolve_big(const uint64_t* buf, uint
     const float tol = race_tol(dist(r, key_to_float(key_cut)));
     uint32_t nf = 0, fpos = 0;
 #pragma unroll
-    for (int m = 0; m < 8; ++m)
-        if (p0 + m < nk && k32[m] >= m32 - tol) {
+    for (int m = 0; m < 8; ++m) {
+        const uint32_t pos = lane + 32u * (uint32_t)m;
+        if (pos < nk && k32[m] >= m32 - tol) {
             ++nf;
-            fpos = p0 + m;
+            fpos = pos;
         }
+    }
     const uint32_t nfin = __reduce_add_sync(0xFFFFFFFFu, nf);
     int32_t token;
     if (nfin == 1) {
@@ -1165,10 +1259,11 @@ __device__ __forceinline__ WarpResult warp_resolve_big(const uint64_t* buf, uint
         a.idx = 0x7FFFFFFF;
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
-            const uint32_t pos = p0 + m;
+            const uint32_t pos = lane + 32u * (uint32_t)m;
             if (pos < nk && k32[m] >= m32 - tol) {
-                const double k64 = race_key64(r, key_to_float(kk[m]), uu[m]);
-                const int32_t i = sb_idx(sorted[pos]);
+                const uint64_t v = sorted[pos];
+                const double k64 = race_key64(r, key_to_float(sb_key(v)), uu[m]);
+                const int32_t i = sb_idx(v);
                 if (better(k64, i, a.key, a.idx)) {
                     a.key = k64;
                     a.idx = i;

@@ -259,6 +259,22 @@ __device__ __forceinline__ float fmax_nan(float a, float b)
     return r;
 }
 
+// Three-input float maximum with NaN propagation (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3_nan(float a, float b, float c)
+{
+    float r;
+    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Lane-wise maximum of two packed bfloat16 pairs with NaN propagation.
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // ---------------------------------------------------------------------------------------------
 // Warp reductions.
 // ---------------------------------------------------------------------------------------------

@@ -178,6 +178,35 @@ def test_edge_cases():
         check(_w(zz, T, k, p, m))
 
 
+def test_split_rows_every_outcome():
+    """Rows of 200,000 float32 logits are streamed as four segments merged by the CTA that finishes
+    a row last: every row status, greedy ties across segments, the maximum in any segment, min-p
+    rows, rows for the cluster kernel, and ragged, unaligned rows."""
+    V, B = 200000, 48
+    rng = np.random.default_rng(5)
+    z = rng.normal(0, 2.0, size=(B, V))
+    z[np.arange(B), rng.integers(0, V, B)] += 9.0       # one leader per row, anywhere
+    z[1, 7] = np.nan
+    z[2, V - 1] = np.inf
+    z[3, :] = -np.inf
+    z[4, [10, 60000, 150000, V - 2]] = 50.0              # greedy ties in different segments
+    z[5, :] = np.round(z[5, :])                           # big tie classes
+    z[6, : V // 2] = -np.inf                              # the first segments fully masked
+    T = np.full(B, 0.8)
+    T[4] = 0.0
+    T[7] = np.nan
+    T[8::6] = 0.0
+    k = np.where(np.arange(B) % 3 == 0, 40, 0)
+    p = np.where(np.arange(B) % 4 == 0, 1.0, 0.9)
+    m = np.where(np.arange(B) % 5 == 0, 0.0, 0.05)       # every fifth row goes to the cluster kernel
+    w = _w(z, T, k, p, m)
+    check(w, max_band_frac=0.1)
+    zb = np.zeros((B, V + 3))
+    zb[:, 1:V + 1] = z
+    base = torch.as_tensor(zb).float().cuda()[:, 1:V + 1]  # rows starting 4 bytes past a 16-byte boundary
+    check(w, logits=base, max_band_frac=0.1)
+
+
 def test_temperature_overflowing_distance():
     """A temperature so small that (zmax - z) / T overflows float to +inf for most of the row: those
     tokens fall in the last fine bin of the general path, where top-k (50 and 300, so the crossing is
@@ -310,8 +339,8 @@ def test_top_logprobs_big_tie_classes(kernel, dtype):
 @pytest.mark.gpu
 def test_kernels_per_call_follows_the_split_rule():
     f32 = torch.float32
-    assert tps.kernels_per_call(f32, 1024, 128256, "auto") == 2   # a large batch is split over both kernels
-    assert tps.kernels_per_call(f32, 1024, 128256, "stream") == 1
+    assert tps.kernels_per_call(f32, 1024, 128256, "auto") == 3   # scratch clear, streaming kernel, cluster kernel
+    assert tps.kernels_per_call(f32, 1024, 128256, "stream") == 2  # scratch clear, streaming kernel
     assert tps.kernels_per_call(f32, 1024, 128256, "cluster") == 1
     assert tps.kernels_per_call(f32, 8, 32000, "auto") == 1       # a small batch: the cluster kernel alone
 
