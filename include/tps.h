@@ -54,7 +54,8 @@ typedef enum {
     TPS_ERR_DTYPE = 2,         /* dtype is not a tps_dtype                                      */
     TPS_ERR_UNSUPPORTED_V = 3, /* V is above tps_max_vocab(dtype)                               */
     TPS_ERR_ALIGN = 4,         /* logits, out_probs or a parameter array is not element-aligned */
-    TPS_ERR_CUDA = 5           /* the CUDA runtime refused the launch (see tps_last_cuda_error) */
+    TPS_ERR_CUDA = 5,          /* the CUDA runtime refused the launch (see tps_last_cuda_error) */
+    TPS_ERR_SCRATCH = 6        /* tps_sample_noalloc: the call needs more than its fixed scratch   */
 } tps_status;
 
 /* Per-row outcome written to out_status. */
@@ -223,6 +224,30 @@ int tps_spec_accept(const void* target_logits, const void* draft_logits, int dty
                     const float* draft_top_p, const float* draft_min_p, const int32_t* draft_token,
                     const uint64_t* seed, uint64_t step, int32_t* out_token, int32_t* out_accepted,
                     int32_t* out_status, void* stream);
+
+/*
+ * tps_sample_noalloc -- tps_sample_full for callers that cannot allocate device memory while they
+ * sample (a serving loop that reserves all device memory up front, a host whose allocator belongs to
+ * another framework, code that must stay out of the driver's allocator).  The pages define no such
+ * call; it is this library's own.  Same arguments, rules and results as tps_sample_full; the only
+ * difference is where the streaming kernel's small per-call scratch lives: tps_sample_full draws it
+ * from the device's stream-ordered memory pool, this call uses a fixed array of 8 MiB compiled into
+ * the library (held on every GPU that loads the library until the process exits) and allocates
+ * nothing.
+ *   - A call whose scratch would exceed 8 MiB returns TPS_ERR_SCRATCH before enqueuing anything (a
+ *     decode batch of 1,024 rows x 128,256 float32 logits needs about 1.3 MiB; very large batches,
+ *     or rows above about 1.6 million elements split over many segments, need more).
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress): make
+ *     that first call before any stream capture.
+ *   - Every call shares the one array and clears the part that must start at zero itself, on its
+ *     stream.  Calls that overlap on the GPU race on the array: issue them in one stream, or order
+ *     their streams.
+ */
+int tps_sample_noalloc(const void* logits, int dtype, int64_t B, int64_t V, int64_t ld, const float* temperature,
+                       const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seed,
+                       uint64_t step, int32_t* out_token, float* out_probs, int32_t* out_status, float* out_cutoff,
+                       int32_t* out_kept, float* out_logprob, int32_t n_top, int32_t* out_top_idx,
+                       float* out_top_logprob, int kernel, void* stream);
 
 /* Kernels one tps_sample_kernel call with these arguments launches (1 or 2; 0 for arguments the call
  * would reject).  Host-only query. */

@@ -32,7 +32,7 @@ _NVCC = ["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo
 TPS_F32, TPS_BF16 = 0, 1
 ROW_STATUS = {0: "ok", 1: "nan", 2: "all_masked", 3: "bad_param", 4: "timeout"}
 _ERRORS = {1: "invalid argument", 2: "unknown dtype", 3: "vocabulary too large", 4: "misaligned pointer",
-           5: "CUDA runtime error"}
+           5: "CUDA runtime error", 6: "more scratch than the fixed array of tps_sample_noalloc holds"}
 
 _lock = threading.Lock()
 _lib = None
@@ -93,6 +93,8 @@ def load():
             lib.tps_sample_full.restype = I32
             lib.tps_sample_full.argtypes = [P, I32, I64, I64, I64, P, P, P, P, P, U64, P, P, P, P, P, P, I32, P, P,
                                             I32, P]
+            lib.tps_sample_noalloc.restype = I32
+            lib.tps_sample_noalloc.argtypes = lib.tps_sample_full.argtypes
             lib.tps_spec_accept.restype = I32
             lib.tps_spec_accept.argtypes = [P, P, I32, I64, I64, I64, P, P, P, P, P, P, P, P, P, P, U64, P, P, P, P]
             lib.tps_max_vocab.restype = I64

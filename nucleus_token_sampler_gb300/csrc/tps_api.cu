@@ -320,10 +320,11 @@ struct Call {
     int64_t stall_chunk = -1;
 };
 
-// Where a streaming call's scratch comes from.
-enum class ScratchSource { kPool };
+// Where a streaming call's scratch comes from: the device's stream-ordered pool, or a fixed array
+// (`fixed`, `fixed_bytes`) the call uses as it is.
+enum class ScratchSource { kPool, kFixed };
 
-int sample_call(const Call& c, ScratchSource src)
+int sample_call(const Call& c, ScratchSource src, void* fixed = nullptr, size_t fixed_bytes = 0)
 {
     const int64_t B = c.B, V = c.V;
     if (c.kernel < TPS_KERNEL_AUTO || c.kernel > TPS_KERNEL_STREAM) return TPS_ERR_ARG;
@@ -416,6 +417,9 @@ int sample_call(const Call& c, ScratchSource src)
     if (src == ScratchSource::kPool) {
         e = cudaMallocAsync(&scratch, (size_t)pl.layout.total, st);
         if (e != cudaSuccess) return fail_cuda(e);
+    } else {
+        if (pl.layout.total > (uint64_t)fixed_bytes) return TPS_ERR_SCRATCH;
+        scratch = fixed;
     }
     a.scratch = scratch;
     a.b_whole = pl.b_whole;
@@ -460,6 +464,7 @@ const char* tps_status_string(int status)
     case TPS_ERR_UNSUPPORTED_V: return "vocabulary too large for this device";
     case TPS_ERR_ALIGN: return "pointer not aligned to its element type";
     case TPS_ERR_CUDA: return "CUDA runtime error";
+    case TPS_ERR_SCRATCH: return "the call needs more scratch than the fixed scratch array of tps_sample_noalloc holds";
     case 100 + TPS_ROW_OK: return "row ok";
     case 100 + TPS_ROW_NAN: return "row holds a NaN or +inf logit";
     case 100 + TPS_ROW_ALL_MASKED: return "every logit of the row is -inf";
@@ -642,6 +647,97 @@ int tps_sample(const void* logits, int dtype, int64_t B, int64_t V, const float*
 {
     return tps_sample_ex(logits, dtype, B, V, V, temperature, top_k, top_p, min_p, seed, step, out_token,
                          out_probs, nullptr, nullptr, nullptr, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocAddr {
+    std::atomic<bool> ready{false};
+    void* ptr = nullptr;
+};
+NoAllocAddr g_noalloc_addr[kMaxDevices];
+std::mutex g_noalloc_mu;
+
+// The fixed array's device address on the current device (looked up once per device).
+cudaError_t noalloc_scratch(void** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    NoAllocAddr& na = g_noalloc_addr[dev];
+    if (!na.ready.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lk(g_noalloc_mu);
+        if (!na.ready.load(std::memory_order_relaxed)) {
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+            if (e != cudaSuccess) return e;
+            na.ptr = p;
+            na.ready.store(true, std::memory_order_release);
+        }
+    }
+    *out = na.ptr;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+// ---------------------------------------------------------------------------------------------
+// tps_sample_noalloc: the sampling call for callers that cannot allocate device memory.  Some
+// callers may not allocate on the device at all while they sample: a serving loop that reserves
+// all device memory up front and must not meet an allocation failure mid-request, a host whose
+// allocator is owned by another framework (allocating behind its back would break its accounting),
+// or code that must not enter the driver's allocator for latency reasons.  The ordinary calls draw
+// the streaming kernel's small per-call scratch from the device's stream-ordered pool
+// (cudaMallocAsync); this call uses a fixed array compiled into the library instead.  The array is
+// kNoAllocScratchBytes of device memory on every GPU that loads the library, held until the process
+// exits.  Its device address is looked up once per device (cudaGetSymbolAddress, with that device
+// current) by the first call on that device, so that first call should come before any stream
+// capture.  Every call shares the one array and leaves its last contents there: the part that must
+// start at zero (the claim and arrival counters) is cleared by each call's own clearing kernel, on the
+// call's stream.  Two calls that overlap on the GPU (different streams, no ordering between them)
+// race on the array and must not be issued.
+// ---------------------------------------------------------------------------------------------
+int tps_sample_noalloc(const void* logits, int dtype, int64_t B, int64_t V, int64_t ld, const float* temperature,
+                       const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seed,
+                       uint64_t step, int32_t* out_token, float* out_probs, int32_t* out_status, float* out_cutoff,
+                       int32_t* out_kept, float* out_logprob, int32_t n_top, int32_t* out_top_idx,
+                       float* out_top_logprob, int kernel, void* stream)
+{
+    Call c;
+    c.logits = logits;
+    c.dtype = dtype;
+    c.B = B;
+    c.V = V;
+    c.ld = ld;
+    c.temperature = temperature;
+    c.top_k = top_k;
+    c.top_p = top_p;
+    c.min_p = min_p;
+    c.seed = seed;
+    c.step = step;
+    c.out_token = out_token;
+    c.out_probs = out_probs;
+    c.out_status = out_status;
+    c.out_cutoff = out_cutoff;
+    c.out_kept = out_kept;
+    c.out_logprob = out_logprob;
+    c.n_top = n_top;
+    c.out_top_idx = out_top_idx;
+    c.out_top_logprob = out_top_logprob;
+    c.kernel = kernel;
+    c.stream = static_cast<cudaStream_t>(stream);
+    void* scratch = nullptr;
+    const cudaError_t e = noalloc_scratch(&scratch);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return sample_call(c, ScratchSource::kFixed, scratch, kNoAllocScratchBytes);
 }
 
 }  // extern "C"
