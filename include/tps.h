@@ -191,6 +191,30 @@ int tps_apply_penalties(void* logits, int dtype, int64_t B, int64_t V, int64_t l
                         const float* frequency, const float* presence, int32_t* out_status, void* stream);
 
 /*
+ * tps_sample_rejection -- the same kept set and distribution as tps_sample, drawn by sort-free
+ * rejection rounds instead of one race over the kept set ("Top-p (Nucleus) Sampling, in depth",
+ * 'Sort-free top-p by rejection sampling': a token is in the nucleus exactly when the mass of
+ * strictly more probable tokens is below p, so a draw is tested with one reduction instead of a
+ * sort; a rejected draw raises the pivot and drops the rejected token and everything less probable).
+ *   S = the survivors of min-p and top-k, Z_S their mass.  Round r races among the survivors above
+ *   the pivot (all of S in round 0): argmax of -(zmax - z_i)/T - ln(-ln u_i), lowest index on equal
+ *   keys.  The winner t is accepted when it holds the largest logit, when p >= 1, or when the mass of
+ *   the survivors with a larger logit is below p Z_S; otherwise its logit becomes the pivot.
+ *   Round r's uniforms: as tps_sample's, with r + 1 in bits 18..31 of the counter's first word
+ *   (counter ((i / 4) | (r + 1) << 18, b, step low, step high)), so they never coincide with them.
+ *   The draw follows the renormalised kept distribution but differs from tps_sample's token.
+ *
+ *   Arguments as tps_sample_ex (out_status, out_cutoff, out_kept: NULL or [B]; cutoff and kept are
+ *   tps_sample's, the nucleus itself), plus out_rounds: NULL or [B] int32, the rounds the row took
+ *   (0 for greedy and failed rows).  All pointers are caller-owned device memory; the call allocates
+ *   nothing and is stream-ordered on `stream`.
+ */
+int tps_sample_rejection(const void* logits, int dtype, int64_t B, int64_t V, int64_t ld, const float* temperature,
+                         const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seed,
+                         uint64_t step, int32_t* out_token, int32_t* out_status, float* out_cutoff, int32_t* out_kept,
+                         int32_t* out_rounds, void* stream);
+
+/*
  * tps_spec_accept -- speculative acceptance of one draft token per row on truncated distributions
  * ("Top-p (Nucleus) Sampling, in depth", 'Logprobs, speculative decoding and reproducibility': accept
  * a draft token x with probability min(1, P(x)/Q(x)); on rejection draw from the normalised positive

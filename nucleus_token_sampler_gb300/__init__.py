@@ -14,7 +14,7 @@ import threading
 
 import torch
 
-__all__ = ["build", "load", "sample", "apply_penalties", "spec_accept", "TPS_F32", "TPS_BF16", "ROW_STATUS", "library_path", "max_vocab",
+__all__ = ["build", "load", "sample", "sample_rejection", "apply_penalties", "spec_accept", "TPS_F32", "TPS_BF16", "ROW_STATUS", "library_path", "max_vocab",
            "cluster_size", "kernels_per_call", "version"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -23,9 +23,9 @@ _LIB = os.path.join(_HERE, "libtps.so")
 _INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
 # The ABI and launch code, and one translation unit per (kernel, element type): compiled in parallel.
 _SOURCES = ["tps_api.cu", "tps_k_cluster_f32.cu", "tps_k_cluster_bf16.cu", "tps_k_stream_f32.cu",
-            "tps_k_stream_bf16.cu", "tps_k_penalty.cu", "tps_k_spec.cu"]
+            "tps_k_stream_bf16.cu", "tps_k_penalty.cu", "tps_k_spec.cu", "tps_k_reject.cu"]
 _HEADERS = ["tps_device.cuh", "tps_common.cuh", "tps_cluster.cuh", "tps_stream.cuh", "tps_penalty.cuh",
-            "tps_spec.cuh", "tps_kernels.h"]
+            "tps_spec.cuh", "tps_reject.cuh", "tps_kernels.h"]
 _NVCC = ["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
          "-Xcompiler", "-fPIC"]
 
@@ -95,6 +95,8 @@ def load():
                                             I32, P]
             lib.tps_sample_noalloc.restype = I32
             lib.tps_sample_noalloc.argtypes = lib.tps_sample_full.argtypes
+            lib.tps_sample_rejection.restype = I32
+            lib.tps_sample_rejection.argtypes = [P, I32, I64, I64, I64, P, P, P, P, P, U64, P, P, P, P, P, P]
             lib.tps_spec_accept.restype = I32
             lib.tps_spec_accept.argtypes = [P, P, I32, I64, I64, I64, P, P, P, P, P, P, P, P, P, P, U64, P, P, P, P]
             lib.tps_max_vocab.restype = I64
@@ -335,3 +337,33 @@ def spec_accept(target_logits: torch.Tensor, draft_logits: torch.Tensor, target,
     if not diagnostics:
         return tok
     return {"token": tok, "accepted": acc, "status": st}
+
+
+def sample_rejection(logits: torch.Tensor, temperature, top_k, top_p, min_p, seed, step: int = 0, *,
+                     diagnostics: bool = False, stream=None):
+    """One token per row drawn by sort-free rejection rounds: the same kept set and distribution as
+    ``sample``, other uniforms (``tps_sample_rejection``).  Returns the [B] int32 tokens, or a dict
+    with ``token``, ``status``, ``cutoff``, ``kept`` and ``rounds`` when ``diagnostics`` is set."""
+    if not logits.is_cuda or logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be a [B, V] CUDA tensor with unit stride along V")
+    B, V = logits.shape
+    ld = logits.stride(0) if B > 1 else V
+    dev = logits.device
+    code = _dtype_code(logits.dtype)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev), torch.cuda.stream(s):
+        T = _param(temperature, B, torch.float32, dev)
+        K = _param(top_k, B, torch.int32, dev)
+        P = _param(top_p, B, torch.float32, dev)
+        M = _param(min_p, B, torch.float32, dev)
+        S = _param(seed, B, torch.int64, dev)
+        tok = torch.empty(B, dtype=torch.int32, device=dev)
+        extra = [torch.empty(B, dtype=dt, device=dev) if diagnostics else None
+                 for dt in (torch.int32, torch.float32, torch.int32, torch.int32)]
+        rc = load().tps_sample_rejection(_ptr(logits), code, B, V, ld, _ptr(T), _ptr(K), _ptr(P), _ptr(M), _ptr(S),
+                                         int(step) & ((1 << 64) - 1), _ptr(tok), *[_ptr(x) for x in extra],
+                                         ctypes.c_void_p(s.cuda_stream))
+    _check(rc)
+    if not diagnostics:
+        return tok
+    return dict(zip(("token", "status", "cutoff", "kept", "rounds"), [tok] + extra))

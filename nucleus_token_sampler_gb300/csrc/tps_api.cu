@@ -22,6 +22,7 @@
 #include "tps_cluster.cuh"
 #include "tps_kernels.h"
 #include "tps_penalty.cuh"
+#include "tps_reject.cuh"
 #include "tps_spec.cuh"
 #include "tps_stream.cuh"
 
@@ -574,6 +575,44 @@ int tps_apply_penalties(void* logits, int dtype, int64_t B, int64_t V, int64_t l
     const cudaError_t e = tps::launch_penalties(a, dtype == TPS_BF16, d->sms, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(e);
     return TPS_OK;
+}
+
+int tps_sample_rejection(const void* logits, int dtype, int64_t B, int64_t V, int64_t ld, const float* temperature,
+                         const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seed,
+                         uint64_t step, int32_t* out_token, int32_t* out_status, float* out_cutoff, int32_t* out_kept,
+                         int32_t* out_rounds, void* stream)
+{
+    if (B < 0 || V < 1 || ld < V) return TPS_ERR_ARG;
+    const int es = elem_bytes(dtype);
+    if (!es) return TPS_ERR_DTYPE;
+    if (B == 0) return TPS_OK;
+    if (!logits || !temperature || !top_k || !top_p || !min_p || !seed || !out_token) return TPS_ERR_ARG;
+    if (!aligned(logits, es) || !aligned(temperature, 4) || !aligned(top_k, 4) || !aligned(top_p, 4) ||
+        !aligned(min_p, 4) || !aligned(seed, 8) || !aligned(out_token, 4) || (out_status && !aligned(out_status, 4)) ||
+        (out_cutoff && !aligned(out_cutoff, 4)) || (out_kept && !aligned(out_kept, 4)) ||
+        (out_rounds && !aligned(out_rounds, 4)))
+        return TPS_ERR_ALIGN;
+    if (V > kMaxVocabMass || V > INT32_MAX) return TPS_ERR_UNSUPPORTED_V;
+    DeviceInfo* d = nullptr;
+    if (!device_info(&d)) return fail_cuda(cudaGetLastError());
+    tps::RejectArgs ra = {};
+    ra.a.logits = logits;
+    ra.a.B = B;
+    ra.a.V = V;
+    ra.a.ld = ld;
+    ra.a.temperature = temperature;
+    ra.a.top_k = top_k;
+    ra.a.top_p = top_p;
+    ra.a.min_p = min_p;
+    ra.a.seed = seed;
+    ra.a.step = step;
+    ra.a.out_token = out_token;
+    ra.a.out_status = out_status;
+    ra.a.out_cutoff = out_cutoff;
+    ra.a.out_kept = out_kept;
+    ra.out_rounds = out_rounds;
+    const cudaError_t e = tps::launch_reject(ra, dtype == TPS_BF16, d->sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TPS_OK : fail_cuda(e);
 }
 
 int tps_spec_accept(const void* target_logits, const void* draft_logits, int dtype, int64_t B, int64_t V, int64_t ld,
