@@ -273,6 +273,20 @@ int tps_sample_noalloc(const void* logits, int dtype, int64_t B, int64_t V, int6
                        int32_t* out_kept, float* out_logprob, int32_t n_top, int32_t* out_top_idx,
                        float* out_top_logprob, int kernel, void* stream);
 
+/*
+ * tps_sample_stall_test -- a test hook for the bounded waits (not for production use).  Samples like
+ * tps_sample_ex with the streaming kernel, except that CTA 0 withholds the copy of its chunk number
+ * `stall_chunk` (counted from 0; -1: none), so that stage never fills, and every wait for data or
+ * for a hand-over gives up after `wait_ns` nanoseconds (1 .. 10^9) instead of one second.  The
+ * waits for copies already in flight keep their full limit.  Rows the stalled CTA could not finish
+ * report TPS_ROW_TIMEOUT with token -1; every other row is sampled as usual; the call returns and
+ * the context stays usable.  Returns TPS_ERR_ARG for wait_ns outside that range.
+ */
+int tps_sample_stall_test(const void* logits, int dtype, int64_t B, int64_t V, const float* temperature,
+                          const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seed,
+                          uint64_t step, int32_t* out_token, int32_t* out_status, int64_t stall_chunk,
+                          uint64_t wait_ns, void* stream);
+
 /* Kernels one tps_sample_kernel call with these arguments launches (1 or 2; 0 for arguments the call
  * would reject).  Host-only query. */
 int tps_kernels_per_call(int dtype, int64_t B, int64_t V, int kernel);

@@ -95,6 +95,8 @@ def load():
                                             I32, P]
             lib.tps_sample_noalloc.restype = I32
             lib.tps_sample_noalloc.argtypes = lib.tps_sample_full.argtypes
+            lib.tps_sample_stall_test.restype = I32
+            lib.tps_sample_stall_test.argtypes = [P, I32, I64, I64, P, P, P, P, P, U64, P, P, I64, U64, P]
             lib.tps_sample_rejection.restype = I32
             lib.tps_sample_rejection.argtypes = [P, I32, I64, I64, I64, P, P, P, P, P, U64, P, P, P, P, P, P]
             lib.tps_spec_accept.restype = I32

@@ -577,6 +577,40 @@ int tps_apply_penalties(void* logits, int dtype, int64_t B, int64_t V, int64_t l
     return TPS_OK;
 }
 
+int tps_sample_stall_test(const void* logits, int dtype, int64_t B, int64_t V, const float* temperature,
+                          const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seed,
+                          uint64_t step, int32_t* out_token, int32_t* out_status, int64_t stall_chunk,
+                          uint64_t wait_ns, void* stream)
+{
+    if (wait_ns == 0 || wait_ns > tps::kWaitLimitNs) return TPS_ERR_ARG;
+    Call c;
+    c.logits = logits;
+    c.dtype = dtype;
+    c.B = B;
+    c.V = V;
+    c.ld = V;
+    c.temperature = temperature;
+    c.top_k = top_k;
+    c.top_p = top_p;
+    c.min_p = min_p;
+    c.seed = seed;
+    c.step = step;
+    c.out_token = out_token;
+    c.out_probs = nullptr;
+    c.out_status = out_status;
+    c.out_cutoff = nullptr;
+    c.out_kept = nullptr;
+    c.out_logprob = nullptr;
+    c.n_top = 0;
+    c.out_top_idx = nullptr;
+    c.out_top_logprob = nullptr;
+    c.kernel = TPS_KERNEL_STREAM;
+    c.stream = static_cast<cudaStream_t>(stream);
+    c.wait_ns = wait_ns;
+    c.stall_chunk = stall_chunk;
+    return sample_call(c, ScratchSource::kPool);
+}
+
 int tps_sample_rejection(const void* logits, int dtype, int64_t B, int64_t V, int64_t ld, const float* temperature,
                          const int32_t* top_k, const float* top_p, const float* min_p, const uint64_t* seed,
                          uint64_t step, int32_t* out_token, int32_t* out_status, float* out_cutoff, int32_t* out_kept,

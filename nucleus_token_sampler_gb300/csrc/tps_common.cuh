@@ -78,7 +78,7 @@ struct ScratchHdr {
     uint32_t claim;   // dynamic claims taken (claim q = gridDim.x + this counter)
     uint32_t ngen;    // rows listed for the cluster kernel
     uint32_t gclaim;  // listed rows the cluster kernel has claimed
-    uint32_t pad;
+    uint32_t done;    // streaming CTAs that have stopped claiming
 };
 constexpr int kPartList = 256;  // tokens one segment publishes at most
 constexpr int kMaxSegments = 8;  // segments of a split row, at most (a merge parks 32 entries of each)

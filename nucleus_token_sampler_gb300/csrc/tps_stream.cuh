@@ -637,13 +637,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
             // This CTA's claims: its block index, then (fixed) its block index + gridDim.x, then the
             // counter's, from 2 gridDim.x on.  Every path that takes a unit takes it from here.
             uint32_t nclaims = 1;
-            auto claim = [&]() -> int64_t {
-                if (nclaims++ == 1) return (int64_t)blockIdx.x + (int64_t)gridDim.x;
+            auto claim_counter = [&]() -> int64_t {
                 if (!waited) {
                     wait_prerequisite();
                     waited = true;
                 }
                 return 2 * (int64_t)gridDim.x + (int64_t)atomicAdd(&sv.hdr->claim, 1u);
+            };
+            auto claim = [&]() -> int64_t {
+                if (nclaims++ == 1) return (int64_t)blockIdx.x + (int64_t)gridDim.x;
+                return claim_counter();
             };
             auto list_for_cluster = [&](int64_t row) {
                 if (!waited) {
@@ -656,8 +659,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
             auto put = [&](const StageInfo& info, const unsigned char* src, uint32_t bytes) -> bool {
                 const int stage = (int)(g % (uint64_t)nstage);
                 if (g >= (uint64_t)nstage) {
+                    // wait (bounded) for the scanners to release the stage; stop as soon as the CTA
+                    // is dead (its scanners then release nothing more)
                     const uint32_t ph = (uint32_t)(((g / (uint64_t)nstage) - 1) & 1u);
-                    if (!mbar_wait_bounded(&st.empty[stage], ph, kWaitLimitNs)) *vdead = 1u;
+                    const uint64_t t0 = globaltimer_ns();
+                    while (!mbar_wait_bounded(&st.empty[stage], ph, 1000000ull)) {
+                        if (*vdead || globaltimer_ns() - t0 > kWaitLimitNs) {
+                            *vdead = 1u;
+                            return false;
+                        }
+                    }
                 }
                 if (*vdead) return false;
                 st.info[stage] = info;
@@ -734,25 +745,28 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
                 (void)put(end, nullptr, 0);
             }
             st.units_put = nput;
-            if (*vdead) {
-                // stop streaming, but keep claiming, so that no row is left without an outcome
-                for (;;) {
-                    if (q >= Q) break;
-                    const Unit u = unit_of(a, q);
-                    const RowParams p = load_params(a, u.row);
-                    if (a.route == kRouteStream && routed_to_cluster(p.T, p.P, p.MP)) {
-                        if (u.seg == 0) list_for_cluster(u.row);
-                    } else {
-                        if (!waited) {
-                            wait_prerequisite();
-                            waited = true;
-                        }
-                        fail_unit(a, sv, q);
-                    }
-                    q = claim();
+            // A unit claimed but not put in the ring (after a timeout) is settled here: listed for
+            // the cluster kernel if it is one of its rows, reported TIMEOUT otherwise.
+            auto settle = [&](int64_t qq) {
+                const Unit uu = unit_of(a, qq);
+                const RowParams pp = load_params(a, uu.row);
+                if (a.route == kRouteStream && routed_to_cluster(pp.T, pp.P, pp.MP)) {
+                    if (uu.seg == 0) list_for_cluster(uu.row);
+                } else {
+                    fail_unit(a, sv, qq);
                 }
+            };
+            if (!waited) {
+                wait_prerequisite();  // this grid completes after the one it waits for
+                waited = true;
             }
-            if (!waited) wait_prerequisite();  // this grid completes after the one it waits for
+            if (*vdead && q < Q) settle(q);
+            // A CTA whose wait gave up stops claiming and leaves the rest to the others.  The last CTA
+            // to stop claiming settles whatever nobody claimed -- units are left only when CTAs died.
+            if (atomicAdd(&sv.hdr->done, 1u) + 1u == gridDim.x) {
+                __threadfence();
+                for (int64_t qq = claim_counter(); qq < Q; qq = claim_counter()) settle(qq);
+            }
             st.issued_lo = (uint32_t)g;
             __threadfence_block();
             *(volatile uint32_t*)&st.producer_done = 1u;
@@ -928,6 +942,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
             const int32_t e0 = geo.nhead + (int32_t)(v0 * (16 / ES));
             if (c > 0 && !dead && !mbar_wait_bounded(&st.full[stage], parity, wait_ns)) dead = true;
             dead = __any_sync(0xFFFFFFFFu, dead);
+            if (dead && lane == 0) *vdead = 1u;  // the producer stops issuing at once
             if (!dead && nv > 0) {
                 float cm;
                 if (c == 0) {
@@ -944,7 +959,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
                 if (lane == 0 && !isnan(wrun)) atomicMax(&slot.runkey, fkey(wrun));
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&st.empty[stage]);
+            // a stage is released only once scanned: after a timeout its copy may never have landed
+            // (or may still land), so it must not be handed back for another copy
+            if (lane == 0 && !dead) mbar_arrive(&st.empty[stage]);
         }
         // hand the unit over: ragged elements (listed), this warp's maximum, arrive on the slot
         if (tid < nx) list_token(xv, xidx);
