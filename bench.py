@@ -62,6 +62,10 @@ def parse(argv=None):
     ap.add_argument("--penalties", type=int, default=0, metavar="H",
                     help="run the penalty kernel (histories of up to H tokens per row) ahead of the sampler "
                          "in every step")
+    ap.add_argument("--draw", default="race", choices=["race", "rejection", "spec"],
+                    help="time the exponential-race sampler (default), the sort-free rejection draw, or speculative "
+                         "acceptance of one draft token per row (draft = the step's logits plus noise)")
+    ap.add_argument("--no-sustained", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="time the sweep grid (B x V x dtype, sweep workload) and print one JSON table instead")
     return ap.parse_args(argv)
@@ -189,38 +193,57 @@ def make_workload(args, device, seed=0):
     return workloads.make(args.workload, device=device, seed=seed)
 
 
-def cpu_baseline(w_cpu, rows_target_s=10.0, max_rows=512):
-    """Time the float64 oracle on the host cores over a bounded sample of rows; rows/s."""
+def cpu_baseline(w, gpu=None, rows_target_s=10.0, max_rows=512):
+    """Time the float64 oracle on the host cores over a bounded sample of the workload's rows (the
+    device workload's first rows, copied to the host); rows/s.  With `gpu` (one GPU call's
+    diagnostics on the same rows, same step), the same oracle outputs also check the GPU: tokens,
+    kept counts, cutoffs and statuses outside the boundary band must match exactly, and the boundary
+    rows are counted by kind."""
     import oracle
     o = oracle.default()
     cores = o.max_threads()
-    B = w_cpu.B
+    B = w.B
     n = 1
     spent = 0.0
     done = 0
+    outs = []
     # grow the sample until ~rows_target_s of CPU work or max_rows
     while done < max_rows and spent < rows_target_s:
         rows = np.arange(done, min(done + n, B))
         if len(rows) == 0:
             break
+        z = w.logits[rows[0]:rows[-1] + 1].double().cpu().numpy()
+        sel = lambda t: t[rows[0]:rows[-1] + 1].cpu().numpy()
         t0 = time.perf_counter()
-        o.sample(w_cpu.logits[rows].double().numpy(), w_cpu.temperature[rows].numpy(), w_cpu.top_k[rows].numpy(),
-                 w_cpu.top_p[rows].numpy(), w_cpu.min_p[rows].numpy(),
-                 w_cpu.seed[rows].numpy().astype(np.uint64), w_cpu.step, row_ids=rows)
+        outs.append(o.sample(z, sel(w.temperature), sel(w.top_k), sel(w.top_p), sel(w.min_p),
+                             sel(w.seed).astype(np.uint64), w.step, row_ids=rows))
         spent += time.perf_counter() - t0
         done += len(rows)
         n = min(2 * n, max_rows)
     # one core, on the first rows of the same workload
     n1 = min(16, B)
-    rows = np.arange(n1)
+    z = w.logits[:n1].double().cpu().numpy()
     t0 = time.perf_counter()
-    o.sample(w_cpu.logits[rows].double().numpy(), w_cpu.temperature[rows].numpy(), w_cpu.top_k[rows].numpy(),
-             w_cpu.top_p[rows].numpy(), w_cpu.min_p[rows].numpy(), w_cpu.seed[rows].numpy().astype(np.uint64),
-             w_cpu.step, row_ids=rows, nthreads=1)
+    o.sample(z, w.temperature[:n1].cpu().numpy(), w.top_k[:n1].cpu().numpy(), w.top_p[:n1].cpu().numpy(),
+             w.min_p[:n1].cpu().numpy(), w.seed[:n1].cpu().numpy().astype(np.uint64), w.step, row_ids=np.arange(n1),
+             nthreads=1)
     one_core = n1 / (time.perf_counter() - t0)
-    return {"value": done / spent, "unit": "rows/s", "cores": cores, "kind": "oracle",
-            "sample": f"{done} of {B} rows of the same workload, float64 oracle, OpenMP over rows ({spent:.1f} s)",
-            "one_core_rows_per_s": round(one_core, 1), "cpu": cpu_model()}
+    res = {"value": done / spent, "unit": "rows/s", "cores": cores, "kind": "oracle",
+           "sample": f"{done} of {B} rows of the same workload, float64 oracle, OpenMP over rows ({spent:.1f} s)",
+           "one_core_rows_per_s": round(one_core, 1), "cpu": cpu_model()}
+    if gpu is not None and outs:
+        cat = lambda k: np.concatenate([x[k] for x in outs])
+        ot, ok_, oc, os_, of = cat("token"), cat("kept"), cat("cutoff"), cat("status"), cat("flags")
+        g = {k: v[:done].cpu().numpy() for k, v in gpu.items()}
+        band = (of & 3) != 0
+        race = (of & 4) != 0
+        chk = (os_ == 0) & ~band
+        mism = int((chk & ~race & (g["token"] != ot)).sum() + (chk & (g["kept"] != ok_)).sum() +
+                   (chk & (g["cutoff"].astype(np.float64) != oc)).sum() + (g["status"] != os_).sum())
+        res["parity"] = {"rows_checked": int(done), "mismatches_outside_band": mism,
+                         "topp_band_rows": int(((of & 1) != 0).sum()), "minp_band_rows": int(((of & 2) != 0).sum()),
+                         "race_margin_rows": int(race.sum())}
+    return res
 
 
 def cpu_model() -> str:
@@ -410,11 +433,26 @@ def main():
         tps.apply_penalties(w.logits, pen.history, pen.hist_len, repetition=pen.repetition,
                             frequency=pen.frequency, presence=pen.presence)
 
+    spec = None
+    if args.draw == "spec":
+        # draft rows: the target's logits plus N(0, 0.5^2) noise, sampled by the draft's own parameters
+        g = torch.Generator(device=dev).manual_seed(1234 + rank)
+        zd = (w.logits.float() + 0.5 * torch.randn(w.logits.shape, generator=g, device=dev)).to(w.logits.dtype)
+        dp = (torch.full_like(w.temperature, 0.9), torch.zeros_like(w.top_k), torch.full_like(w.top_p, 0.95),
+              torch.full_like(w.min_p, 0.02))
+        x = tps.sample(zd, *dp, w.seed + 7, 0)
+        spec = (zd, dp, x)
+
     def step(i):
         if pen is not None:
             penalise()  # in place, as an engine does on each step's fresh logits
-        tps.sample(w.logits, w.temperature, w.top_k, w.top_p, w.min_p, w.seed, i, out=out, kernel=args.kernel,
-                   **lp_kw)
+        if args.draw == "rejection":
+            tps.sample_rejection(w.logits, w.temperature, w.top_k, w.top_p, w.min_p, w.seed, i)
+        elif args.draw == "spec":
+            tps.spec_accept(w.logits, spec[0], (w.temperature, w.top_k, w.top_p, w.min_p), spec[1], spec[2], w.seed, i)
+        else:
+            tps.sample(w.logits, w.temperature, w.top_k, w.top_p, w.min_p, w.seed, i, out=out, kernel=args.kernel,
+                       **lp_kw)
 
     for i in range(args.warmup):
         step(i)
@@ -444,8 +482,11 @@ def main():
     ms_per_step = total_ms / args.steps
     value = job_rows_per_s(B, world, args.steps, total_ms)
 
-    # roofline for the one kernel of the step (each step is exactly one launch)
-    alg_bytes = B * (V * es + ROW_PARAM_BYTES)
+    # roofline of the step: the algorithmic bytes over the step's device time.  A step is one call,
+    # which launches the scratch clear and the streaming kernel (and the cluster kernel behind it for
+    # a split batch); the step time covers all of them, so this is a lower bound on the streaming
+    # kernel's own throughput (its share of the step is in the committed ncu launch list).
+    alg_bytes = B * ((2 if args.draw == "spec" else 1) * V * es + ROW_PARAM_BYTES)
     kern_ms = statistics.mean(per)
     achieved = alg_bytes / (kern_ms / 1e3) / 1e9
     peak, peak_kind = measured_peaks()
@@ -461,7 +502,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32" if args.dtype == "f32" else "bf16", "data": "synthetic",
             "config": workload_config(args), "roofline": roof,
-            "gpu_launches": args.steps * (tps.kernels_per_call(w.logits.dtype, B, V, args.kernel) + (pen is not None)),
+            "gpu_launches": args.steps * (launches_per_step(args, tps, w) + (pen is not None)),
             "hbm_gbs": round(achieved, 1), "us_per_step": round(1e3 * ms_per_step, 2),
             "wall_s_timed": round(t_wall, 3), "cluster_size": tps.cluster_size(w.logits.dtype, B, V)}
     if clk:
@@ -469,18 +510,68 @@ def main():
     if pen is not None:
         line["penalties"] = penalty_kernel_stats(pen, penalise, stream, B, V, es)
 
+    if args.draw != "race":
+        line["config"]["draw"] = args.draw
+    if rank == 0 and world == 1 and not args.no_sustained:
+        line["sustained"] = sustained(args, step, stream, B, local)
     if rank == 0 and not args.no_latency:
         line["latency_b1"] = latency_b1(args, dev)
     if not args.no_e2e:
         line["e2e"] = e2e(args, w, dev, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        wc = make_workload(args, "cpu", seed=rank)
-        line["cpu_baseline"] = cpu_baseline(wc)
+        gpu = None
+        if args.draw == "race" and pen is None:  # the sampler's own answer on the same rows, same step
+            gpu = tps.sample(w.logits, w.temperature, w.top_k, w.top_p, w.min_p, w.seed, w.step, diagnostics=True,
+                             kernel=args.kernel)
+            torch.cuda.synchronize()
+        line["cpu_baseline"] = cpu_baseline(w, gpu)
+        if "parity" in line["cpu_baseline"]:
+            line["parity"] = line["cpu_baseline"]["parity"]
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def launches_per_step(args, tps, w):
+    """Kernels one step launches (the library's own count for the sampler call)."""
+    if args.draw in ("rejection", "spec"):
+        return 1
+    return tps.kernels_per_call(w.logits.dtype, w.B, w.V, args.kernel)
+
+
+def sustained(args, step, stream, B, local, seconds=1.2):
+    """At least a second of back-to-back steps (after the main timed region), timed with CUDA events
+    on the launching stream, with the SM clock sampled by nvidia-smi during it; the samples are also
+    binned by clock so a throttled stretch would show."""
+    n = 50
+    for i in range(n):
+        step(10_000 + i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n):
+        step(10_000 + i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    per = e0.elapsed_time(e1) / n
+    steps = max(50, int(seconds * 1e3 / per))
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    e0.record(stream)
+    for i in range(steps):
+        step(20_000 + i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    out = {"steps": steps, "seconds": round(ms / 1e3, 3), "ms_per_step": round(ms / steps, 5),
+           "value": B * steps / (ms / 1e3), "unit": UNIT}
+    if clk:
+        out["clocks"] = clk
+    return out
 
 
 def latency_b1(args, dev, calls=300):

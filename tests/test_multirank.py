@@ -39,7 +39,7 @@ def _rank(rank, world, port, out):
 
 def test_two_gloo_ranks_shard_rows_and_take_the_slowest_time():
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_rank, args=(2, port, out), nprocs=2, join=True)
         res = dict(out)
