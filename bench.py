@@ -193,33 +193,40 @@ def make_workload(args, device, seed=0):
     return workloads.make(args.workload, device=device, seed=seed)
 
 
-def cpu_baseline(w, gpu=None, rows_target_s=10.0, max_rows=512):
-    """Time the float64 oracle on the host cores over a bounded sample of the workload's rows (the
-    device workload's first rows, copied to the host); rows/s.  With `gpu` (one GPU call's
-    diagnostics on the same rows, same step), the same oracle outputs also check the GPU: tokens,
-    kept counts, cutoffs and statuses outside the boundary band must match exactly, and the boundary
-    rows are counted by kind."""
+def cpu_baseline(w, gpu=None, seconds=10.0, max_passes=16, chunk=128):
+    """Time the float64 oracle on the host cores over a bounded sample of the workload: passes over
+    the device workload's rows (copied to the host), pass q at step counter step + q, in chunks of
+    `chunk` rows, until about `seconds` of oracle time or `max_passes` passes; rows/s.  With `gpu`
+    (one GPU call's diagnostics on the same rows at the same step), the first pass's oracle outputs
+    also check the GPU: tokens, kept counts, cutoffs and statuses outside the boundary band must
+    match exactly, and the boundary rows are counted by kind."""
     import oracle
     o = oracle.default()
     cores = o.max_threads()
     B = w.B
-    n = 1
     spent = 0.0
     done = 0
     outs = []
-    # grow the sample until ~rows_target_s of CPU work or max_rows
-    while done < max_rows and spent < rows_target_s:
-        rows = np.arange(done, min(done + n, B))
-        if len(rows) == 0:
+    chunks = []
+    for q in range(max_passes):
+        for c, r0 in enumerate(range(0, B, chunk)):
+            r1 = min(B, r0 + chunk)
+            if q == 0:  # host copies of the chunk, made once and outside the timed calls
+                sel = lambda t: t[r0:r1].cpu().numpy()
+                chunks.append((w.logits[r0:r1].double().cpu().numpy(), sel(w.temperature), sel(w.top_k),
+                               sel(w.top_p), sel(w.min_p), sel(w.seed).astype(np.uint64)))
+            z, T, k, p, m, sd = chunks[c]
+            t0 = time.perf_counter()
+            res = o.sample(z, T, k, p, m, sd, w.step + q, row_ids=np.arange(r0, r1))
+            spent += time.perf_counter() - t0
+            done += r1 - r0
+            if q == 0:
+                outs.append(res)
+            if spent >= seconds and q > 0:
+                break
+        if spent >= seconds:
             break
-        z = w.logits[rows[0]:rows[-1] + 1].double().cpu().numpy()
-        sel = lambda t: t[rows[0]:rows[-1] + 1].cpu().numpy()
-        t0 = time.perf_counter()
-        outs.append(o.sample(z, sel(w.temperature), sel(w.top_k), sel(w.top_p), sel(w.min_p),
-                             sel(w.seed).astype(np.uint64), w.step, row_ids=rows))
-        spent += time.perf_counter() - t0
-        done += len(rows)
-        n = min(2 * n, max_rows)
+    passes = q + 1
     # one core, on the first rows of the same workload
     n1 = min(16, B)
     z = w.logits[:n1].double().cpu().numpy()
@@ -229,18 +236,19 @@ def cpu_baseline(w, gpu=None, rows_target_s=10.0, max_rows=512):
              nthreads=1)
     one_core = n1 / (time.perf_counter() - t0)
     res = {"value": done / spent, "unit": "rows/s", "cores": cores, "kind": "oracle",
-           "sample": f"{done} of {B} rows of the same workload, float64 oracle, OpenMP over rows ({spent:.1f} s)",
+           "sample": f"{done} rows: {passes} pass(es) over the {B} rows of the same workload at successive step "
+                     f"counters, float64 oracle, OpenMP over rows ({spent:.1f} s)",
            "one_core_rows_per_s": round(one_core, 1), "cpu": cpu_model()}
     if gpu is not None and outs:
         cat = lambda k: np.concatenate([x[k] for x in outs])
         ot, ok_, oc, os_, of = cat("token"), cat("kept"), cat("cutoff"), cat("status"), cat("flags")
-        g = {k: v[:done].cpu().numpy() for k, v in gpu.items()}
+        g = {k: v.cpu().numpy() for k, v in gpu.items()}
         band = (of & 3) != 0
         race = (of & 4) != 0
         chk = (os_ == 0) & ~band
         mism = int((chk & ~race & (g["token"] != ot)).sum() + (chk & (g["kept"] != ok_)).sum() +
                    (chk & (g["cutoff"].astype(np.float64) != oc)).sum() + (g["status"] != os_).sum())
-        res["parity"] = {"rows_checked": int(done), "mismatches_outside_band": mism,
+        res["parity"] = {"rows_checked": int(len(ot)), "mismatches_outside_band": mism,
                          "topp_band_rows": int(((of & 1) != 0).sum()), "minp_band_rows": int(((of & 2) != 0).sum()),
                          "race_margin_rows": int(race.sum())}
     return res
@@ -273,11 +281,11 @@ def run_reference(args):
     o = oracle.default()
     w = make_workload(args, "cpu")
     # each step: a bounded sample of rows (sized so the whole run stays within a few minutes)
-    per_step = max(1, min(args.B, 16))
+    per_step = max(1, min(w.B, 16))
     times = []
     total_steps = args.warmup + args.steps
     for it in range(total_steps):
-        rows = (np.arange(per_step) + it * per_step) % args.B
+        rows = (np.arange(per_step) + it * per_step) % w.B
         t0 = time.perf_counter()
         o.sample(w.logits[rows].double().numpy(), w.temperature[rows].numpy(), w.top_k[rows].numpy(),
                  w.top_p[rows].numpy(), w.min_p[rows].numpy(), w.seed[rows].numpy().astype(np.uint64), it,
@@ -290,9 +298,9 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(args),
+        "config": workload_config(args, w),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": o.max_threads(), "kind": "oracle",
-                         "sample": f"{per_step} rows per step of the {args.B}-row workload, float64 oracle"},
+                         "sample": f"{per_step} rows per step of the {w.B}-row workload, float64 oracle"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -336,12 +344,26 @@ def penalty_kernel_stats(pen, penalise, stream, B, V, es, calls=50):
                     "history and the touched lines fit L2)"}
 
 
-def workload_config(args):
-    return {"workload": f"{args.workload}_b{args.B}_v{args.V}_{args.dtype}", "B": args.B, "V": args.V,
-            "logits_dtype": args.dtype, "params": "T=0.7 top_k=50 top_p=0.9 min_p=0.05" if args.workload == "decode"
+L2_BYTES = 129e6  # GB300's L2
+
+
+def in_bytes(w) -> int:
+    return w.logits.numel() * w.logits.element_size()
+
+
+def workload_config(args, w):
+    """The workload as it was built (a named workload other than decode and sweep has its own B, V
+    and dtype)."""
+    dt = "f32" if w.logits.dtype == torch.float32 else "bf16"
+    mb = in_bytes(w) / 1e6
+    return {"workload": f"{args.workload}_b{w.B}_v{w.V}_{dt}", "B": w.B, "V": w.V,
+            "logits_dtype": dt, "params": "T=0.7 top_k=50 top_p=0.9 min_p=0.05" if args.workload == "decode"
             else args.workload, "parallelism": "rows sharded over ranks (replicas, no collective)",
-            "l2": "inputs larger than L2 (no flush): %.0f MB of logits per step per GPU" % (
-                args.B * args.V * (4 if args.dtype == "f32" else 2) / 1e6),
+            "l2": ("inputs larger than L2 (no flush): %.0f MB of logits per step per GPU" % mb if in_bytes(w) > 2 * L2_BYTES
+                   else "inputs within 2x L2 (%.0f MB of logits per step per GPU): a 512 MB buffer is written "
+                        "between timed steps and each step is timed alone" % mb),
+            "timing": "CUDA events on the launching stream around each step; the K steps are enqueued behind "
+                      "a GPU spin so host launch gaps are not timed",
             **({"penalties": f"repetition/frequency/presence, histories of up to {args.penalties} tokens"}
                if args.penalties else {}),
             **({"logprobs": f"sampled token's processed log-probability and the top {args.logprobs}"}
@@ -413,7 +435,7 @@ def main():
 
     w = make_workload(args, dev, seed=rank)
     B, V = w.B, w.V
-    es = 4 if args.dtype == "f32" else 2
+    es = w.logits.element_size()
     stream = torch.cuda.current_stream(dev)
     tok = torch.empty(B, dtype=torch.int32, device=dev)
     out = {"token": tok}
@@ -462,22 +484,48 @@ def main():
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    if clocks:
+    if clocks:  # the sampler starts while the GPU runs untimed steps, so its samples are under load
         clocks.start()
-        time.sleep(0.5)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    t_wall0 = time.perf_counter()
-    ev[0].record(stream)
-    for i in range(args.steps):
-        step(args.warmup + i)
-        ev[i + 1].record(stream)
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall0
+        t0 = time.perf_counter()
+        i = 0
+        while time.perf_counter() - t0 < 0.5:
+            step(50_000 + i)
+            i += 1
+            if i % 64 == 0:
+                torch.cuda.synchronize()
+    # The timed steps are enqueued behind a short GPU spin, so the first event is recorded after the
+    # host has queued them: the region measures the device's time for the K steps, not the host's
+    # launch cadence (the e2e key times the host path).
+    torch.cuda._sleep(int(min(200e6, 2e6 * args.steps)))
+    flush = in_bytes(w) <= 2 * L2_BYTES
+    if not flush:  # back to back: each step reads inputs larger than L2
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        t_wall0 = time.perf_counter()
+        ev[0].record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i)
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+        per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+        total_ms = ev[0].elapsed_time(ev[-1])
+    else:  # a write of 512 MB between steps pushes the inputs out of L2; each step is timed alone
+        scrub = torch.empty(128 << 20, dtype=torch.float32, device=dev)
+        ea = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        eb = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            scrub.fill_(float(i))
+            ea[i].record(stream)
+            step(args.warmup + i)
+            eb[i].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+        per = [ea[i].elapsed_time(eb[i]) for i in range(args.steps)]
+        total_ms = sum(per)
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop() if clocks else None
-    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-    total_ms = ev[0].elapsed_time(ev[-1])
     total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
     value = job_rows_per_s(B, world, args.steps, total_ms)
@@ -490,18 +538,20 @@ def main():
     kern_ms = statistics.mean(per)
     achieved = alg_bytes / (kern_ms / 1e3) / 1e9
     peak, peak_kind = measured_peaks()
-    tag = f"{args.workload}_b{B}_v{V}_{args.dtype}" + (f"_pen{args.penalties}" if pen is not None else "") + (
+    dt_name = "f32" if w.logits.dtype == torch.float32 else "bf16"
+    tag = f"{args.workload}_b{B}_v{V}_{dt_name}" + (f"_pen{args.penalties}" if pen is not None else "") + (
         f"_lp{args.logprobs}" if args.logprobs >= 0 else "")
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
             "frac_of_8000": round(achieved / 8000.0, 4), "traffic": committed_traffic(tag),
             "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms_mean": round(kern_ms, 5),
-            "kernel_ms_p50": round(statistics.median(per), 5)}
+            "kernel_ms_p50": round(statistics.median(per), 5), "kernel_ms_min": round(min(per), 5),
+            "kernel_ms_max": round(max(per), 5)}
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32" if args.dtype == "f32" else "bf16", "data": "synthetic",
-            "config": workload_config(args), "roofline": roof,
+            "vs_baseline": None, "dtype": dt_name, "data": "synthetic",
+            "config": workload_config(args, w), "roofline": roof,
             "gpu_launches": args.steps * (launches_per_step(args, tps, w) + (pen is not None)),
             "hbm_gbs": round(achieved, 1), "us_per_step": round(1e3 * ms_per_step, 2),
             "wall_s_timed": round(t_wall, 3), "cluster_size": tps.cluster_size(w.logits.dtype, B, V)}

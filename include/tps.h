@@ -26,10 +26,16 @@
  *     (low word first) and counter = (i / 4, b, step low word, step high word).
  *
  * Calling convention (all entry points):
- *   - every pointer argument is a DEVICE pointer owned by the caller, except where marked; the
- *     library allocates no memory per call, never synchronises the host, keeps no state between
- *     calls beyond a per-device cache of queried limits, and may be called from several host
- *     threads at once;
+ *   - every pointer argument is a DEVICE pointer owned by the caller, except where marked;
+ *   - a sampling call that runs the streaming kernel (tps_sample, tps_sample_ex, tps_sample_kernel
+ *     and tps_sample_full, see tps_kernel) draws a small scratch buffer (claim counters, a row
+ *     list and, for a batch of fewer than four rows per SM, the partial results of its split rows:
+ *     a few KB for 1,024 rows of 128,256 logits, at most about 2.5 MB for a split batch) from a
+ *     stream-ordered memory pool the library creates once per device, and returns it on the call's
+ *     stream; the pool keeps up to 64 MiB reserved between calls.  tps_sample_noalloc uses a fixed
+ *     array instead; no other call allocates device memory;
+ *   - the library never synchronises the host, keeps no state between calls beyond that pool and
+ *     a per-device cache of queried limits, and may be called from several host threads at once;
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream); all work is enqueued on it;
  *   - the return value is a tps_status; errors in the arguments are reported before anything is
  *     enqueued; problems in a row's data are reported per row in out_status and never abort the
@@ -105,10 +111,11 @@ int tps_sample_ex(const void* logits, int dtype, int64_t B, int64_t V, int64_t l
 /*
  * Which kernel samples the rows (tps_sample_kernel).
  *   AUTO    the library's choice (what tps_sample uses): below 32 rows the cluster kernel; from 32
- *           rows the batch is split -- the cluster kernel takes the rows that sample without min-p
- *           (they need several passes over the row, which it makes on-chip), and the streaming
- *           kernel, launched right behind it, takes every other row.  The split costs a few
- *           microseconds when no row needs the cluster kernel.
+ *           rows the batch is split -- the streaming kernel samples the rows with min-p (and greedy
+ *           and failed rows) and lists the others in its scratch, and the cluster kernel, launched
+ *           right behind it, samples the listed rows (rows without min-p take the general path,
+ *           which makes several passes over the row, and the cluster kernel makes them on-chip).
+ *           When no row is listed the cluster kernel finds an empty list and exits.
  *   CLUSTER every row by the cluster kernel (one cluster of up to 16 CTAs per row).
  *   STREAM  every row by the streaming kernel (one CTA per SM, rows streamed through a ring); the
  *           fastest choice for a batch whose rows all use min-p or are greedy, e.g. decode batches
@@ -137,7 +144,9 @@ int tps_sample_kernel(const void* logits, int dtype, int64_t B, int64_t V, int64
 /*
  * tps_sample_full -- tps_sample_kernel plus processed log-probabilities: those of the sampled
  * token and of the row's most probable kept tokens ("processed": under the renormalised kept
- * distribution that out_probs holds, not the raw softmax).
+ * distribution that out_probs holds, not the raw softmax; "Top-p (Nucleus) Sampling, in depth",
+ * 'Logprobs, speculative decoding and reproducibility': under the processed distribution every
+ * token outside the nucleus has probability zero, and callers must know which of the two they get).
  *
  *   out_logprob      [B] float, or NULL: ln P(token) = -(zmax - z_token)/T - ln(sum over kept i of
  *                    e^{-(zmax - z_i)/T}); 0 for greedy rows, NaN for failed rows.
@@ -255,12 +264,13 @@ int tps_spec_accept(const void* target_logits, const void* draft_logits, int dty
  * another framework, code that must stay out of the driver's allocator).  The pages define no such
  * call; it is this library's own.  Same arguments, rules and results as tps_sample_full; the only
  * difference is where the streaming kernel's small per-call scratch lives: tps_sample_full draws it
- * from the device's stream-ordered memory pool, this call uses a fixed array of 8 MiB compiled into
- * the library (held on every GPU that loads the library until the process exits) and allocates
- * nothing.
- *   - A call whose scratch would exceed 8 MiB returns TPS_ERR_SCRATCH before enqueuing anything (a
- *     decode batch of 1,024 rows x 128,256 float32 logits needs about 1.3 MiB; very large batches,
- *     or rows above about 1.6 million elements split over many segments, need more).
+ * from a stream-ordered memory pool the library keeps per device, this call uses a fixed array of
+ * 8 MiB compiled into the library (held on every GPU that loads the library until the process exits)
+ * and allocates nothing.
+ *   - A call whose scratch would exceed 8 MiB returns TPS_ERR_SCRATCH before enqueuing anything.
+ *     The scratch holds 4 bytes per row plus, for a batch of fewer than four rows per SM, about
+ *     2 KB per segment of its split rows (at most about 2.5 MB): only batches of about two million
+ *     rows or more exceed it.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress): make
  *     that first call before any stream capture.
  *   - Every call shares the one array and clears the part that must start at zero itself, on its
@@ -287,8 +297,9 @@ int tps_sample_stall_test(const void* logits, int dtype, int64_t B, int64_t V, c
                           uint64_t step, int32_t* out_token, int32_t* out_status, int64_t stall_chunk,
                           uint64_t wait_ns, void* stream);
 
-/* Kernels one tps_sample_kernel call with these arguments launches (1 or 2; 0 for arguments the call
- * would reject).  Host-only query. */
+/* Kernels one tps_sample_kernel call with these arguments launches (0 for arguments the call would
+ * reject): 1 for the cluster kernel alone; 2 for the streaming kernel (a one-CTA kernel clears its
+ * scratch first); 3 for a split batch (those two, then the cluster kernel).  Host-only query. */
 int tps_kernels_per_call(int dtype, int64_t B, int64_t V, int kernel);
 
 /* Largest V the library accepts for `dtype` on the current device (0 for an unknown dtype or

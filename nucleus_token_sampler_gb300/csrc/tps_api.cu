@@ -6,8 +6,9 @@
 // the cluster's shared memory) spreads each row over up to 16 SMs; it samples small batches.  The
 // streaming kernel (one persistent CTA per SM, rows streamed through a ring of bulk-copied chunks)
 // reads each row once at HBM speed and resolves rows with min-p (and greedy rows) on the fly; its
-// CTAs claim work dynamically through a small global scratch, which the call draws from the
-// device's stream-ordered memory pool and which a one-CTA kernel clears just before.  A large batch
+// CTAs claim work dynamically through a small global scratch, which the call draws from a
+// stream-ordered memory pool the library keeps per device and which a one-CTA kernel clears just
+// before.  A large batch
 // is split: the streaming kernel lists the rows without min-p (whose general path makes several
 // passes over the row) in the scratch, and the cluster kernel, launched behind it, samples them.
 #include <cuda_runtime.h>
@@ -50,7 +51,8 @@ constexpr int kMaxCluster = 16;
 constexpr int kStreamStages = 3;
 constexpr uint32_t kStreamChunk = 64u * 1024u;
 constexpr int64_t kStreamMinRows = 32;  // batches at least this large use the streaming kernel
-constexpr int64_t kSegBytes = 256 * 1024;  // target size of a segment of a split row
+constexpr int64_t kMinSegBytes = 128 * 1024;  // smallest segment of a split row
+constexpr int kClaimsPerSm = 4;                // claims per SM below which rows are split
 
 // Per-device limits, filled once under g_mu and published through `ready` (release/acquire), so a
 // thread that sees ready == true also sees sms and smem_optin.  The attribute flags only record that
@@ -70,6 +72,47 @@ struct DeviceInfo {
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
+
+// The library's own stream-ordered memory pool per device, for the streaming kernel's per-call
+// scratch.  The device's default pool gives all unused memory back at every synchronisation, so the
+// first call after a cudaStreamSynchronize would map fresh memory on the host's critical path; this
+// pool keeps up to kPoolKeepBytes reserved instead (a call's scratch is a few KB for a batch of whole
+// rows and at most about 2.5 MB for a split batch).  Created once per device, with that device current, and kept until the
+// process exits.
+constexpr uint64_t kPoolKeepBytes = 64ull << 20;
+std::atomic<cudaMemPool_t> g_pool[kMaxDevices];
+std::mutex g_pool_mu;
+
+cudaError_t scratch_pool(cudaMemPool_t* out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    cudaMemPool_t p = g_pool[dev].load(std::memory_order_acquire);
+    if (!p) {
+        std::lock_guard<std::mutex> lk(g_pool_mu);
+        p = g_pool[dev].load(std::memory_order_relaxed);
+        if (!p) {
+            cudaMemPoolProps props = {};
+            props.allocType = cudaMemAllocationTypePinned;
+            props.handleTypes = cudaMemHandleTypeNone;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            e = cudaMemPoolCreate(&p, &props);
+            if (e != cudaSuccess) return e;
+            uint64_t keep = kPoolKeepBytes;
+            e = cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep);
+            if (e != cudaSuccess) {
+                cudaMemPoolDestroy(p);
+                return e;
+            }
+            g_pool[dev].store(p, std::memory_order_release);
+        }
+    }
+    *out = p;
+    return cudaSuccess;
+}
 
 int elem_bytes(int dtype) { return dtype == TPS_F32 ? 4 : (dtype == TPS_BF16 ? 2 : 0); }
 
@@ -110,9 +153,12 @@ size_t smem_bytes(uint32_t slice_cap)
            (size_t)tps::kThreads * sizeof(int32_t) + sizeof(tps::Inbox);
 }
 
-// The streaming kernel's work for B rows: rows [0, b_whole) are claimed whole; the last nsplit rows
-// (two per SM, so the last claims of the call are short) are claimed as nseg segments of about
-// kSegBytes each; rows of at most kSegBytes are never split.
+// The streaming kernel's work for B rows: rows [0, b_whole) are claimed whole, the last nsplit rows
+// as nseg segments each.  A batch of at least kClaimsPerSm rows per SM is streamed in whole rows:
+// claims are dynamic, so the SMs finish within about one row of each other, and a split row costs a
+// merge of its segments' partial results through the scratch at the end of the row.  A smaller batch
+// would leave SMs idle, so every row is split into enough segments (of at least kMinSegBytes, at most
+// tps::kMaxSegments) to give about kClaimsPerSm claims per SM.
 struct StreamPlan {
     int64_t b_whole, nsplit;
     int nseg;
@@ -124,9 +170,12 @@ StreamPlan stream_plan(const DeviceInfo& d, int64_t B, int64_t V, int es)
 {
     StreamPlan p;
     const int64_t row_bytes = V * es;
-    int64_t nseg = (row_bytes + kSegBytes - 1) / kSegBytes;
-    p.nseg = (int)std::max<int64_t>(1, std::min<int64_t>(nseg, tps::kMaxSegments));
-    p.nsplit = p.nseg > 1 ? std::min<int64_t>(B, 2 * (int64_t)d.sms) : 0;
+    const int64_t want = kClaimsPerSm * (int64_t)d.sms;
+    int64_t nseg = 1;
+    if (B < want)
+        nseg = std::min<int64_t>(std::min<int64_t>((want + B - 1) / B, row_bytes / kMinSegBytes), tps::kMaxSegments);
+    p.nseg = (int)std::max<int64_t>(1, nseg);
+    p.nsplit = p.nseg > 1 ? B : 0;
     p.b_whole = B - p.nsplit;
     p.claims = p.b_whole + p.nsplit * p.nseg;
     p.grid = (int)std::min<int64_t>(d.sms, p.claims);
@@ -321,7 +370,7 @@ struct Call {
     int64_t stall_chunk = -1;
 };
 
-// Where a streaming call's scratch comes from: the device's stream-ordered pool, or a fixed array
+// Where a streaming call's scratch comes from: the library's stream-ordered pool, or a fixed array
 // (`fixed`, `fixed_bytes`) the call uses as it is.
 enum class ScratchSource { kPool, kFixed };
 
@@ -416,7 +465,9 @@ int sample_call(const Call& c, ScratchSource src, void* fixed = nullptr, size_t 
     const StreamPlan pl = stream_plan(*d, B, V, es);
     void* scratch = nullptr;
     if (src == ScratchSource::kPool) {
-        e = cudaMallocAsync(&scratch, (size_t)pl.layout.total, st);
+        cudaMemPool_t pool = nullptr;
+        e = scratch_pool(&pool);
+        if (e == cudaSuccess) e = cudaMallocFromPoolAsync(&scratch, (size_t)pl.layout.total, pool, st);
         if (e != cudaSuccess) return fail_cuda(e);
     } else {
         if (pl.layout.total > (uint64_t)fixed_bytes) return TPS_ERR_SCRATCH;
@@ -768,8 +819,8 @@ extern "C" {
 // all device memory up front and must not meet an allocation failure mid-request, a host whose
 // allocator is owned by another framework (allocating behind its back would break its accounting),
 // or code that must not enter the driver's allocator for latency reasons.  The ordinary calls draw
-// the streaming kernel's small per-call scratch from the device's stream-ordered pool
-// (cudaMallocAsync); this call uses a fixed array compiled into the library instead.  The array is
+// the streaming kernel's small per-call scratch from the library's stream-ordered pool
+// (cudaMallocFromPoolAsync); this call uses a fixed array compiled into the library instead.  The array is
 // kNoAllocScratchBytes of device memory on every GPU that loads the library, held until the process
 // exits.  Its device address is looked up once per device (cudaGetSymbolAddress, with that device
 // current) by the first call on that device, so that first call should come before any stream

@@ -433,17 +433,55 @@ struct ElemOf<VecSource<TIn, kG>> {
 template <typename TIn>
 using GlobalRow = VecSource<TIn, true>;
 
+// NaN-propagating maximum of N floats by a tree of three-input maxima (one instruction each on
+// sm_100 and later).
+template <int N>
+__device__ __forceinline__ float max_tree_nan(const float (&z)[N])
+{
+    if constexpr (N == 1) {
+        return z[0];
+    } else if constexpr (N == 2) {
+        return fmax_nan(z[0], z[1]);
+    } else {
+        constexpr int M = (N + 2) / 3;
+        float r[M];
+#pragma unroll
+        for (int i = 0; i < M; ++i) {
+            if (3 * i + 2 < N) r[i] = fmax3_nan(z[3 * i], z[3 * i + 1], z[3 * i + 2]);
+            else if (3 * i + 1 < N) r[i] = fmax_nan(z[3 * i], z[3 * i + 1]);
+            else r[i] = z[3 * i];
+        }
+        return max_tree_nan(r);
+    }
+}
+
+// The same over N words of two packed bfloat16 values each (packed maxima, no unpacking).
+template <int N>
+__device__ __forceinline__ uint32_t bmax_tree_nan(const uint32_t (&x)[N])
+{
+    if constexpr (N == 1) {
+        return x[0];
+    } else {
+        constexpr int M = (N + 1) / 2;
+        uint32_t r[M];
+#pragma unroll
+        for (int i = 0; i < M; ++i) r[i] = (2 * i + 1 < N) ? bmax2_nan(x[2 * i], x[2 * i + 1]) : x[2 * i];
+        return bmax_tree_nan(r);
+    }
+}
+
 // Maximum (NaN-propagating) over nvec 16-byte vectors, listing every element above thr through
-// list(z, i).  Each thread takes 16 elements per step and reduces them with a tree of max
+// list(z, i).  Each thread takes kVecs vectors per step and reduces them with a tree of max
 // operations -- three-input float maxima for float32, packed bfloat16x2 maxima for bfloat16 (no
 // unpacking) -- and only a step whose maximum exceeds thr is looked at element by element, so a pass
-// costs well under one instruction per element when little is listed.
-template <typename TIn, bool kGlobal, typename ListF>
+// costs well under one instruction per element when little is listed.  The default step is 16
+// elements; wider steps measured slower in the streaming kernel (more code in its hot loop).
+template <typename TIn, bool kGlobal, int kVecs = 16 / Elem<TIn>::kPerVec, typename ListF>
 __device__ __forceinline__ float scan_max_list(const uint4* vec, int nvec, int32_t elem0, float thr, ListF&& list)
 {
     using E = Elem<TIn>;
     constexpr int EPV = E::kPerVec;
-    constexpr int U = 16 / EPV;  // vectors per step
+    constexpr int U = kVecs;  // vectors per step
     const uint4 neg_inf = (EPV == 4) ? make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u)
                                      : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
     float cm = -INFINITY;
@@ -461,7 +499,7 @@ __device__ __forceinline__ float scan_max_list(const uint4* vec, int nvec, int32
         }
         float m;
         if constexpr (EPV == 4) {
-            float z[16];
+            float z[4 * U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 z[4 * u] = __uint_as_float(w[u].x);
@@ -469,12 +507,17 @@ __device__ __forceinline__ float scan_max_list(const uint4* vec, int nvec, int32
                 z[4 * u + 2] = __uint_as_float(w[u].z);
                 z[4 * u + 3] = __uint_as_float(w[u].w);
             }
-            const float n0 = fmax3_nan(fmax3_nan(z[0], z[1], z[2]), fmax3_nan(z[3], z[4], z[5]), fmax3_nan(z[6], z[7], z[8]));
-            const float n1 = fmax3_nan(fmax3_nan(z[9], z[10], z[11]), fmax3_nan(z[12], z[13], z[14]), z[15]);
-            m = fmax_nan(n0, n1);
+            m = max_tree_nan(z);
         } else {
-            const uint32_t c = bmax2_nan(bmax2_nan(bmax2_nan(w[0].x, w[0].y), bmax2_nan(w[0].z, w[0].w)),
-                                         bmax2_nan(bmax2_nan(w[1].x, w[1].y), bmax2_nan(w[1].z, w[1].w)));
+            uint32_t x[4 * U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                x[4 * u] = w[u].x;
+                x[4 * u + 1] = w[u].y;
+                x[4 * u + 2] = w[u].z;
+                x[4 * u + 3] = w[u].w;
+            }
+            const uint32_t c = bmax_tree_nan(x);
             m = fmax_nan(__uint_as_float(c << 16), __uint_as_float(c & 0xFFFF0000u));
         }
         cm = fmax_nan(cm, m);

@@ -1,11 +1,12 @@
 // tps_stream.cuh -- the streaming sampler: one persistent CTA per SM, rows streamed through a ring
 // of bulk-copied chunks.  Used when the batch has enough rows to fill the GPU.
 //
-// Work is claimed dynamically, so SMs that stream faster take more of it and all finish together:
-// the first rows of the batch are claimed whole, and each of the last rows (about two per SM) is
-// claimed as a few segments, so the last claims are short.  A CTA's first claim is its block index;
-// later claims come from a counter in the call's global scratch (cleared by a small kernel launched
-// just before this one, which this kernel waits for before it touches the scratch).
+// Work is claimed dynamically, so SMs that stream faster take more of it and all finish within about
+// one claim of each other.  A batch with several rows per SM is claimed in whole rows; a smaller one
+// has every row split into segments (the host chooses, see the plan in tps_api.cu).  A CTA's first
+// two claims are fixed (its block index, then that plus the grid size); later claims come from a
+// counter in the call's global scratch (cleared by a small kernel launched just before this one,
+// which this kernel waits for before it touches the scratch).
 //
 // Three kinds of warps, so that neither the HBM stream nor the scan ever waits for a row's
 // resolution:
@@ -16,8 +17,9 @@
 //   * eight scanner warps read the chunks and release each stage through its "empty" mbarrier.
 //     While a unit streams, each warp keeps its running maximum (pooled across warps through an
 //     atomic maximum) and lists every token that min-p, measured against that running maximum,
-//     does not already reject -- a superset of the survivors, since the maximum only grows.  At the
-//     end of the unit they hand the list and their maxima over in one of two slots and go on;
+//     does not already reject -- a superset of the survivors, since the maximum only grows.  The
+//     unit's first chunk is read twice: once for its maximum, then to list against it.  At the end
+//     of the unit they hand the list and their maxima over in one of three slots and go on;
 //   * two resolver warps take the finished slots, alternately.  A whole row is resolved on the spot: the exact
 //     maximum, the exact min-p filter of the list, the top-k and top-p cuts and the race.  A segment
 //     of a split row publishes its maximum and its exactly filtered list to the scratch and counts
@@ -671,8 +673,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
                     }
                 }
                 if (*vdead) return false;
+                // No proxy fence: the scanners' reads of this stage are ordered before the copy by
+                // their arrival on its empty barrier and the wait above, and the description written
+                // here reaches them through the full barrier's release (the arrival below).
                 st.info[stage] = info;
-                fence_proxy_async();
                 mbar_arrive_expect_tx(&st.full[stage], bytes);
                 // test hook: CTA 0 withholds the copy of chunk stall_chunk, so that stage never fills
                 // and the scanners' bounded wait on it runs out (no copy is left in flight)
@@ -943,11 +947,20 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_rows_kernel(const Ar
             if (c > 0 && !dead && !mbar_wait_bounded(&st.full[stage], parity, wait_ns)) dead = true;
             dead = __any_sync(0xFFFFFFFFu, dead);
             if (dead && lane == 0) *vdead = 1u;  // the producer stops issuing at once
+            if (c == 0) {
+                // first chunk: a pass for the maximum alone, published to the slot's running maximum,
+                // so the listing pass below tests against the whole chunk's maximum (a warp's own
+                // share would list several times more tokens, each through a shared counter).  Every
+                // scanner thread reaches the barrier, dead or not.
+                if (!dead && nv > 0) {
+                    wrun = warp_max_nan(scan_max_list<TIn, false>(cv, nv, e0, INFINITY, nolist));
+                    if (lane == 0 && !isnan(wrun)) atomicMax(&slot.runkey, fkey(wrun));
+                }
+                cta_sync();
+            }
             if (!dead && nv > 0) {
                 float cm;
                 if (c == 0) {
-                    // first chunk: this warp's own maximum over its part sets its first threshold
-                    wrun = warp_max_nan(scan_max_list<TIn, false>(cv, nv, e0, INFINITY, nolist));
                     const float mref = fmax_nan(wrun, key_to_float(*(volatile uint32_t*)&slot.runkey));
                     if (listing) (void)scan_max_list<TIn, false>(cv, nv, e0, thr_of(mref), list_token);
                     cm = wrun;
