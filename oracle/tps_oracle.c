@@ -432,7 +432,9 @@ int tpso_max_threads(void)
  *   accepted iff u * Q(x) < P(x), with u the acceptance uniform (an odd multiple of 2^-24 in (0, 1),
  *       so this holds with probability min(1, P(x)/Q(x)) up to the 2^-23 grid);
  *   otherwise the token is argmax over i with r_i = P_i - Q_i > 0 of ln r_i - ln(-ln u_i) (an
- *       exponential race over the residual; lowest index on equal keys).
+ *       exponential race over the residual; lowest index on equal keys).  With exact arithmetic a
+ *       rejection leaves some r_i > 0 (P and Q both sum to 1 and P(x) < Q(x)); if rounding leaves
+ *       none, P and Q agree, and since P = Q accepts every draft, x stands (accepted).
  * A row fails (token -1, not accepted) when the target or the draft row fails, or when x is not a
  * token the draft distribution can produce (outside [0, V), or Q(x) = 0): TPSO_ROW_BAD_PARAM.
  * Flags: the target's top-p / min-p band flags in bits 0-1, the draft's in bits 4-5; bit 3 when
@@ -507,6 +509,10 @@ int tpso_spec_accept(const double* zt, const double* zd, int64_t B, int64_t V, i
                             }
                         }
                         if (second > -INFINITY && best - second <= tol_best + tol_second + 1e-12) flags |= TPSO_FLAG_RACE_BAND;
+                        if (token < 0) {  /* no P_i above Q_i after rounding: P = Q, and x stands */
+                            token = x;
+                            accepted = 1;
+                        }
                     }
                 }
                 out_token[b] = token;
