@@ -29,15 +29,14 @@ import torch  # noqa: E402
 METRIC = "rows/s & HBM GB/s (% of peak) at B=1024 V=128256 fp32; p50 us at B=1"
 UNIT = "rows/s"
 ROW_PARAM_BYTES = 4 + 4 + 4 + 4 + 8 + 4  # T, top_k, top_p, min_p, seed, token out
+# The sources the streaming kernel (the dominant kernel of the decode step) and its launch plan are
+# built from: a committed ncu traffic figure applies only while their hash is unchanged.
 KERNEL_SOURCES = ["nucleus_token_sampler_gb300/csrc/tps_stream.cuh",
-                  "nucleus_token_sampler_gb300/csrc/tps_cluster.cuh",
                   "nucleus_token_sampler_gb300/csrc/tps_common.cuh",
                   "nucleus_token_sampler_gb300/csrc/tps_device.cuh",
                   "nucleus_token_sampler_gb300/csrc/tps_kernels.h",
                   "nucleus_token_sampler_gb300/csrc/tps_k_stream_f32.cu",
                   "nucleus_token_sampler_gb300/csrc/tps_k_stream_bf16.cu",
-                  "nucleus_token_sampler_gb300/csrc/tps_k_cluster_f32.cu",
-                  "nucleus_token_sampler_gb300/csrc/tps_k_cluster_bf16.cu",
                   "nucleus_token_sampler_gb300/csrc/tps_api.cu"]
 
 
@@ -351,6 +350,38 @@ def in_bytes(w) -> int:
     return w.logits.numel() * w.logits.element_size()
 
 
+def timed_steps(step, first, steps, stream, flush, dev):
+    """Time `steps` calls step(first), step(first + 1), ... with CUDA events on `stream`.  The steps
+    are enqueued behind a GPU spin, so the host's launch gaps are not timed.  flush=False: back to
+    back, one event between steps (inputs larger than L2); flush=True: a 512 MB buffer is written
+    between steps, each step timed alone.  Returns (per-step ms, total ms, host wall seconds)."""
+    torch.cuda._sleep(int(min(200e6, 2e6 * steps)))
+    if not flush:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        t0 = time.perf_counter()
+        ev[0].record(stream)
+        for i in range(steps):
+            step(first + i)
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+        return per, ev[0].elapsed_time(ev[-1]), wall
+    scrub = torch.empty(128 << 20, dtype=torch.float32, device=dev)
+    ea = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    eb = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t0 = time.perf_counter()
+    for i in range(steps):
+        scrub.fill_(float(i))
+        ea[i].record(stream)
+        step(first + i)
+        eb[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    per = [ea[i].elapsed_time(eb[i]) for i in range(steps)]
+    return per, sum(per), wall
+
+
 def workload_config(args, w):
     """The workload as it was built (a named workload other than decode and sweep has its own B, V
     and dtype)."""
@@ -372,9 +403,9 @@ def workload_config(args, w):
 
 def run_sweep(args):
     """The sweep grid: every B x V x dtype point of the sweep workload (top-p ~ U[.1, 1], T ~ U[.3, 2],
-    no top-k, no min-p), timed like the main run (warm-up, then CUDA events around args.steps calls)
-    through the chosen kernel; inputs larger than L2 are not flushed, smaller ones are re-read from
-    L2 (a point's `l2` field says which).  Prints one JSON object with a row per point."""
+    no top-k, no min-p), timed like the main run (warm-up, then timed_steps: back to back for inputs
+    larger than 2x L2, L2 scrubbed between steps otherwise) through the chosen kernel.  Prints one
+    JSON object with a row per point."""
     import nucleus_token_sampler_gb300 as tps
     from nucleus_token_sampler_gb300 import workloads
     dev = torch.device("cuda", 0)
@@ -395,20 +426,16 @@ def run_sweep(args):
                 for i in range(args.warmup):
                     call(i)
                 torch.cuda.synchronize()
-                s = torch.cuda.current_stream(dev)
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(s)
-                for i in range(args.steps):
-                    call(args.warmup + i)
-                e1.record(s)
-                torch.cuda.synchronize()
-                ms = e0.elapsed_time(e1) / args.steps
+                flush = in_bytes(w) <= 2 * L2_BYTES
+                per, total, _ = timed_steps(call, args.warmup, args.steps, torch.cuda.current_stream(dev), flush, dev)
+                ms = total / args.steps
                 alg = B * (V * es + ROW_PARAM_BYTES)
                 gbs = alg / (ms / 1e3) / 1e9
                 rows.append({"dtype": dt_name, "B": B, "V": V, "us_per_step": round(ms * 1e3, 2),
                              "rows_per_s": round(B / (ms / 1e3), 1), "gbs": round(gbs, 1),
                              "frac": round(gbs / peak, 4), "kernels": tps.kernels_per_call(dt, B, V, args.kernel),
-                             "l2": "larger than L2" if B * V * es > 129e6 else "fits L2 (re-read)"})
+                             "p50_us": round(statistics.median(per) * 1e3, 2),
+                             "l2": "flushed between steps" if flush else "larger than 2x L2 (back to back)"})
                 del w, out
                 torch.cuda.empty_cache()
     print(json.dumps({"sweep": rows, "kernel": args.kernel, "steps": args.steps, "warmup": args.warmup,
@@ -493,36 +520,7 @@ def main():
             i += 1
             if i % 64 == 0:
                 torch.cuda.synchronize()
-    # The timed steps are enqueued behind a short GPU spin, so the first event is recorded after the
-    # host has queued them: the region measures the device's time for the K steps, not the host's
-    # launch cadence (the e2e key times the host path).
-    torch.cuda._sleep(int(min(200e6, 2e6 * args.steps)))
-    flush = in_bytes(w) <= 2 * L2_BYTES
-    if not flush:  # back to back: each step reads inputs larger than L2
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-        t_wall0 = time.perf_counter()
-        ev[0].record(stream)
-        for i in range(args.steps):
-            step(args.warmup + i)
-            ev[i + 1].record(stream)
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall0
-        per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-        total_ms = ev[0].elapsed_time(ev[-1])
-    else:  # a write of 512 MB between steps pushes the inputs out of L2; each step is timed alone
-        scrub = torch.empty(128 << 20, dtype=torch.float32, device=dev)
-        ea = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        eb = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        t_wall0 = time.perf_counter()
-        for i in range(args.steps):
-            scrub.fill_(float(i))
-            ea[i].record(stream)
-            step(args.warmup + i)
-            eb[i].record(stream)
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall0
-        per = [ea[i].elapsed_time(eb[i]) for i in range(args.steps)]
-        total_ms = sum(per)
+    per, total_ms, t_wall = timed_steps(step, args.warmup, args.steps, stream, in_bytes(w) <= 2 * L2_BYTES, dev)
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop() if clocks else None

@@ -179,8 +179,8 @@ def test_edge_cases():
 
 
 def test_split_rows_every_outcome():
-    """Rows of 200,000 float32 logits are streamed as four segments merged by the CTA that finishes
-    a row last: every row status, greedy ties across segments, the maximum in any segment, min-p
+    """A batch of 48 rows (under four rows per SM) has each row of 200,000 float32 logits streamed
+    as six segments, merged by the CTA that finishes a row last: every row status, greedy ties across segments, the maximum in any segment, min-p
     rows, rows for the cluster kernel, and ragged, unaligned rows."""
     V, B = 200000, 48
     rng = np.random.default_rng(5)
