@@ -623,9 +623,11 @@ def sustained(args, step, stream, B, local, seconds=1.2):
 
 
 def latency_b1(args, dev, calls=300):
-    """B=1 latency at the same V and dtype (the decode distribution), two ways:
+    """B=1 latency at the same V and dtype (the decode distribution), three ways:
     - graph: one call captured in a CUDA graph and replayed back to back; the interval between
       consecutive events is the device time of one call (launch to completion, no host gap);
+    - in_graph: 20 calls captured in one graph, the replay's time per call (no graph launch per
+      call: what the call costs inside a captured decode step);
     - isolated: event, Python call, event, synchronize -- includes the host-side marshalling of the
       call, i.e. what one unbatched request sees end to end on an idle GPU."""
     import nucleus_token_sampler_gb300 as tps
@@ -673,6 +675,28 @@ def latency_b1(args, dev, calls=300):
         gt = [ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(calls)]
         out["p50_us"], out["p90_us"], out["p99_us"] = pct(gt)
         out["method"] = "CUDA graph replays back to back; events between replays"
+        # The same call inside a longer graph (as when a serving loop captures its whole decode step):
+        # 20 calls per graph, the replay's time divided by 20; median of 15 replays.
+        g20 = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            side.wait_stream(s)
+            with torch.cuda.graph(g20, stream=side):
+                for i in range(20):
+                    tps.sample(w.logits, w.temperature, w.top_k, w.top_p, w.min_p, w.seed, 20000 + i, out=tok)
+        s.wait_stream(side)
+        for _ in range(3):
+            g20.replay()
+        torch.cuda.synchronize()
+        per = []
+        for _ in range(15):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            g20.replay()
+            b.record(s)
+            b.synchronize()
+            per.append(a.elapsed_time(b) * 1e3 / 20)
+        out["in_graph_us"] = round(sorted(per)[len(per) // 2], 2)
+        out["in_graph_method"] = "20 calls captured in one CUDA graph; replay time / 20, median of 15 replays"
     except Exception as e:  # graph capture unavailable: report the isolated numbers only
         out["graph_error"] = str(e)[:200]
         out["p50_us"], out["p90_us"], out["p99_us"] = out["isolated_p50_us"], out["isolated_p90_us"], out["isolated_p99_us"]

@@ -21,7 +21,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kFineBins = 512;        // count bins over d, width 1/16 (last bin: d >= 511/16)
 constexpr float kFineScale = 16.f;
-constexpr int kRaceQueue = 64;        // per-warp queue of vectors with tokens to race
+constexpr int kRaceQueue = 96;        // per-warp queue of vectors with tokens to race
 constexpr int kSubBins = 128;         // sub-bins over a key interval (exact refinement)
 constexpr int kMaxWin = 32;           // groups of fine bins in a top-p window
 constexpr int kMaxTop = 32;           // top tokens a call may report per row
@@ -1544,28 +1544,43 @@ struct RaceAcc {
 };
 
 // Per-warp queue of vectors holding tokens to race, so that the Philox blocks and logarithms run
-// for full warps: a lane queues (vector, token mask) when it finds tokens to race, and every 32
-// queued vectors are raced one per lane.  Any lane may race any token: a token skipped against some
-// lane's second-best key cannot be among the two best of the row.
+// for full warps: a lane queues (vector, token mask) when it finds tokens to race, and every 64
+// queued vectors are raced two per lane, the first Philox block of each pair drawn together.  Any
+// lane may race any token: a token skipped against some lane's second-best key cannot be among the
+// two best of the row.
 template <typename Src>
 struct RaceQueue {
     uint32_t* q;  // this warp's kRaceQueue entries: vector | (mask << 24)
     uint32_t n;   // queued entries (the same in every lane)
     __device__ __forceinline__ explicit RaceQueue(Shared& s) : q(s.u.rq[threadIdx.x >> 5]), n(0) {}
+    __device__ __forceinline__ void race_vector(const Src& src, const RowCtx& r, const RaceCtx& rc, RaceAcc& race,
+                                                uint32_t e, uint4 x)
+    {
+        const int v = (int)(e & 0xFFFFFFu);
+        const uint32_t mask = e >> 24;
+        float z[Src::kEPV];
+        Elem<typename ElemOf<Src>::type>::unpack(src.load(v), z);
+        const int32_t i0 = (int32_t)src.elem0 + v * Src::kEPV;
+        race.ctr = (uint32_t)i0 >> 2;  // the block of the vector's first token, drawn by the caller
+        race.x = x;
+#pragma unroll
+        for (int j = 0; j < Src::kEPV; ++j)
+            if ((mask >> j) & 1u) race.add(rc, dist(r, z[j]), i0 + j);
+    }
+    // Races entries [0, cnt) (cnt <= 64): lane l takes entries l and l + 32.
     __device__ __forceinline__ void run(const Src& src, const RowCtx& r, const RaceCtx& rc, RaceAcc& race, uint32_t cnt)
     {
         const uint32_t lane = threadIdx.x & 31;
-        if (lane < cnt) {
-            const uint32_t e = q[lane];
-            const int v = (int)(e & 0xFFFFFFu);
-            const uint32_t mask = e >> 24;
-            float z[Src::kEPV];
-            Elem<typename ElemOf<Src>::type>::unpack(src.load(v), z);
-            const int32_t i0 = (int32_t)src.elem0 + v * Src::kEPV;
-#pragma unroll
-            for (int j = 0; j < Src::kEPV; ++j)
-                if ((mask >> j) & 1u) race.add(rc, dist(r, z[j]), i0 + j);
-        }
+        if (lane >= cnt) return;
+        const uint32_t e0 = q[lane];
+        const bool two = lane + 32u < cnt;
+        const uint32_t e1 = two ? q[lane + 32u] : e0;
+        const uint32_t c0 = (uint32_t)((int32_t)src.elem0 + (int)(e0 & 0xFFFFFFu) * Src::kEPV) >> 2;
+        const uint32_t c1 = (uint32_t)((int32_t)src.elem0 + (int)(e1 & 0xFFFFFFu) * Src::kEPV) >> 2;
+        uint4 x0 = make_uint4(c0, rc.row, rc.s_lo, rc.s_hi), x1 = make_uint4(c1, rc.row, rc.s_lo, rc.s_hi);
+        philox4x32_10_x2(x0, x1, rc.k0, rc.k1);
+        race_vector(src, r, rc, race, e0, x0);
+        if (two) race_vector(src, r, rc, race, e1, x1);
     }
     // Every lane calls this for its vector v (mask 0: nothing to race).
     __device__ __forceinline__ void push(const Src& src, const RowCtx& r, const RaceCtx& rc, RaceAcc& race, int v,
@@ -1576,13 +1591,13 @@ struct RaceQueue {
         if (bal == 0u) return;
         if (mask) q[n + __popc(bal & ((1u << lane) - 1u))] = (uint32_t)v | (mask << 24);
         n += __popc(bal);
-        if (n >= 32u) {
+        if (n >= 64u) {  // at most 63 + 32 < kRaceQueue entries
             __syncwarp();
-            run(src, r, rc, race, 32u);
+            run(src, r, rc, race, 64u);
             __syncwarp();
-            if (lane + 32u < n) q[lane] = q[lane + 32u];
+            if (lane + 64u < n) q[lane] = q[lane + 64u];
             __syncwarp();
-            n -= 32u;
+            n -= 64u;
         }
     }
     __device__ __forceinline__ void drain(const Src& src, const RowCtx& r, const RaceCtx& rc, RaceAcc& race)

@@ -30,6 +30,26 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
     return c;
 }
 
+// Two blocks at once, their rounds interleaved: each block's ten rounds are a chain of dependent
+// multiplies, so two independent chains keep the multiplier busy for twice the work in about the
+// same latency.  Bit for bit the same function as philox4x32_10 on each counter.
+__device__ __forceinline__ void philox4x32_10_x2(uint4& c, uint4& d, uint32_t k0, uint32_t k1)
+{
+    constexpr uint32_t kMulA = 0xD2511F53u, kMulB = 0xCD9E8D57u;
+    constexpr uint32_t kWeylA = 0x9E3779B9u, kWeylB = 0xBB67AE85u;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t a_hi = __umulhi(kMulA, c.x), a_lo = kMulA * c.x;
+        const uint32_t b_hi = __umulhi(kMulB, c.z), b_lo = kMulB * c.z;
+        const uint32_t e_hi = __umulhi(kMulA, d.x), e_lo = kMulA * d.x;
+        const uint32_t f_hi = __umulhi(kMulB, d.z), f_lo = kMulB * d.z;
+        c = make_uint4(b_hi ^ c.y ^ k0, b_lo, a_hi ^ c.w ^ k1, a_lo);
+        d = make_uint4(f_hi ^ d.y ^ k0, f_lo, e_hi ^ d.w ^ k1, e_lo);
+        k0 += kWeylA;
+        k1 += kWeylB;
+    }
+}
+
 // One block out of line: the race code that draws it stays small inside unrolled loops.
 static __device__ __noinline__ uint4 philox_block(uint4 c, uint32_t k0, uint32_t k1) { return philox4x32_10(c, k0, k1); }
 
