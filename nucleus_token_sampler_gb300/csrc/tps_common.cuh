@@ -924,18 +924,42 @@ __device__ __forceinline__ double race_key64(const RowCtx& r, float z, float u) 
 __device__ __forceinline__ float race_tol(float dcut) { return 1e-5f + 1e-6f * dcut; }
 
 // Refine the cut among the survivors (min-p, key >= key_lo) whose scaled distance d32 lies in the
-// fine bins [b_lo, b_end), given the (count, mass) of the survivors above that range.  Exact: ends with a sorted
-// candidate list or with a single logit value.  Starts with a topology barrier.
+// fine bins [b_lo, b_end), given the (count, mass) of the survivors above that range.  Exact: ends
+// with a sorted candidate list or with a single logit value.  Starts with a topology barrier.
+// Each round is one pass over the row: the survivors of the current key interval are counted,
+// listed (the first kCand) and histogrammed over kSubBins sub-intervals at once; a round with at
+// most kCand of them sorts the list (or finds a single class), otherwise the crossing sub-interval
+// becomes the next interval.  The first interval holds every logit whose distance can fall in the
+// fine bins (their bounds widened by a relative 1e-5, far above the float rounding of the
+// distance); the bin test itself stays exact.  Lanes of a warp holding the same key (a tie class)
+// add to the histogram once, together: a class of thousands of tied logits would otherwise queue
+// on one shared-memory address.  need_mass = false (a count criterion whose caller uses only the
+// key and the count) skips the fixed-point mass sums.
 template <typename Topo, typename Src>
 __device__ Sel refine_range(Topo& topo, Shared& s, const Src& sl, const RowCtx& r, float zc, int b_lo, int b_end,
-                            uint32_t key_lo, const Crit& cr, uint64_t C0, uint64_t A0)
+                            uint32_t key_lo, const Crit& cr, uint64_t C0, uint64_t A0, bool need_mass = true)
 {
     const uint32_t C = topo.C;
-    uint32_t klo = 0, khi = 0xFFFFFFFFu;
+    uint32_t klo, khi;
+    {
+        const float w_lo = (float)b_lo * (r.T / kFineScale), w_hi = (float)b_end * (r.T / kFineScale);
+        const float slack = 1e-5f * (fabsf(r.zmax) + w_hi) + 1e-30f;
+        khi = fkey(r.zmax - w_lo + slack);
+        klo = (b_end >= kFineBins) ? 0u : fkey(r.zmax - w_hi - slack);
+        if (!(isfinite(w_hi) && isfinite(slack))) klo = 0u;  // huge T: no useful lower bound
+        if (!isfinite(r.zmax - w_lo + slack)) khi = 0xFFFFFFFFu;
+        klo = max(klo, key_lo);
+    }
     bool by_range = true;
     for (int iter = 0; iter < 8; ++iter) {
-        // Gather the tokens of the current range (a level-1 bin, or a key interval).
         topo.sync();  // nobody still reads my candidate list, published counts or shares
+        int sh = 0;
+        while (khi >= klo && ((uint64_t)(khi - klo) >> sh) >= (uint64_t)kSubBins) ++sh;
+        const int nsub = (khi >= klo) ? (int)((uint64_t)(khi - klo) >> sh) + 1 : 1;
+        for (int b = threadIdx.x; b < kSubBins; b += kThreads) {
+            s.u.sh.hcnt[b] = 0;
+            s.u.sh.hmass[b] = 0;
+        }
         if (threadIdx.x == 0) s.ncand = 0;
         cta_sync();
         uint32_t lcnt = 0, lmin = 0xFFFFFFFFu, lmax = 0;
@@ -956,6 +980,14 @@ __device__ Sel refine_range(Topo& topo, Shared& s, const Src& sl, const RowCtx& 
                     s.ckey[slot] = key;
                     s.cidx[slot] = (uint32_t)i;
                 }
+            }
+            const uint32_t peers = __match_any_sync(__activemask(), key);  // this warp's lanes with this key
+            if ((threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1)) {
+                const uint32_t np = (uint32_t)__popc(peers);
+                const int sb = (int)((hi - key) >> sh);
+                atomicAdd(&s.u.sh.hcnt[sb], np);
+                if (need_mass)
+                    atomicAdd((unsigned long long*)&s.u.sh.hmass[sb], (unsigned long long)np * qmass_d(d));
             }
         });
         const uint32_t cnt = block_sum_u32(lcnt, s);
@@ -1008,29 +1040,7 @@ __device__ Sel refine_range(Topo& topo, Shared& s, const Src& sl, const RowCtx& 
             prefix_masses(s, r, n);
             return walk_classes(s, n, cr, C0, A0);
         }
-        // Too many: split the key range [gmin, gmax] into sub-bins (sub-bin 0 = largest keys).
-        klo = gmin;
-        khi = gmax;
-        by_range = false;
-        int sh = 0;
-        while (((uint64_t)(khi - klo) >> sh) >= (uint64_t)kSubBins) ++sh;
-        const int nsub = (int)((uint64_t)(khi - klo) >> sh) + 1;
-        for (int b = threadIdx.x; b < kSubBins; b += kThreads) {
-            s.u.sh.hcnt[b] = 0;
-            s.u.sh.hmass[b] = 0;
-        }
-        cta_sync();
-        const uint32_t lo2 = klo, hi2 = khi;
-        sl.for_each(s, [&](float z, int32_t) {
-            if (!(z > zc)) return;
-            const uint32_t key = fkey(z);
-            if (key < key_lo || key < lo2 || key > hi2) return;
-            const float d = dist(r, z);
-            if (!minp_ok(r, z, d)) return;
-            const int sb = (int)((hi2 - key) >> sh);
-            atomicAdd(&s.u.sh.hcnt[sb], 1u);
-            atomicAdd((unsigned long long*)&s.u.sh.hmass[sb], (unsigned long long)qmass_d(d));
-        });
+        // Too many: the sub-interval holding the crossing (sub-bin 0 = largest keys) is next.
         cluster_reduce_hist(topo, s, kSubBins);
         int jb;
         uint64_t c_at, a_at;
@@ -1038,13 +1048,14 @@ __device__ Sel refine_range(Topo& topo, Shared& s, const Src& sl, const RowCtx& 
         if (jb < 0) jb = 0;
         C0 = c_at;
         A0 = a_at;
-        const uint64_t top = (uint64_t)hi2 - ((uint64_t)jb << sh);
+        const uint64_t top = (uint64_t)hi - ((uint64_t)jb << sh);
         const uint64_t width = (uint64_t)1 << sh;
         const uint64_t bot = (top + 1 >= width) ? top + 1 - width : 0;
-        khi = (uint32_t)top;
-        klo = (uint32_t)max((uint64_t)lo2, bot);
+        khi = (uint32_t)min(top, (uint64_t)gmax);
+        klo = (uint32_t)max((uint64_t)max(lo, gmin), bot);
+        by_range = false;
     }
-    // Unreachable in practice (each split shrinks the 32-bit range by 2^7); keep a valid answer.
+    // Unreachable in practice (each round shrinks the 32-bit interval by 2^7); keep a valid answer.
     Sel o;
     o.key = khi;
     o.cnt = C0;
@@ -1822,7 +1833,7 @@ __device__ RowResult general_path(Topo& topo, Shared& s, const Src& src, const R
         ck2.by_mass = false;
         ck2.tcnt = (uint64_t)K;
         ck2.tmass = 0.0;
-        const Sel sk = refine_range(topo, s, src, r, zc, bk, bk + 1, 0u, ck2, ck, 0);
+        const Sel sk = refine_range(topo, s, src, r, zc, bk, bk + 1, 0u, ck2, ck, 0, false);
         key_k = sk.key;
         NS = sk.cnt;
         part = (uint32_t)(sk.cnt - ck);
@@ -2190,7 +2201,7 @@ __device__ __noinline__ void general_top(Topo& topo, Shared& s, const Src& src, 
         ck.by_mass = false;
         ck.tcnt = Kt;
         ck.tmass = 0.0;
-        const Sel sk = refine_range(topo, s, src, r, zc, bn, bn + 1, 0u, ck, cn, 0);
+        const Sel sk = refine_range(topo, s, src, r, zc, bn, bn + 1, 0u, ck, cn, 0, false);
         key_lo = sk.key;
         if (sk.cnt > (uint64_t)kCand) key_lo = sk.key + 1u;  // the tie class at sk.key is resolved below
     }
