@@ -180,8 +180,9 @@ def test_edge_cases():
 
 def test_split_rows_every_outcome():
     """A batch of 48 rows (under four rows per SM) has each row of 200,000 float32 logits streamed
-    as six segments, merged by the CTA that finishes a row last: every row status, greedy ties across segments, the maximum in any segment, min-p
-    rows, rows for the cluster kernel, and ragged, unaligned rows."""
+    as six segments, merged by the CTA that finishes a row last: every row status, greedy ties
+    across segments, the maximum in any segment, min-p rows, rows for the cluster kernel, and
+    ragged, unaligned rows."""
     V, B = 200000, 48
     rng = np.random.default_rng(5)
     z = rng.normal(0, 2.0, size=(B, V))

@@ -47,9 +47,11 @@ def _call(fn, d, out, n_top, kernel=0):
 
 @pytest.mark.parametrize("name", ["decode", "mixed"])
 def test_no_alloc_matches_the_pool_call(name):
-    """The decode batch (B = 1024 x 128,256; split tail rows merged through the scratch) and the mixed
-    batch (rows without min-p listed in the scratch for the cluster kernel): identical tokens, statuses,
-    kept sets and top tokens, log-probabilities within the parity tolerance, on two calls in a row."""
+    """The decode batch (B = 1024 x 128,256: whole rows claimed through the scratch's counter) and the
+    mixed batch (B = 64, under four rows per SM: every row split into segments whose partial results
+    merge through the scratch, and the rows without min-p listed there for the cluster kernel):
+    identical tokens, statuses, kept sets and top tokens, log-probabilities within the parity
+    tolerance, on two calls in a row."""
     lib = tps.load()
     w = workloads.make(name, device="cpu")
     d = w.to("cuda")
