@@ -179,3 +179,52 @@ def test_caller_output_buffers_are_checked():
     top = torch.empty((8, 4), dtype=torch.int32)  # a buffer kept from a call with fewer top tokens
     with pytest.raises(ValueError):
         tps._out({"top_idx": top}, "top_idx", (8, 8), torch.int32, dev)
+
+
+def test_spec_accept_checks_its_arguments():
+    lib = tps.load()
+    v = lambda p: None if p is None else ctypes.c_void_p(p)
+
+    def call(B=4, V=100, ld=100, dtype=0, zt=FAKE, zd=FAKE, tp=FAKE, dp=FAKE, x=FAKE, S=FAKE, out=FAKE, acc=None):
+        return lib.tps_spec_accept(v(zt), v(zd), dtype, B, V, ld, v(tp), v(tp), v(tp), v(tp), v(dp), v(dp), v(dp),
+                                   v(dp), v(x), v(S), 0, v(out), v(acc), None, None)
+    assert call(B=-1) == 1 and call(V=0) == 1 and call(ld=99) == 1
+    assert call(dtype=7) == 2
+    assert call(B=0, zt=None, zd=None, tp=None, dp=None, x=None, S=None, out=None) == 0  # nothing to do
+    for kw in ("zt", "zd", "tp", "dp", "x", "S", "out"):
+        assert call(**{kw: None}) == 1, kw                     # a required pointer is missing
+    assert call(zd=FAKE + 2) == 4                              # misaligned draft logits
+    assert call(x=FAKE + 1) == 4                               # misaligned draft tokens
+    assert call(S=FAKE + 4) == 4                               # seeds are 8-byte words
+    assert call(acc=FAKE + 2) == 4                             # misaligned optional output
+    assert call(V=1 << 20, ld=1 << 20) == 3                    # above the exact-mass vocabulary bound
+
+
+def test_sample_rejection_checks_its_arguments():
+    lib = tps.load()
+    v = lambda p: None if p is None else ctypes.c_void_p(p)
+
+    def call(B=4, V=100, ld=100, dtype=0, z=FAKE, p=FAKE, S=FAKE, out=FAKE, rounds=None):
+        return lib.tps_sample_rejection(v(z), dtype, B, V, ld, v(p), v(p), v(p), v(p), v(S), 0, v(out), None, None,
+                                        None, v(rounds), None)
+    assert call(B=-1) == 1 and call(V=0) == 1 and call(ld=99) == 1
+    assert call(dtype=3) == 2
+    assert call(B=0, z=None, p=None, S=None, out=None) == 0
+    for kw in ("z", "p", "S", "out"):
+        assert call(**{kw: None}) == 1, kw
+    assert call(z=FAKE + 2) == 4 and call(rounds=FAKE + 1) == 4
+    assert call(V=1 << 20, ld=1 << 20) == 3
+
+
+def test_stall_test_hook_checks_its_wait_limit():
+    """The test hook takes a consumer-side wait limit of 1 ns .. 1 s; anything else is refused before
+    the sampling call's own checks."""
+    lib = tps.load()
+    v = lambda p: None if p is None else ctypes.c_void_p(p)
+
+    def call(wait_ns, dtype=0, B=4):
+        return lib.tps_sample_stall_test(v(FAKE), dtype, B, 100, v(FAKE), v(FAKE), v(FAKE), v(FAKE), v(FAKE), 0,
+                                         v(FAKE), None, 0, wait_ns, None)
+    assert call(0) == 1 and call(10**9 + 1) == 1
+    assert call(1000, dtype=9) == 2          # then the sampling call's checks
+    assert call(1000, B=0) == 0
